@@ -1,0 +1,168 @@
+/*
+ * moe.h — C ABI of a single-GPU dropless token-choice MoE layer (forward and
+ * backward) for NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute (sources: page title, section):
+ *   moe_route           logits z = x W_g^T (+ bias), p = softmax(z), the K largest
+ *                       experts per token, weights renormalised over the chosen K.
+ *                       [MoEBlaze paper notes 2.1 "gating network"; Dropless MoE,
+ *                       in depth, "A reference implementation"]
+ *   moe_build_dispatch  expert_token_indices, expert_token_offsets and
+ *                       token_index_map of the routing, built without a global
+ *                       sort and without contended atomics.
+ *                       [MoEBlaze paper notes 4.1 data structures, 4.2 build]
+ *   moe_forward         per expert: a = x W1^T, b = x W3^T, A = SiLU(a) * b,
+ *                       Y = A W2^T, read through expert_token_indices (no routed
+ *                       copy of x); y_t = sum_k w_{t,k} Y_{t,k}.
+ *                       [MoEBlaze paper notes 2.3, 5.1, Algorithm 1; SonicMoE 3.4.1]
+ *   moe_backward        dx, dW_g, dW1, dW3, dW2 and the router-score gradient
+ *                       dS_{t,k} = <dO_t, Y_{t,k}> (computed as <dO W2, A>).
+ *                       [MoEBlaze paper notes 3.2, Algorithm 1; SonicMoE 3.4.1]
+ *
+ * Conventions for every call
+ *   - Shapes: T tokens, d model width, E experts, K experts per token, h expert
+ *     hidden width. TK = T*K.
+ *   - All pointers are DEVICE pointers (cudaMalloc or equivalent), except where
+ *     a comment says otherwise. bf16 arrays are passed as void* and hold IEEE
+ *     bfloat16 values. All arrays are dense, row-major, 16-byte aligned.
+ *   - x, dy, y, dx: [T, d] bf16. W_g, dW_g: [E, d] fp32. bias: [E] fp32.
+ *     W1, W3, dW1, dW3: [E, h, d] bf16. W2, dW2: [E, d, h] bf16 (out x in).
+ *     topk_ids: [T, K] int32, slot 0 = largest weight. topk_w, dS: [T, K] fp32.
+ *     expert_token_indices, token_index_map: [TK] int32. offsets: [E+1] int32.
+ *     H_saved: [TK, 2h] bf16, row r = (a | b) of the r-th expert-sorted row.
+ *   - Ownership: the caller allocates and owns every buffer and the workspace.
+ *     The library allocates no device memory and keeps no state between calls
+ *     other than the optional kernel timer below.
+ *   - Execution: every call enqueues kernels on `stream` (a cudaStream_t; NULL
+ *     means the legacy default stream) and returns without waiting. Per-expert
+ *     counts never leave the device. Workspace contents need not survive
+ *     between calls.
+ *   - Errors: a call returns MOE_OK or a status code. Arguments that the host
+ *     can check (null pointers, unsupported shapes, misalignment, workspace too
+ *     small) are rejected before anything is launched. Errors that only the
+ *     device can see (an expert id out of range or repeated within a token, a
+ *     bounded wait that ran out) set a sticky device status word; kernels that
+ *     start after it is set do nothing, and moe_get_error() reports it.
+ *     No call traps or aborts the process.
+ *   - Supported shapes: 1 <= T <= 2^24, 1 <= K <= 8, K <= E <= 256,
+ *     d and h multiples of 128, d, h <= 32768, TK * 2h < 2^31 elements is NOT
+ *     required (64-bit addressing is used throughout).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int32_t T, d, E, K, h;
+} moe_shape;
+
+enum moe_status_code {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null pointer or negative size            */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* outside the supported shapes above       */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_size(...)       */
+    MOE_ERR_CUDA = 4,                /* a CUDA runtime call failed               */
+    MOE_ERR_BAD_EXPERT_ID = 5,       /* device: id out of [0,E) or repeated      */
+    MOE_ERR_TIMEOUT = 6,             /* device: a bounded wait ran out           */
+    MOE_ERR_MISALIGNED = 7,          /* a pointer is not 16-byte aligned         */
+    MOE_ERR_NO_DEVICE = 8            /* no usable sm_100-family device           */
+};
+
+enum moe_workspace_kind {
+    MOE_WS_ROUTE = 0,
+    MOE_WS_DISPATCH = 1,
+    MOE_WS_FORWARD = 2,
+    MOE_WS_BACKWARD = 3
+};
+
+/* Bytes of device workspace that the call `which` needs for shape s (0 if the
+ * shape is unsupported). Pure host function. */
+size_t moe_workspace_size(moe_shape s, int which);
+
+/* Tokens per combine chunk: moe_forward and moe_backward run the down
+ * projection (and the dX of the up projection) over token chunks of this many
+ * tokens, so the transient expert-output buffer holds chunk*K*d elements, at
+ * most a quarter of T*K*d once T >= 1024. Pure host function. */
+int moe_chunk_tokens(moe_shape s);
+
+/* Router. x [T,d] bf16, Wg [E,d] fp32, bias [E] fp32 or NULL.
+ * Outputs: logits [T,E] fp32 (NULL to skip), topk_ids [T,K] int32 (descending
+ * weight, ties to the lower id), topk_w [T,K] fp32 (sum to 1 per token).
+ * Selection is on the fp32 logits z + bias; weights are exp(z_k - z_max)
+ * normalised over the chosen K (equal to the renormalised softmax). */
+int moe_route(moe_shape s, const void* x, const float* Wg, const float* bias,
+              float* logits, int32_t* topk_ids, float* topk_w,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch index from topk_ids [T,K] int32.
+ * Outputs: expert_token_indices [TK] (token ids grouped by expert, ascending
+ * token inside an expert), expert_token_offsets [E+1] (exclusive prefix of the
+ * per-expert counts, offsets[E] = TK), token_index_map [TK] (position of
+ * assignment (t,k) in expert_token_indices, at index t*K+k).
+ * Bit-exact with a stable sort of the flattened ids by expert. Invalid ids set
+ * MOE_ERR_BAD_EXPERT_ID on the device; the outputs are then undefined. */
+int moe_build_dispatch(moe_shape s, const int32_t* topk_ids,
+                       int32_t* expert_token_indices, int32_t* expert_token_offsets,
+                       int32_t* token_index_map, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward. Inputs: x, W1, W3, W2, the routing (topk_ids, topk_w) and its
+ * dispatch index. Outputs: y [T,d] bf16 and H_saved [TK,2h] bf16 (the
+ * pre-activations kept for the backward; SiLU is recomputed there).
+ * No [TK,d] copy of the routed tokens is made: expert rows are gathered from x
+ * through expert_token_indices by the GEMM's loads. */
+int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, const void* W2,
+                const int32_t* topk_ids, const float* topk_w,
+                const int32_t* expert_token_indices, const int32_t* expert_token_offsets,
+                const int32_t* token_index_map,
+                void* y, void* H_saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward with upstream gradient dy [T,d] bf16. Outputs: dx [T,d] bf16
+ * (expert and router paths), dWg [E,d] fp32, dW1, dW3 [E,h,d] bf16,
+ * dW2 [E,d,h] bf16 (an expert with no tokens gets exact zeros) and
+ * dS [T,K] fp32 = <dy_t, Y_{t,k}>. Gradients are written, not accumulated. */
+int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg,
+                 const void* W1, const void* W3, const void* W2,
+                 const int32_t* topk_ids, const float* topk_w,
+                 const int32_t* expert_token_indices, const int32_t* expert_token_offsets,
+                 const int32_t* token_index_map, const void* H_saved,
+                 void* dx, float* dWg, void* dW1, void* dW3, void* dW2, float* dS,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for `stream`, then returns and clears the device status word of the
+ * current device (MOE_OK if no device-side error happened since the last
+ * call). The only call that blocks the host. */
+int moe_get_error(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* ---- Instrumentation (host-side; off by default) ------------------------ */
+
+/* Number of kernels this library has launched in this process. */
+long long moe_launch_count(void);
+
+/* When on, every kernel launch is bracketed by two CUDA events on its stream
+ * (recorded, not waited on). Turning it on clears earlier records. */
+int moe_timing_enable(int on);
+
+typedef struct {
+    char name[32];
+    int32_t launches;
+    double total_ms;
+} moe_kernel_time;
+
+/* Waits for the recorded events and fills up to `max` entries (one per
+ * kernel name, in first-launch order). Returns the number of names, or a
+ * negative status. */
+int moe_timing_collect(moe_kernel_time* out, int max);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

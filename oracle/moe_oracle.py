@@ -314,6 +314,13 @@ def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
     out_y = np.zeros((len(tokens), d))
     out_dS = np.zeros((len(tokens), K))
     out_dx = np.zeros((len(tokens), d))
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            cache[e] = (_as64(W1[e]), _as64(W3[e]), _as64(W2[e]))
+        return cache[e]
+
     for i, t in enumerate(tokens):
         xt = _as64(x[t])
         dOt = _as64(dO[t])
@@ -321,7 +328,7 @@ def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
         dx_e = np.zeros(d)
         for k in range(K):
             e = int(ids[t, k])
-            W1e, W3e, W2e = _as64(W1[e]), _as64(W3[e]), _as64(W2[e])
+            W1e, W3e, W2e = expert(e)
             a = W1e @ xt
             b = W3e @ xt
             A = silu(a) * b
@@ -354,11 +361,11 @@ def hidden_unit_grads(e: int, j: int, x, dO, W1, W3, W2, ids, w):
         return np.zeros(d), np.zeros(d), np.zeros(d)
     xe = _as64(x[sel_t])
     dY = w[sel_t, sel_k][:, None] * _as64(dO[sel_t])
-    W2e = _as64(W2[e])
+    W2e_j = _as64(W2[e][:, j])
     a = xe @ _as64(W1[e][j])
     b = xe @ _as64(W3[e][j])
     A = silu(a) * b
-    dA = dY @ W2e[:, j]
+    dA = dY @ W2e_j
     da = dA * b * silu_grad(a)
     db = dA * silu(a)
     return da @ xe, db @ xe, dY.T @ A

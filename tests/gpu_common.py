@@ -1,0 +1,30 @@
+"""Helpers shared by the GPU parity tests (no arithmetic of the layer here)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Tolerances: indices bit-exact; fp32 router logits / weights within relative
+# Frobenius 1e-5; bf16 outputs and gradients within relative Frobenius 1e-2 of
+# the fp64 oracle.
+TOL_ROUTER = 1e-5
+TOL_BF16 = 1e-2
+GAP = 1e-3      # router ids are compared where the deciding logit gap exceeds this
+
+
+def rel_fro(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def cpu(t) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        t = t.float()
+    return t.numpy()
+
+
+def to_dev(d: dict, device="cuda") -> dict:
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}

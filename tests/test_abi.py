@@ -1,0 +1,69 @@
+"""The C-ABI library builds, loads and exports every symbol that include/*.h
+declares; its pure host functions behave as documented. No compute calls."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from token_dispatch_grouped_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "moe_route" in names and "moe_backward" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_functions():
+    from token_dispatch_grouped_gb300 import binding as B
+    s = B.shape(4096, 4096, 8, 2, 14336)
+    assert B.moe_chunk_tokens(s) == 1024
+    fwd = B.moe_workspace_size(s, B.MOE_WS_FORWARD)
+    # the forward workspace holds the SwiGLU output [TK, h] and one Y chunk of
+    # chunk*K*d elements -- a quarter of the T*K*d routed buffer
+    TK = 4096 * 2
+    assert fwd >= TK * 14336 * 2 + 1024 * 2 * 4096 * 2
+    assert fwd < TK * 14336 * 2 + 4096 * 2 * 4096 * 2 // 2
+    assert B.moe_workspace_size(s, B.MOE_WS_ROUTE) == 0
+    for bad in (B.shape(0, 128, 8, 2, 128), B.shape(8, 100, 8, 2, 128), B.shape(8, 128, 4, 5, 128),
+                B.shape(8, 128, 300, 2, 128), B.shape(8, 128, 16, 9, 128)):
+        assert B.moe_workspace_size(bad, B.MOE_WS_FORWARD) == 0
+    assert B.status_string(B.MOE_ERR_BAD_EXPERT_ID).startswith("expert id")
+
+
+def test_null_pointers_rejected_before_any_device_work():
+    from token_dispatch_grouped_gb300 import binding as B
+    s = B.shape(16, 128, 8, 2, 128)
+    assert B.LIB.moe_route(s, None, None, None, None, None, None, None, 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_build_dispatch(s, None, None, None, None, None, 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    bad = B.shape(16, 128, 8, 9, 128)
+    assert B.LIB.moe_route(bad, None, None, None, None, None, None, None, 0, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_oracle_is_not_imported_by_the_product():
+    pkg = os.path.join(ROOT, "token_dispatch_grouped_gb300")
+    for py in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
+        src = open(py).read()
+        assert "oracle" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", src, flags=re.M), py

@@ -1,0 +1,238 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Small and ragged shapes are compared element by element; the full workloads are
+compared on sampled tokens and hidden units (the oracle evaluates those one by
+one) and on properties that hold at any size."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from tests.gpu_common import GAP, TOL_BF16, TOL_ROUTER, cpu, rel_fro, to_dev
+from token_dispatch_grouped_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _layer(s):
+    from token_dispatch_grouped_gb300.layer import MoELayer
+    return MoELayer(s.T, s.d, s.E, s.K, s.h)
+
+
+def _check_route(z_gpu, ids_gpu, w_gpu, x, Wg, K, bias, rows=None):
+    xs = x if rows is None else x[rows]
+    z, p, ids, w = O.route(xs, Wg, K, None if bias is None else bias)
+    zg = cpu(z_gpu) if rows is None else cpu(z_gpu)[rows]
+    ig = cpu(ids_gpu) if rows is None else cpu(ids_gpu)[rows]
+    wg = cpu(w_gpu) if rows is None else cpu(w_gpu)[rows]
+    assert rel_fro(zg, z) <= TOL_ROUTER
+    sure = O.topk_gap(z, K) > GAP
+    assert sure.mean() > 0.5
+    assert np.array_equal(ig[sure], ids[sure])
+    assert rel_fro(wg[sure], w[sure]) <= TOL_ROUTER
+    assert np.allclose(wg.sum(axis=1), 1.0, atol=1e-5)
+
+
+def _check_dispatch(ids_gpu, dp, E):
+    eti, off, tim, counts = O.build_dispatch(cpu(ids_gpu), E)
+    assert np.array_equal(cpu(dp.eti), eti)
+    assert np.array_equal(cpu(dp.offsets), off)
+    assert np.array_equal(cpu(dp.tim), tim)
+
+
+SMALL = [
+    I.WORKLOADS["tiny"],
+    I.Shape(300, 256, 6, 3, 384),     # ragged tiles, h % 256 != 0 (128-wide N tiles)
+    I.Shape(1, 128, 4, 4, 128),       # one token, K = E
+    I.Shape(1500, 128, 16, 1, 256),   # K = 1 (router gradient is zero), 4 token chunks
+    I.Shape(129, 384, 8, 8, 128),     # K = E = 8
+]
+
+
+@pytest.mark.parametrize("s", SMALL, ids=lambda s: f"T{s.T}d{s.d}E{s.E}K{s.K}h{s.h}")
+def test_layer_small_full_parity(s):
+    inp = I.make_layer_inputs(s, seed=1)
+    dv = to_dev(inp)
+    L = _layer(s)
+    r, dp, y, H, g = L.step(dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], dv["dO"])
+    L.check_error()
+    _check_route(r.logits, r.ids, r.w, inp["x"], inp["Wg"], s.K, None)
+    _check_dispatch(r.ids, dp, s.E)
+    # Layer parity on the GPU's own routing (ids and fp32 weights as inputs).
+    ids, w = cpu(r.ids), cpu(r.w)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f)
+    assert rel_fro(cpu(H), f["H"]) <= TOL_BF16
+    assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
+    assert rel_fro(cpu(g["dS"]), b["dS"]) <= TOL_BF16
+    for k in ("dx", "dW1", "dW3", "dW2"):
+        assert rel_fro(cpu(g[k]), b[k]) <= TOL_BF16, k
+    if s.K == 1:
+        assert np.all(cpu(g["dWg"]) == 0.0)
+    else:
+        assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
+
+
+def test_injected_routing_skewed_and_empty_experts():
+    s = I.Shape(700, 256, 16, 4, 256)
+    inp = I.make_layer_inputs(s, seed=2)
+    ids = I.random_ids(s.T, 12, s.K, seed=5, skew=1.5)      # experts 12..15 get no token
+    w = I.random_weights(s.T, s.K, seed=5)
+    dv = to_dev(inp)
+    L = _layer(s)
+    from token_dispatch_grouped_gb300.layer import Routing
+    r = Routing(None, ids.cuda(), w.cuda())
+    dp = L.dispatch(r.ids)
+    y, H = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp)
+    grads = L.alloc_grads()
+    for t in grads.values():                                 # poison: every element must be written
+        t.fill_(float("nan"))
+    L.backward(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r, dp, H, grads)
+    L.check_error()
+    _check_dispatch(r.ids, dp, s.E)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f)
+    assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
+    for k in ("dx", "dW1", "dW3", "dW2", "dS", "dWg"):
+        assert not np.isnan(cpu(grads[k])).any(), k
+        assert rel_fro(cpu(grads[k]), b[k]) <= TOL_BF16, k
+    for k in ("dW1", "dW3", "dW2"):
+        assert np.all(cpu(grads[k])[12:] == 0.0)
+
+
+def test_fig2_worked_example_on_gpu():
+    with open(os.path.join(GOLD, "moeblaze_fig2.json")) as f:
+        g = json.load(f)
+    s = I.Shape(5, 128, g["E"], g["K"], 128)
+    L = _layer(s)
+    ids = torch.tensor(g["assignments"], dtype=torch.int32, device="cuda")
+    dp = L.dispatch(ids)
+    L.check_error()
+    assert cpu(dp.eti).tolist() == g["expert_token_indices"]
+    assert cpu(dp.offsets).tolist() == g["expert_token_offsets"]
+    assert cpu(dp.tim)[:2].tolist() == g["token_index_map_token0"]
+
+
+@pytest.mark.parametrize("case", ["all_to_one", "two_experts", "ragged_blocks", "skew"])
+def test_dispatch_adversarial(case):
+    if case == "all_to_one":
+        T, E, K = 1000, 8, 1
+        ids = torch.full((T, K), 3, dtype=torch.int32)
+    elif case == "two_experts":
+        T, E, K = 777, 64, 2
+        ids = torch.tensor([[5, 60]] * T, dtype=torch.int32)
+    elif case == "ragged_blocks":
+        T, E, K = 513, 256, 8
+        ids = I.random_ids(T, E, K, seed=9)
+    else:
+        T, E, K = 5000, 128, 6
+        ids = I.random_ids(T, E, K, seed=3, skew=2.0)
+    s = I.Shape(T, 128, E, K, 128)
+    L = _layer(s)
+    dp = L.dispatch(ids.cuda())
+    L.check_error()
+    _check_dispatch(ids, dp, E)
+
+
+def test_bad_expert_ids_raise_device_error():
+    from token_dispatch_grouped_gb300 import binding as B
+    s = I.Shape(64, 128, 8, 2, 128)
+    L = _layer(s)
+    B.moe_get_error()
+    ids = I.random_ids(64, 8, 2, seed=1)
+    ids[10, 1] = 8                                   # out of range
+    L.dispatch(ids.cuda())
+    assert B.moe_get_error() == B.MOE_ERR_BAD_EXPERT_ID
+    ids = I.random_ids(64, 8, 2, seed=1)
+    ids[3, 1] = ids[3, 0]                            # repeated within a token
+    L.dispatch(ids.cuda())
+    assert B.moe_get_error() == B.MOE_ERR_BAD_EXPERT_ID
+    assert B.moe_get_error() == B.MOE_OK             # the word was cleared
+
+
+def test_host_checks_reject_bad_calls():
+    from token_dispatch_grouped_gb300 import binding as B
+    s = B.shape(64, 128, 8, 2, 128)
+    ids = torch.zeros(64, 2, dtype=torch.int32, device="cuda")
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    out = torch.empty(128, dtype=torch.int32, device="cuda")
+    rc = B.moe_build_dispatch(s, ids, out, out, out, small, check=False)
+    assert rc == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert B.moe_workspace_size(B.shape(64, 100, 8, 2, 128), 2) == 0   # d % 128 != 0
+    x = torch.empty(64 * 128 + 1, dtype=torch.bfloat16, device="cuda")[1:]
+    Wg = torch.empty(8, 128, device="cuda")
+    w = torch.empty(64, 2, device="cuda")
+    assert B.moe_route(s, x, Wg, None, None, ids, w, check=False) == B.MOE_ERR_MISALIGNED
+
+
+def test_determinism_bitwise():
+    s = I.Shape(1200, 256, 8, 2, 512)
+    inp = to_dev(I.make_layer_inputs(s, seed=4))
+    L = _layer(s)
+    outs = []
+    for _ in range(2):
+        r, dp, y, H, g = L.step(inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], inp["dO"])
+        outs.append([t.clone() for t in (r.ids, r.w, dp.eti, dp.tim, y, H, *g.values())])
+    L.check_error()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full workloads
+def _full(name):
+    s = I.WORKLOADS[name]
+    inp = I.make_layer_inputs(s, seed=0, with_bias=(name == "skew"))
+    if name == "skew":
+        assert inp["bias"] is not None
+    dv = to_dev(inp)
+    L = _layer(s)
+    bias = dv["bias"]
+    r = L.route(dv["x"], dv["Wg"], bias)
+    dp = L.dispatch(r.ids)
+    y, H = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp)
+    g = L.backward(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r, dp, H)
+    L.check_error()
+    return s, inp, r, dp, y, H, g
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral", "fine", "skew", "long"])
+def test_full_workload_sampled(name):
+    s, inp, r, dp, y, H, g = _full(name)
+    rng = np.random.default_rng(0)
+    toks = np.sort(rng.choice(s.T, size=6, replace=False))
+    toks[-1] = s.T - 1
+    bias = inp["bias"]
+    _check_route(r.logits, r.ids, r.w, inp["x"], inp["Wg"], s.K, bias, rows=toks)
+    ids, w = cpu(r.ids), cpu(r.w)
+    _check_dispatch(r.ids, dp, s.E)
+    counts = np.diff(cpu(dp.offsets))
+    if name == "skew":
+        assert (counts == 0).sum() >= 4
+    ys, dSs, dxs = O.tokens_forward_backward(toks, inp["x"], inp["dO"], inp["Wg"], inp["W1"],
+                                             inp["W3"], inp["W2"], ids, w)
+    assert rel_fro(cpu(y)[toks], ys) <= TOL_BF16
+    assert rel_fro(cpu(g["dS"])[toks], dSs) <= TOL_BF16
+    assert rel_fro(cpu(g["dx"])[toks], dxs) <= TOL_BF16
+    # weight gradients on sampled (expert, hidden unit) pairs
+    busy = np.nonzero(counts > 0)[0]
+    for e in rng.choice(busy, size=min(2, len(busy)), replace=False):
+        j = int(rng.integers(0, s.h))
+        g1, g3, g2 = O.hidden_unit_grads(int(e), j, inp["x"], inp["dO"], inp["W1"], inp["W3"],
+                                         inp["W2"], ids, w)
+        assert rel_fro(cpu(g["dW1"][e, j]), g1) <= TOL_BF16
+        assert rel_fro(cpu(g["dW3"][e, j]), g3) <= TOL_BF16
+        assert rel_fro(cpu(g["dW2"][e, :, j]), g2) <= TOL_BF16
+    # properties at any size: dW_g rows sum to zero over experts (sum_k dz_k = 0),
+    # empty experts have exact-zero weight gradients, outputs are finite
+    dWg = cpu(g["dWg"])
+    assert np.abs(dWg.sum(axis=0)).max() <= 1e-3 * max(1e-30, np.abs(dWg).max())
+    for e in np.nonzero(counts == 0)[0]:
+        assert not cpu(g["dW1"][e]).any() and not cpu(g["dW2"][e]).any()
+    for t in (y, g["dx"]):
+        assert torch.isfinite(t).all()

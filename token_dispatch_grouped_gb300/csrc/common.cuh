@@ -1,0 +1,104 @@
+// common.cuh — shared internals of the MoE library: device status word,
+// launch bookkeeping, tensor-map encoding and the kernel launchers' signatures.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Device status word layout: the first error code that was raised wins.
+__device__ __forceinline__ void raise_error(int* err, int code) {
+    atomicCAS(err, 0, code);
+}
+__device__ __forceinline__ bool has_error(const int* err) {
+    return *reinterpret_cast<const volatile int*>(err) != 0;
+}
+
+// Per-row segment of one expert inside the expert-sorted row space:
+// rows [lo, hi) of A's row space; `out` is the output row of `lo` (used by the
+// chunked down projection; equal to lo otherwise).
+struct Seg {
+    int lo, hi, out, pad;
+};
+
+// Launch bookkeeping: counts launches and (optionally) brackets them with
+// events. Implemented in api.cu.
+struct LaunchScope {
+    LaunchScope(const char* name, cudaStream_t st);
+    ~LaunchScope();
+    const char* name_;
+    cudaStream_t st_;
+    int slot_;
+};
+
+// Tensor map of a 2D row-major bf16 array [rows, cols] with a box of
+// box_cols x box_rows and 128-byte swizzle. Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows);
+
+int num_sms();
+
+// ---------------------------------------------------------------- launchers
+// Every launcher enqueues on `st` and returns a cudaError_t of the launch.
+
+// router.cu
+cudaError_t launch_router(const moe_shape& s, const __nv_bfloat16* x, const float* Wg,
+                          const float* bias, float* logits, int32_t* ids, float* w, int* err,
+                          cudaStream_t st);
+
+// dispatch.cu
+int dispatch_block_tokens();
+cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
+                            int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
+                            cudaStream_t st);
+
+// misc.cu
+cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchunks,
+                                  const int32_t* eti, const int32_t* offsets, Seg* segs, int* err,
+                                  cudaStream_t st);
+cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const int32_t* tim,
+                               float* wrow, int* err, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
+                           const float* topk_w, const int32_t* tim, const Seg* seg,
+                           const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st);
+cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
+                             const float* topk_w, const int32_t* tim, float* dS, float* dz,
+                             int* err, cudaStream_t st);
+cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
+                              const float* dz, const int32_t* tim, const Seg* seg,
+                              const __nv_bfloat16* dXc, const float* Wg, __nv_bfloat16* dx,
+                              int* err, cudaStream_t st);
+int dwg_token_chunk();
+cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* ids,
+                              const float* dz, float* part, float* dWg, int* err,
+                              cudaStream_t st);
+
+// gemm.cu — the grouped tcgen05 GEMMs.
+enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5 };
+
+struct GemmProblem {
+    GemmKind kind;
+    moe_shape s;
+    const Seg* segs;          // [E] rows of each expert (VM: this chunk's rows)
+    const int32_t* eti;       // expert_token_indices (gather rows)
+    // operands (bf16 unless noted)
+    const void* a_src;        // x (G1) | A_act (G2) | dy (G3) | dy (G4) | dH (G5) | dH (G6)
+    const void* b_src0;       // W1 (G1) | W2 (G2) | W2 (G3) | A' (G4) | x (G5) | W1 (G6)
+    const void* b_src1;       // W3 (G1, G6)
+    // epilogue
+    void* out0;               // H (G1) | Yc (G2) | dH (G3) | dW2 (G4) | dW1 (G5) | dXc (G6)
+    void* out1;               // A_act (G1) | A' (G3) | dW3 (G5)
+    const void* aux0;         // H (G3)
+    const float* wrow;        // per-row routing weight (G3)
+    float* dS_part;           // [h/BN][TK] (G3)
+    int* err;
+};
+cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t st);
+int gemm_bn(GemmKind kind, const moe_shape& s);
+
+}  // namespace moe

@@ -1,0 +1,190 @@
+// dispatch.cu — D1..D3: the dispatch index without a global sort and without
+// contended atomics.
+//
+// Outputs (MoEBlaze paper notes 4.1, data structures of Figure 2):
+//   expert_token_indices [TK]  token ids grouped by expert, ascending token
+//                              order inside each expert
+//   expert_token_offsets [E+1] exclusive prefix of the per-expert counts
+//   token_index_map      [TK]  position of assignment (t, k), at t*K + k
+// The build follows the three-step, atomic-free idea of MoEBlaze paper notes
+// 4.2 (count per expert, prefix-sum into offsets, then conflict-free writes to
+// precomputed positions), but replaces the dense L x E token map with
+// per-block histograms:
+//   D1  one CTA per block of 256 tokens. Each warp owns 32 tokens (one per
+//       lane). For each slot k, __match_any_sync groups the lanes that chose
+//       the same expert; the group's leader ORs the group's lane mask into the
+//       warp's per-expert mask in shared memory (one writer per address, no
+//       atomics). popc of the masks gives the block's per-expert counts.
+//   D2  one CTA: exclusive scan of the counts over blocks for every expert
+//       (block bases), then over experts (offsets).
+//   D3  one CTA per block again: rebuilds the warp masks; the in-block rank of
+//       (t, k) is the number of lower lanes in its warp's mask plus the counts
+//       of earlier warps; position = offsets[e] + base[block][e] + rank. This
+//       is exactly the order of a stable sort of the flattened ids by expert.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBlockTokens = 256;
+constexpr int kWarps = kBlockTokens / 32;
+constexpr int kMaxE = 256;
+constexpr int kScanThreads = 1024;
+
+// Builds masks[w][e] (bit l set when lane l of warp w chose expert e) for the
+// block `blk`. Flags ids out of range or repeated within a token.
+__device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int T, int E, int K,
+                                            int blk, uint32_t (*masks)[kMaxE], int* err,
+                                            int (&my_e)[8]) {
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    for (int i = threadIdx.x; i < kWarps * kMaxE; i += blockDim.x) (&masks[0][0])[i] = 0u;
+    __syncthreads();
+    const int t = blk * kBlockTokens + warp * 32 + lane;
+    const bool valid = t < T;
+    bool bad = false;
+    for (int k = 0; k < K; ++k) {
+        int e = valid ? ids[static_cast<size_t>(t) * K + k] : -1;
+        if (valid) {
+            bool dup = false;
+            for (int j = 0; j < k; ++j) dup |= (my_e[j] == e);
+            if (e < 0 || e >= E || dup) {
+                bad = true;
+                e = -1;
+            }
+        }
+        my_e[k] = e;
+        const uint32_t m = __match_any_sync(0xffffffffu, e);
+        const int leader = __ffs(m) - 1;
+        if (lane == leader && e >= 0) masks[warp][e] |= m;
+        __syncwarp();
+    }
+    if (bad) raise_error(err, MOE_ERR_BAD_EXPERT_ID);
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kBlockTokens)
+dispatch_hist_kernel(const int32_t* __restrict__ ids, int T, int E, int K, int32_t* __restrict__ hist,
+                     int* err) {
+    if (has_error(err)) return;
+    __shared__ uint32_t masks[kWarps][kMaxE];
+    int my_e[8];
+    build_masks(ids, T, E, K, blockIdx.x, masks, err, my_e);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) c += __popc(masks[w][e]);
+        hist[static_cast<size_t>(blockIdx.x) * E + e] = c;
+    }
+}
+
+// hist [nblk][E] -> exclusive scan over blocks in place (block bases), and
+// offsets [E+1]. Thread (part p, expert e) scans a contiguous run of blocks.
+__global__ void __launch_bounds__(kScanThreads)
+dispatch_scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int32_t* __restrict__ offsets,
+                     int* err) {
+    if (has_error(err)) return;
+    __shared__ int32_t part_sum[kScanThreads];
+    __shared__ int32_t exp_tot[kMaxE];
+    const int P = kScanThreads / E;  // parts per expert (E <= 256 -> P >= 4)
+    const int e = threadIdx.x % E;
+    const int p = threadIdx.x / E;
+    const bool active = p < P;
+    const int per = (nblk + P - 1) / P;
+    const int b0 = min(nblk, p * per);
+    const int b1 = min(nblk, b0 + per);
+    int32_t s = 0;
+    if (active)
+        for (int b = b0; b < b1; ++b) s += hist[static_cast<size_t>(b) * E + e];
+    part_sum[threadIdx.x] = active ? s : 0;
+    __syncthreads();
+    if (threadIdx.x < E) {
+        int32_t run = 0;
+        for (int q = 0; q < P; ++q) {
+            const int32_t v = part_sum[q * E + threadIdx.x];
+            part_sum[q * E + threadIdx.x] = run;
+            run += v;
+        }
+        exp_tot[threadIdx.x] = run;
+    }
+    __syncthreads();
+    if (active) {
+        int32_t run = part_sum[threadIdx.x];
+        for (int b = b0; b < b1; ++b) {
+            const size_t i = static_cast<size_t>(b) * E + e;
+            const int32_t v = hist[i];
+            hist[i] = run;
+            run += v;
+        }
+    }
+    if (threadIdx.x == 0) {
+        int32_t run = 0;
+        for (int q = 0; q < E; ++q) {
+            offsets[q] = run;
+            run += exp_tot[q];
+        }
+        offsets[E] = run;
+    }
+}
+
+__global__ void __launch_bounds__(kBlockTokens)
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
+                        const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ eti, int32_t* __restrict__ tim, int* err) {
+    if (has_error(err)) return;
+    __shared__ uint32_t masks[kWarps][kMaxE];
+    __shared__ int32_t wbase[kWarps][kMaxE];
+    int my_e[8];
+    build_masks(ids, T, E, K, blockIdx.x, masks, err, my_e);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int32_t run = offsets[e] + base[static_cast<size_t>(blockIdx.x) * E + e];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            wbase[w][e] = run;
+            run += __popc(masks[w][e]);
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int t = blockIdx.x * kBlockTokens + warp * 32 + lane;
+    if (t >= T) return;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int k = 0; k < K; ++k) {
+        const int e = my_e[k];
+        if (e < 0) continue;
+        const int32_t pos = wbase[warp][e] + __popc(masks[warp][e] & lt);
+        eti[pos] = t;
+        tim[static_cast<size_t>(t) * K + k] = pos;
+    }
+}
+
+}  // namespace
+
+int dispatch_block_tokens() { return kBlockTokens; }
+
+cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
+                            int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
+                            cudaStream_t st) {
+    const int nblk = (s.T + kBlockTokens - 1) / kBlockTokens;
+    {
+        LaunchScope ls("dispatch_hist", st);
+        dispatch_hist_kernel<<<nblk, kBlockTokens, 0, st>>>(ids, s.T, s.E, s.K, hist, err);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    {
+        LaunchScope ls("dispatch_scan", st);
+        dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(hist, nblk, s.E, offsets, err);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    {
+        LaunchScope ls("dispatch_scatter", st);
+        dispatch_scatter_kernel<<<nblk, kBlockTokens, 0, st>>>(ids, s.T, s.E, s.K, hist, offsets,
+                                                               eti, tim, err);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,640 @@
+// gemm.cu — grouped expert GEMMs on tcgen05 tensor cores (sm_103a).
+//
+// One persistent, warp-specialised kernel template serves the six expert
+// GEMMs of the layer. Per CTA (192 threads, one CTA per SM):
+//   warp 0      producer: TMA loads of the A and B tiles into a ring of
+//               shared-memory stages; token rows are fetched through
+//               expert_token_indices with tile::gather4 (four rows per
+//               instruction, one instruction per lane), so no routed copy of
+//               the activations exists anywhere.
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (128 x BN x 16,
+//               bf16 in, fp32 accumulate) and tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               output row per thread), fused element-wise work, bf16 stores.
+// The accumulator is double-buffered in TMEM, so the epilogue of one tile
+// overlaps the main loop of the next. Tiles are walked in a static
+// round-robin over a device-side tile list derived from the per-expert row
+// ranges (counts never go to the host).
+//
+// The six GEMMs (T_e = rows of expert e, all bf16 with fp32 accumulation):
+//   G1  [T_e, d] x [d, h|h]  gather x; B = W1_e, W3_e (K-major);
+//       epilogue: H = (a | b) saved, A = SiLU(a) * b. (MoEBlaze paper notes 5.2
+//       epilogue fusion; SonicMoE 3.4.2 SwiGLU epilogue)
+//   G2  [T_e, h] x [h, d]    A rows contiguous; B = W2_e (K-major); Y chunk out.
+//   G3  [T_e, d] x [d, h]    gather dy; B = W2_e (MN-major): dA' = dy W2_e.
+//       epilogue: recompute sigma(a), SiLU(a), A from H; partial dS = <dA', A>;
+//       dA = w dA'; da = dA b SiLU'(a); db = dA SiLU(a); A' = w A.
+//       (SonicMoE 3.4.1 dS = <dA', A>, dA = s dA', A' = s A; MoEBlaze
+//       Algorithm 1 lines for grad A, grad B with SiLU recomputed)
+//   G4  dW2_e [d, h] = dy_e^T A'_e   varlen-K over T_e; gather dy (MN-major A),
+//       A' rows (MN-major B). (SonicMoE 3.4.1 dW2 = A'^T dO)
+//   G5  [dW1_e; dW3_e] [2h, d] = dH_e^T x_e   varlen-K; dH rows (MN-major A),
+//       gather x (MN-major B). (MoEBlaze Algorithm 1, FusedBwdW)
+//   G6  dX~ [T_e, d] = da W1_e + db W3_e   one accumulator over K = 2h
+//       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer)
+// Rows past an expert's end are zero-filled (gather of an out-of-range row)
+// on the gathered operand, so ragged tails need no padding buffers.
+#include <algorithm>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
+constexpr int kMaxE = 256;
+
+template <GemmKind KIND>
+struct Tr;
+template <> struct Tr<G1_UP>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 1, B_G = 0; };
+template <> struct Tr<G2_DOWN> { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 0, B_G = 0; };
+template <> struct Tr<G3_DH>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 1, B_G = 0; };
+template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1, B_G = 0; };
+template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 0, B_G = 1; };
+template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0, B_G = 0; };
+
+template <int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_TILES = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int SMEM_MISC = 1024 + 16 * kMaxE + 4 * (kMaxE + 1);
+    static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC;
+};
+
+struct Params {
+    int T, TK, d, h, E;
+    int Kdim;      // VM: reduction length
+    int M;         // VK: rows of the output per expert
+    int n_tiles;   // tiles along N
+    const Seg* segs;
+    const int32_t* eti;
+    void* out0;
+    void* out1;
+    const void* aux0;
+    const float* wrow;
+    float* dS_part;
+    int* err;
+};
+
+struct Tile {
+    int e, m_blk, n_blk, lo, hi, out;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const Seg* segs, int E,
+                                            int n_tiles, bool vk, int m_tiles_vk) {
+    int lo = 0, hi = E;  // largest e with prefix[e] <= tile
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (prefix[mid] <= tile) lo = mid;
+        else hi = mid;
+    }
+    Tile t;
+    t.e = lo;
+    const Seg s = segs[lo];
+    t.lo = s.lo;
+    t.hi = s.hi;
+    t.out = s.out;
+    const int local = tile - prefix[lo];
+    if (vk) {
+        t.m_blk = local % m_tiles_vk;
+        t.n_blk = local / m_tiles_vk;
+    } else {
+        const int mt = (s.hi - s.lo + BM - 1) / BM;
+        t.m_blk = local % mt;
+        t.n_blk = local / mt;
+    }
+    return t;
+}
+
+// Warp-uniform bounded wait: every lane polls, all lanes agree on the result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort, kWaitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 32 fp32 values -> 32 bf16 at dst (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void store32_bf16(void* dst, const float (&v)[32]) {
+    uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+        u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+        u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+        u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+        p[q] = u;
+    }
+}
+
+__device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
+    const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = p[q];
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            v[8 * q + 2 * j] = f.x;
+            v[8 * q + 2 * j + 1] = f.y;
+        }
+    }
+}
+
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    tmem_ld32(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <GemmKind KIND, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
+                    const __grid_constant__ CUtensorMap mapB0,
+                    const __grid_constant__ CUtensorMap mapB1, const Params p) {
+    using TR = Tr<KIND>;
+    using C = Cfg<BN>;
+    constexpr bool VK = TR::VK;
+    constexpr int NMMA = BN;  // MMA N (for G1: 128 gate + 128 up columns)
+    constexpr uint32_t IDESC = idesc_bf16(BM, NMMA, TR::A_MN, TR::B_MN);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_addr - raw_addr);
+    const uint32_t sA = base_addr;
+    const uint32_t sB = base_addr + C::STAGES * C::A_BYTES;
+    uint8_t* misc = base + C::SMEM_TILES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);  // full[S], empty[S], tfull[2], tempty[2]
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * (2 * C::STAGES + 4) + 8);
+    Seg* s_segs = reinterpret_cast<Seg*>(misc + 1024);
+    int* s_prefix = reinterpret_cast<int*>(misc + 1024 + 16 * kMaxE);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int E = p.E;
+    const int m_tiles_vk = VK ? p.M / BM : 0;
+
+    if (has_error(p.err)) return;
+
+    // ---- setup: segments, tile prefix, barriers, TMEM
+    for (int e = threadIdx.x; e < E; e += kThreads) s_segs[e] = p.segs[e];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < E; ++e) {
+            s_prefix[e] = run;
+            const int rows = s_segs[e].hi - s_segs[e].lo;
+            run += VK ? m_tiles_vk * p.n_tiles : ((rows + BM - 1) / BM) * p.n_tiles;
+        }
+        s_prefix[E] = run;
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&mapA);
+        prefetch_tensormap(&mapB0);
+        prefetch_tensormap(&mapB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = s_prefix[E];
+
+    if (warp == 0) {
+        // =========================== producer
+        int stage = 0;
+        uint32_t phase = 0;
+        bool stop = false;
+        for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+            // VM: rows of this M tile; lane l gathers rows 4l..4l+3.
+            const int row0 = t.lo + t.m_blk * BM;
+            int gi[4] = {0, 0, 0, 0};
+            if constexpr (!VK && TR::A_G) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = row0 + 4 * lane + i;
+                    gi[i] = r < t.hi ? p.eti[r] : p.T;
+                }
+            }
+            // VK: lane l owns row group (l & 15) of each 64-row K block.
+            int nx[4] = {0, 0, 0, 0};
+            auto load_vk_idx = [&](int kb, int (&dst)[4]) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = t.lo + kb * BK + 4 * (lane & 15) + i;
+                    dst[i] = r < t.hi ? p.eti[r] : p.T;
+                }
+            };
+            if constexpr (VK && (TR::A_G || TR::B_G)) {
+                if (num_kb > 0) load_vk_idx(0, gi);
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if constexpr (VK && (TR::A_G || TR::B_G)) {
+                    if (kb + 1 < num_kb) load_vk_idx(kb + 1, nx);
+                }
+                if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), C::A_BYTES + C::B_BYTES);
+                __syncwarp();
+                const uint32_t a_dst = sA + stage * C::A_BYTES;
+                const uint32_t b_dst = sB + stage * C::B_BYTES;
+                const uint32_t fb = full_bar(stage);
+                const int k0 = kb * BK;
+                if constexpr (KIND == G1_UP || KIND == G3_DH) {
+                    // A: 128 gathered rows x 64 columns, K-major.
+                    tma_gather4(a_dst + lane * 512, &mapA, fb, k0, gi[0], gi[1], gi[2], gi[3]);
+                } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
+                    if (lane == 0) tma_load_2d(a_dst, &mapA, fb, k0, row0);
+                } else if constexpr (KIND == G4_DW2) {
+                    // A (MN-major): two 64-column chunks x 16 row groups.
+                    const int c = lane >> 4, g = lane & 15;
+                    tma_gather4(a_dst + c * 8192 + g * 512, &mapA, fb, t.m_blk * BM + c * 64,
+                                gi[0], gi[1], gi[2], gi[3]);
+                } else {  // G5
+                    if (lane < 2)
+                        tma_load_2d(a_dst + lane * 8192, &mapA, fb, t.m_blk * BM + lane * 64,
+                                    t.lo + k0);
+                }
+                if constexpr (KIND == G1_UP) {
+                    if (lane == 0) {
+                        const int brow = t.e * p.h + t.n_blk * 128;
+                        tma_load_2d(b_dst, &mapB0, fb, k0, brow);
+                        tma_load_2d(b_dst + 16384, &mapB1, fb, k0, brow);
+                    }
+                } else if constexpr (KIND == G2_DOWN) {
+                    if (lane == 0) tma_load_2d(b_dst, &mapB0, fb, k0, t.e * p.d + t.n_blk * BN);
+                } else if constexpr (KIND == G3_DH) {
+                    if (lane < BN / 64)
+                        tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
+                                    t.e * p.d + k0);
+                } else if constexpr (KIND == G4_DW2) {
+                    if (lane < BN / 64)
+                        tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
+                                    t.lo + k0);
+                } else if constexpr (KIND == G5_DW13) {
+                    // B (MN-major): BN/64 column chunks x 16 row groups, gathered.
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int q = lane + 32 * j;
+                        const int c = q >> 4, g = q & 15;
+                        tma_gather4(b_dst + c * 8192 + g * 512, &mapB0, fb,
+                                    t.n_blk * BN + c * 64, gi[0], gi[1], gi[2], gi[3]);
+                    }
+                } else {  // G6: K = 2h, first h from W1, then W3.
+                    if (lane < BN / 64) {
+                        const bool up = k0 >= p.h;
+                        const int brow = t.e * p.h + (up ? k0 - p.h : k0);
+                        tma_load_2d(b_dst + lane * 8192, up ? &mapB1 : &mapB0, fb,
+                                    t.n_blk * BN + lane * 64, brow);
+                    }
+                }
+                if constexpr (VK && (TR::A_G || TR::B_G)) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) gi[i] = nx[i];
+                }
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // =========================== MMA issuer
+        int stage = 0;
+        uint32_t phase = 0;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * NMMA;
+            bool ok = true;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!warp_wait(full_bar(stage), phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a_s = sA + stage * C::A_BYTES;
+                    const uint32_t b_s = sB + stage * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = TR::A_MN ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
+                                                     : sdesc_sw128(a_s + k * 32, 16, 1024);
+                        const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, 8192, 1024)
+                                                     : sdesc_sw128(b_s + k * 32, 16, 1024);
+                        mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(tfull_bar(acc));
+            __syncwarp();
+        }
+    } else {
+        // =========================== epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t tacc = tmem_base + lane_addr + acc * NMMA;
+            float v[32];
+            if constexpr (KIND == G1_UP) {
+                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const bool valid = r < t.hi;
+                const int n0 = t.n_blk * 128;
+                __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0);
+                __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1);
+#pragma unroll 1
+                for (int j = 0; j < 128; j += 32) {
+                    float b[32];
+                    tmem_ld32f(tacc + j, v);
+                    tmem_ld32f(tacc + 128 + j, b);
+                    if (valid) {
+                        const size_t hrow = static_cast<size_t>(r) * (2 * p.h);
+                        store32_bf16(H + hrow + n0 + j, v);
+                        store32_bf16(H + hrow + p.h + n0 + j, b);
+                        float o[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = v[i] / (1.f + __expf(-v[i])) * b[i];
+                        store32_bf16(Aact + static_cast<size_t>(r) * p.h + n0 + j, o);
+                    }
+                }
+            } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
+                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const bool valid = r < t.hi;
+                const int n0 = t.n_blk * BN;
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
+                                     static_cast<size_t>(t.out + (r - t.lo)) * p.d + n0;
+#pragma unroll 1
+                for (int j = 0; j < BN; j += 32) {
+                    tmem_ld32f(tacc + j, v);
+                    if (valid) store32_bf16(out + j, v);
+                }
+            } else if constexpr (KIND == G3_DH) {
+                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const bool valid = r < t.hi;
+                const int n0 = t.n_blk * BN;
+                const size_t hrow = static_cast<size_t>(valid ? r : t.lo) * (2 * p.h);
+                const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.aux0) + hrow;
+                __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + hrow;
+                __nv_bfloat16* Ap = static_cast<__nv_bfloat16*>(p.out1) +
+                                    static_cast<size_t>(valid ? r : t.lo) * p.h;
+                const float w = valid ? p.wrow[r] : 0.f;
+                float dsum = 0.f;
+#pragma unroll 1
+                for (int j = 0; j < BN; j += 32) {
+                    tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
+                    if (valid) {
+                        float a[32], b[32], da[32], db[32], ap[32];
+                        load32_bf16(H + n0 + j, a);
+                        load32_bf16(H + p.h + n0 + j, b);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float sg = 1.f / (1.f + __expf(-a[i]));
+                            const float si = a[i] * sg;
+                            const float Av = si * b[i];
+                            dsum = fmaf(v[i], Av, dsum);
+                            const float dA = w * v[i];
+                            da[i] = dA * b[i] * (sg + a[i] * sg * (1.f - sg));
+                            db[i] = dA * si;
+                            ap[i] = w * Av;
+                        }
+                        store32_bf16(dH + n0 + j, da);
+                        store32_bf16(dH + p.h + n0 + j, db);
+                        store32_bf16(Ap + n0 + j, ap);
+                    }
+                }
+                if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
+            } else {  // G4, G5: weight gradients, one output row per thread
+                const bool empty = t.hi <= t.lo;
+                const int m = t.m_blk * BM + row_in_tile;
+                const int n0 = t.n_blk * BN;
+                __nv_bfloat16* out;
+                if constexpr (KIND == G4_DW2) {
+                    out = static_cast<__nv_bfloat16*>(p.out0) +
+                          (static_cast<size_t>(t.e) * p.d + m) * p.h + n0;
+                } else {
+                    out = (m < p.h ? static_cast<__nv_bfloat16*>(p.out0) +
+                                         (static_cast<size_t>(t.e) * p.h + m) * p.d
+                                   : static_cast<__nv_bfloat16*>(p.out1) +
+                                         (static_cast<size_t>(t.e) * p.h + (m - p.h)) * p.d) +
+                          n0;
+                }
+#pragma unroll 1
+                for (int j = 0; j < BN; j += 32) {
+                    if (empty) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    } else {
+                        tmem_ld32f(tacc + j, v);
+                    }
+                    store32_bf16(out + j, v);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    // ---- teardown
+    if (*abort_flag) {
+        raise_error(p.err, MOE_ERR_TIMEOUT);
+        // Let copies and MMAs already in flight land before the CTA exits.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 5000000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+struct Maps {
+    CUtensorMap a, b0, b1;
+};
+
+template <GemmKind KIND, int BN>
+cudaError_t launch_kind(const GemmProblem& g, const Maps& mp, const Params& prm, int max_tiles,
+                        cudaStream_t st, const char* name) {
+    using C = Cfg<BN>;
+    auto kfn = grouped_gemm_kernel<KIND, BN>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_TOTAL);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(num_sms(), max_tiles));
+    LaunchScope ls(name, st);
+    kfn<<<grid, kThreads, C::SMEM_TOTAL, st>>>(mp.a, mp.b0, mp.b1, prm);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_bn(GemmKind kind, const moe_shape& s) {
+    switch (kind) {
+        case G1_UP: return 256;  // 128 gate + 128 up columns
+        case G2_DOWN:
+        case G5_DW13:
+        case G6_DX: return s.d % 256 == 0 ? 256 : 128;
+        case G3_DH:
+        case G4_DW2: return s.h % 256 == 0 ? 256 : 128;
+    }
+    return 128;
+}
+
+cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
+    const moe_shape& s = g.s;
+    const int BN = gemm_bn(g.kind, s);
+    const uint64_t T = s.T, TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
+    Maps mp;
+    bool ok = true;
+    Params prm{};
+    prm.T = s.T;
+    prm.TK = s.T * s.K;
+    prm.d = s.d;
+    prm.h = s.h;
+    prm.E = s.E;
+    prm.segs = g.segs;
+    prm.eti = g.eti;
+    prm.out0 = g.out0;
+    prm.out1 = g.out1;
+    prm.aux0 = g.aux0;
+    prm.wrow = g.wrow;
+    prm.dS_part = g.dS_part;
+    prm.err = g.err;
+    // Upper bound on the tile count (rows of all experts + one partial tile
+    // per expert), only used to size the persistent grid.
+    const int vm_mtiles = static_cast<int>(TK / BM) + s.E;
+    int max_tiles = 0;
+    switch (g.kind) {
+        case G1_UP:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 128);
+            ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
+            prm.Kdim = s.d;
+            prm.n_tiles = s.h / 128;
+            max_tiles = vm_mtiles * prm.n_tiles;
+            break;
+        case G2_DOWN:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, h, 64, 128);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, BN);
+            mp.b1 = mp.b0;
+            prm.Kdim = s.h;
+            prm.n_tiles = s.d / BN;
+            max_tiles = vm_mtiles * prm.n_tiles;
+            break;
+        case G3_DH:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, 64);
+            mp.b1 = mp.b0;
+            prm.Kdim = s.d;
+            prm.n_tiles = s.h / BN;
+            max_tiles = vm_mtiles * prm.n_tiles;
+            break;
+        case G4_DW2:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, h, 64, 64);
+            mp.b1 = mp.b0;
+            prm.M = s.d;
+            prm.n_tiles = s.h / BN;
+            max_tiles = s.E * (s.d / BM) * prm.n_tiles;
+            break;
+        case G5_DW13:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 64);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, T, d, 64, 1);
+            mp.b1 = mp.b0;
+            prm.M = 2 * s.h;
+            prm.n_tiles = s.d / BN;
+            max_tiles = s.E * (2 * s.h / BM) * prm.n_tiles;
+            break;
+        case G6_DX:
+            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 128);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 64);
+            ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
+            prm.Kdim = 2 * s.h;
+            prm.n_tiles = s.d / BN;
+            max_tiles = vm_mtiles * prm.n_tiles;
+            break;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    switch (g.kind) {
+        case G1_UP: return launch_kind<G1_UP, 256>(g, mp, prm, max_tiles, st, "g1_up_swiglu");
+        case G2_DOWN:
+            return BN == 256 ? launch_kind<G2_DOWN, 256>(g, mp, prm, max_tiles, st, "g2_down")
+                             : launch_kind<G2_DOWN, 128>(g, mp, prm, max_tiles, st, "g2_down");
+        case G3_DH:
+            return BN == 256 ? launch_kind<G3_DH, 256>(g, mp, prm, max_tiles, st, "g3_dh")
+                             : launch_kind<G3_DH, 128>(g, mp, prm, max_tiles, st, "g3_dh");
+        case G4_DW2:
+            return BN == 256 ? launch_kind<G4_DW2, 256>(g, mp, prm, max_tiles, st, "g4_dw2")
+                             : launch_kind<G4_DW2, 128>(g, mp, prm, max_tiles, st, "g4_dw2");
+        case G5_DW13:
+            return BN == 256 ? launch_kind<G5_DW13, 256>(g, mp, prm, max_tiles, st, "g5_dw13")
+                             : launch_kind<G5_DW13, 128>(g, mp, prm, max_tiles, st, "g5_dw13");
+        case G6_DX:
+            return BN == 256 ? launch_kind<G6_DX, 256>(g, mp, prm, max_tiles, st, "g6_dx")
+                             : launch_kind<G6_DX, 128>(g, mp, prm, max_tiles, st, "g6_dx");
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe
