@@ -1,0 +1,366 @@
+"""Layer fwd+bwd throughput of the dropless MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = route + dispatch index + forward + backward of one layer over one
+batch of synthetic, seeded inputs (all through the C ABI). Prints one JSON line
+on rank 0. With N > 1 (torchrun), every rank runs an independent replica on its
+own GPU (the layer has no exchange step), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from token_dispatch_grouped_gb300 import inputs as I  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s and % of BF16 tensor peak on 1 GB300; peak act bytes"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+# Algorithmic FLOPs per step of each kernel family, in units of TK*d*h
+# (expert GEMMs: 18 TK d h in total; SonicMoE 3.4.5 counts (6 + 12) d n per token-expert).
+GEMM_FLOP_UNITS = {"g1_up_swiglu": 4, "g2_down": 2, "g3_dh": 2, "g4_dw2": 2, "g5_dw13": 4,
+                   "g6_dx": 4}
+
+
+def flops_per_step(s) -> float:
+    return 18.0 * s.T * s.K * s.d * s.h + 6.0 * s.T * s.d * s.E
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return dict(hbm=p.get("hbm_gbs"), bf16=p.get("bf16_tflops"),
+                    bf16_sus=p.get("bf16_tflops_sustained"), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(dev_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait(timeout=10)
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        loaded = [v for v in sm if v > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline)
+def cpu_oracle_sample(s, inp, tokens: int) -> tuple[float, int]:
+    """Times the CPU oracle (as it stands) on the first `tokens` tokens of the
+    workload: route, dispatch, forward and backward. Returns (seconds, tokens)."""
+    from oracle import moe_oracle as O
+    sl = slice(0, tokens)
+    t0 = time.perf_counter()
+    O.layer_step(inp["x"][sl], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], inp["dO"][sl], s.K,
+                 inp.get("bias"))
+    return time.perf_counter() - t0, tokens
+
+
+def cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def run_reference(args, s, name):
+    """The oracle as the reference arm: each step is a bounded sample."""
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    inp = I.make_layer_inputs(s, seed=0, with_bias=(name == "skew"))
+    tok = args.ref_tokens
+    for _ in range(args.warmup):
+        cpu_oracle_sample(s, inp, tok)
+    secs = 0.0
+    for _ in range(args.steps):
+        dt, _ = cpu_oracle_sample(s, inp, tok)
+        secs += dt
+    v = tok * args.steps / secs
+    line = dict(metric=METRIC, value=v, unit="tokens/s", n_gpus=args.gpus, steps=args.steps,
+                warmup=args.warmup, ms_per_step=1e3 * secs / args.steps, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=workload_config(s, name),
+                cpu_baseline=dict(value=v, unit="tokens/s", cores=cores(), kind="oracle",
+                                  sample=f"first {tok} tokens of the workload per step"),
+                e2e=dict(value=v, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(s, name):
+    return {"workload": f"{name}: T={s.T} d={s.d} E={s.E} K={s.K} h={s.h}", "T": s.T, "d": s.d,
+            "E": s.E, "K": s.K, "h": s.h, "global_batch_tokens": s.T,
+            "l2": "working set > L2 (expert weights alone exceed 129 MB and are streamed every step)"}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    name = args.workload
+    s = I.WORKLOADS[name]
+    if args.impl == "reference":
+        run_reference(args, s, name)
+        return
+
+    from token_dispatch_grouped_gb300 import binding as B
+    from token_dispatch_grouped_gb300.layer import MoELayer, Routing
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+
+    inp = I.make_layer_inputs(s, seed=0, with_bias=(name == "skew"))
+    dv = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    L = MoELayer(s.T, s.d, s.E, s.K, s.h, device=dev)
+    TK = s.T * s.K
+    # Preallocated outputs (gradients are written, not accumulated).
+    logits = torch.empty(s.T, s.E, dtype=torch.float32, device=dev)
+    r = Routing(logits, torch.empty(s.T, s.K, dtype=torch.int32, device=dev),
+                torch.empty(s.T, s.K, dtype=torch.float32, device=dev))
+    from token_dispatch_grouped_gb300.layer import Dispatch
+    dp = Dispatch(torch.empty(TK, dtype=torch.int32, device=dev),
+                  torch.empty(s.E + 1, dtype=torch.int32, device=dev),
+                  torch.empty(TK, dtype=torch.int32, device=dev))
+    y = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
+    H = torch.empty(TK, 2 * s.h, dtype=torch.bfloat16, device=dev)
+    grads = L.alloc_grads()
+    bias = dv["bias"]
+    st = torch.cuda.current_stream(dev)
+
+    def step(x, dy):
+        B.moe_route(L.s, x, dv["Wg"], bias, r.logits, r.ids, r.w, L.ws)
+        B.moe_build_dispatch(L.s, r.ids, dp.eti, dp.offsets, dp.tim, L.ws)
+        B.moe_forward(L.s, x, dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti, dp.offsets,
+                      dp.tim, y, H, L.ws)
+        B.moe_backward(L.s, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti,
+                       dp.offsets, dp.tim, H, grads["dx"], grads["dWg"], grads["dW1"],
+                       grads["dW3"], grads["dW2"], grads["dS"], L.ws)
+
+    # ---- memory: activation bytes of one fwd+bwd beyond inputs/weights/grads/outputs
+    torch.cuda.synchronize(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step(dv["x"], dv["dO"])
+    L.check_error()
+    torch.cuda.synchronize(dev)
+    routed_bytes = s.T * s.K * s.d * 2
+    ws_f = B.moe_workspace_size(L.s, B.MOE_WS_FORWARD)
+    ws_b = B.moe_workspace_size(L.s, B.MOE_WS_BACKWARD)
+    saved = H.numel() * 2 + 3 * TK * 4 + (s.E + 1) * 4 + 2 * TK * 4
+    memory = {"routed_buffer_bytes_not_allocated": routed_bytes,
+              "saved_for_backward_bytes": saved,
+              "saved_over_routed": saved / routed_bytes,
+              "workspace_fwd_bytes": ws_f, "workspace_bwd_bytes": ws_b,
+              "peak_activation_bytes": saved + max(ws_f, ws_b),
+              "peak_activation_over_routed": (saved + max(ws_f, ws_b)) / routed_bytes,
+              "combine_chunk_bytes": B.moe_chunk_tokens(L.s) * s.K * s.d * 2,
+              "allocator_peak_delta_bytes": torch.cuda.max_memory_allocated(dev) - base_alloc}
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        step(dv["x"], dv["dO"])
+    torch.cuda.synchronize(dev)
+    L.check_error()
+    clocks = ClockSampler(local)
+    launches0 = B.moe_launch_count()
+    B.moe_timing_enable(True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        step(dv["x"], dv["dO"])
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    launches = B.moe_launch_count() - launches0
+    per_kernel = B.moe_timing_collect()
+    B.moe_timing_enable(False)
+    clk = clocks.stop()
+    L.check_error()
+    ms = max_over_ranks(ms, world)
+    ms_step = ms / args.steps
+    value = world * s.T * args.steps / (ms / 1e3)
+    tflops = flops_per_step(s) / (ms_step / 1e3) / 1e12
+
+    # ---- roofline of the dominant kernel (event-timed over the timed region)
+    top = max(per_kernel.items(), key=lambda kv: kv[1][1])
+    kname, (klaunches, kms) = top
+    roof = None
+    if kname in GEMM_FLOP_UNITS:
+        per_launch_flop = GEMM_FLOP_UNITS[kname] * TK * s.d * s.h * args.steps / klaunches
+        achieved = per_launch_flop / (kms / klaunches / 1e3) / 1e12
+        peak = peaks["bf16_sus"]
+        traffic = None
+        if os.path.exists(PROFILE_TRAFFIC):
+            with open(PROFILE_TRAFFIC) as f:
+                tr = json.load(f)
+            ent = tr.get(f"{kname}@{name}")
+            if ent and ent.get("source_hash") == source_hash():
+                traffic = ent["dram_bytes_per_launch"]
+        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peaks['src']} bf16 sustained (kernel timed inside the step)"}
+    kernels = {k: {"launches": n, "ms_per_step": t / args.steps} for k, (n, t) in per_kernel.items()}
+
+    # ---- end to end: host buffers in, results out, through the same C ABI calls
+    xh = inp["x"].pin_memory()
+    dyh = inp["dO"].pin_memory()
+    yh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(dv["x"])
+    dyd = torch.empty_like(dv["dO"])
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        step(xd, dyd)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(grads["dx"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0.record(st)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e = {"value": world * s.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": xh.numel() * 2 + dyh.numel() * 2,
+           "d2h_bytes_per_step": yh.numel() * 2 + dxh.numel() * 2}
+    L.check_error()
+
+    # ---- routing statistics
+    counts = (dp.offsets[1:] - dp.offsets[:-1]).cpu()
+    routing = {"min_rows": int(counts.min()), "max_rows": int(counts.max()),
+               "empty_experts": int((counts == 0).sum()),
+               "cv": float(counts.float().std() / counts.float().mean())}
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok = args.cpu_tokens or max(8, min(s.T, 256 if s.d * s.h < 2 ** 26 else 64))
+        dt, n = cpu_oracle_sample(s, inp, tok)
+        cpu_base = {"value": n / dt, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                    "sample": f"first {n} tokens of the {name} workload, one fwd+bwd, "
+                              f"{dt:.1f} s (numpy float64, BLAS threads = all host cores)"}
+
+    if rank == 0:
+        line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
+                    warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
+                    config=workload_config(s, name), tflops=tflops,
+                    frac_of_bf16_peak=tflops / peaks["bf16_sus"],
+                    peak_note=f"{peaks['src']} bf16 sustained {peaks['bf16_sus']} TFLOP/s",
+                    memory=memory, roofline=roof, kernels=kernels, routing=routing,
+                    cpu_baseline=cpu_base, e2e=e2e, gpu_launches=launches, clocks=clk)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for f in sorted(os.listdir(os.path.join(ROOT, "token_dispatch_grouped_gb300", "csrc"))):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(ROOT, "token_dispatch_grouped_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+if __name__ == "__main__":
+    main()

@@ -57,7 +57,7 @@ def _load() -> ctypes.CDLL:
         "moe_route": (I, [MoeShape, P, P, P, P, P, P, P, S, P]),
         "moe_build_dispatch": (I, [MoeShape, P, P, P, P, P, S, P]),
         "moe_forward": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
-        "moe_backward": (I, [MoeShape] + [P] * 20 + [S, P]),
+        "moe_backward": (I, [MoeShape] + [P] * 19 + [S, P]),
         "moe_get_error": (I, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_launch_count": (L, []),
