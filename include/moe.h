@@ -71,7 +71,8 @@ enum moe_status_code {
     MOE_ERR_BAD_EXPERT_ID = 5,       /* device: id out of [0,E) or repeated      */
     MOE_ERR_TIMEOUT = 6,             /* device: a bounded wait ran out           */
     MOE_ERR_MISALIGNED = 7,          /* a pointer is not 16-byte aligned         */
-    MOE_ERR_NO_DEVICE = 8            /* no usable sm_100-family device           */
+    MOE_ERR_NO_DEVICE = 8,           /* no usable sm_100-family device           */
+    MOE_ERR_STATIC_SCRATCH_LIMIT = 9 /* shape needs more than the static scratch */
 };
 
 enum moe_workspace_kind {
@@ -110,6 +111,35 @@ int moe_route(moe_shape s, const void* x, const float* Wg, const float* bias,
 int moe_build_dispatch(moe_shape s, const int32_t* topk_ids,
                        int32_t* expert_token_indices, int32_t* expert_token_offsets,
                        int32_t* token_index_map, void* ws, size_t ws_bytes, void* stream);
+
+/* Allocation-free variant of moe_build_dispatch (the pages have no
+ * counterpart; it exists for callers that cannot allocate device memory).
+ *
+ * Some callers cannot call cudaMalloc or hand over a workspace at this point:
+ * an inference runtime or plugin host that owns every byte of device memory
+ * and forbids allocation after start-up, or a latency-critical loop where an
+ * allocation (which may synchronise the device) is not acceptable. This entry
+ * point takes no workspace: its per-block histogram lives in a file-scope
+ * device array of MOE_NOALLOC_DISPATCH_MAX_ENTRIES int32 values (4 MiB),
+ * which every GPU that loads the library holds until the process exits.
+ * It computes exactly what moe_build_dispatch computes, with the same inputs,
+ * outputs and device-side errors.
+ *   - Limit: ceil(T / 256) * E <= MOE_NOALLOC_DISPATCH_MAX_ENTRIES (for
+ *     example T <= 1,048,576 tokens at E = 256); larger shapes return
+ *     MOE_ERR_STATIC_SCRATCH_LIMIT and launch nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call
+ *     before any stream capture. Later calls do no set-up.
+ *   - All calls on a device share the one array, and it keeps the last
+ *     call's contents. Every entry a call reads is first written by the same
+ *     call, so nothing needs clearing, but calls whose kernels overlap on the
+ *     GPU (different streams, no ordering between them) race on the array and
+ *     give wrong results. Order such calls on one stream or with events.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+#define MOE_NOALLOC_DISPATCH_MAX_ENTRIES (1 << 20)
+int moe_build_dispatch_noalloc(moe_shape s, const int32_t* topk_ids,
+                               int32_t* expert_token_indices, int32_t* expert_token_offsets,
+                               int32_t* token_index_map, void* stream);
 
 /* Forward. Inputs: x, W1, W3, W2, the routing (topk_ids, topk_w) and its
  * dispatch index. Outputs: y [T,d] bf16 and H_saved [TK,2h] bf16 (the

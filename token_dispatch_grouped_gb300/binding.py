@@ -24,6 +24,8 @@ MOE_ERR_BAD_EXPERT_ID = 5
 MOE_ERR_TIMEOUT = 6
 MOE_ERR_MISALIGNED = 7
 MOE_ERR_NO_DEVICE = 8
+MOE_ERR_STATIC_SCRATCH_LIMIT = 9
+MOE_NOALLOC_DISPATCH_MAX_ENTRIES = 1 << 20
 
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_FORWARD, MOE_WS_BACKWARD = 0, 1, 2, 3
 
@@ -56,6 +58,7 @@ def _load() -> ctypes.CDLL:
         "moe_chunk_tokens": (I, [MoeShape]),
         "moe_route": (I, [MoeShape, P, P, P, P, P, P, P, S, P]),
         "moe_build_dispatch": (I, [MoeShape, P, P, P, P, P, S, P]),
+        "moe_build_dispatch_noalloc": (I, [MoeShape, P, P, P, P, P]),
         "moe_forward": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_backward": (I, [MoeShape] + [P] * 19 + [S, P]),
         "moe_get_error": (I, [P]),
@@ -124,6 +127,17 @@ def moe_build_dispatch(s, topk_ids, eti, offsets, tim, ws, stream=None, check=Tr
                                 _stream(stream))
     if check:
         _check(rc, "moe_build_dispatch")
+    return rc
+
+
+def moe_build_dispatch_noalloc(s, topk_ids, eti, offsets, tim, stream=None, check=True):
+    """Same result as moe_build_dispatch without a workspace: for callers that
+    cannot allocate device memory (the scratch is a static device array inside
+    the library; calls that overlap on the GPU must not share it)."""
+    rc = LIB.moe_build_dispatch_noalloc(s, _ptr(topk_ids), _ptr(eti), _ptr(offsets), _ptr(tim),
+                                        _stream(stream))
+    if check:
+        _check(rc, "moe_build_dispatch_noalloc")
     return rc
 
 

@@ -198,6 +198,8 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+int* device_status_word() { return status_ptr(); }
+
 int num_sms() {
     const int dev = current_device();
     if (dev < 0) return 1;
@@ -427,6 +429,8 @@ const char* moe_status_string(int status) {
         case MOE_ERR_TIMEOUT: return "bounded device wait ran out";
         case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case MOE_ERR_NO_DEVICE: return "no usable CUDA device";
+        case MOE_ERR_STATIC_SCRATCH_LIMIT:
+            return "shape needs more scratch than the library's static device array holds";
     }
     return "unknown status";
 }

@@ -43,6 +43,9 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 
 int num_sms();
 
+// Address of the current device's status word (nullptr without a device).
+int* device_status_word();
+
 // ---------------------------------------------------------------- launchers
 // Every launcher enqueues on `st` and returns a cudaError_t of the launch.
 

@@ -21,6 +21,8 @@
 //       (t, k) is the number of lower lanes in its warp's mask plus the counts
 //       of earlier warps; position = offsets[e] + base[block][e] + rank. This
 //       is exactly the order of a stable sort of the flattened ids by expert.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -188,3 +190,57 @@ cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free dispatch build: the per-block histogram lives in a
+// file-scope device array instead of the caller's workspace. In host code the
+// array's name is only a host-side stand-in; its device address is looked up
+// once per device (with that device current) and passed to the kernels.
+namespace moe {
+namespace {
+
+static __device__ __align__(256) int32_t g_noalloc_hist[MOE_NOALLOC_DISPATCH_MAX_ENTRIES];
+
+constexpr int kNoAllocMaxDevices = 64;
+int32_t* g_noalloc_hist_ptr[kNoAllocMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_hist on the current device (set up on first use).
+int32_t* noalloc_hist_ptr() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_hist_ptr[dev] == nullptr) {
+        int32_t* ptr = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_hist) != cudaSuccess)
+            return nullptr;
+        g_noalloc_hist_ptr[dev] = ptr;
+    }
+    return g_noalloc_hist_ptr[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_build_dispatch_noalloc(moe_shape s, const int32_t* topk_ids, int32_t* eti,
+                                          int32_t* offsets, int32_t* tim, void* stream) {
+    using namespace moe;
+    if (moe_workspace_size(s, MOE_WS_DISPATCH) == 0) {
+        if (s.T < 1 || s.d < 1 || s.E < 1 || s.K < 1 || s.h < 1) return MOE_ERR_INVALID_ARG;
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (!topk_ids || !eti || !offsets || !tim) return MOE_ERR_INVALID_ARG;
+    const long long nblk = (static_cast<long long>(s.T) + kBlockTokens - 1) / kBlockTokens;
+    if (nblk * s.E > MOE_NOALLOC_DISPATCH_MAX_ENTRIES) return MOE_ERR_STATIC_SCRATCH_LIMIT;
+    int* err = device_status_word();
+    if (!err) return MOE_ERR_NO_DEVICE;
+    int32_t* hist = noalloc_hist_ptr();
+    if (!hist) return MOE_ERR_CUDA;
+    // Every histogram entry the kernels read is written earlier in the same
+    // call (one entry per block and expert), so the array is not cleared.
+    if (launch_dispatch(s, topk_ids, eti, offsets, tim, hist, err,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
