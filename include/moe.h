@@ -86,10 +86,15 @@ enum moe_workspace_kind {
  * shape is unsupported). Pure host function. */
 size_t moe_workspace_size(moe_shape s, int which);
 
-/* Tokens per combine chunk: moe_forward and moe_backward run the down
- * projection (and the dX of the up projection) over token chunks of this many
- * tokens, so the transient expert-output buffer holds chunk*K*d elements, at
- * most a quarter of T*K*d once T >= 1024. Pure host function. */
+/* Transient-buffer bound: moe_forward runs the down projection and the
+ * weighted combine (and moe_backward the dX of the up projection and the
+ * token-gradient sum) in passes once T >= 1024, so the expert-output buffer
+ * holds at most about a quarter of T*K*d elements. A pass covers either a
+ * chunk of tokens or, when d is a multiple of 512, a quarter of the output
+ * columns; the library takes the split that re-reads fewer bytes (token
+ * chunks re-read the expert weights once per pass, column chunks re-read the
+ * activation operand). This function returns the tokens per token chunk.
+ * Pure host function. */
 int moe_chunk_tokens(moe_shape s);
 
 /* Router. x [T,d] bf16, Wg [E,d] fp32, bias [E] fp32 or NULL.

@@ -51,6 +51,7 @@ SMALL = [
     I.Shape(1, 128, 4, 4, 128),       # one token, K = E
     I.Shape(1500, 128, 16, 1, 256),   # K = 1 (router gradient is zero), 4 token chunks
     I.Shape(129, 384, 8, 8, 128),     # K = E = 8
+    I.Shape(1100, 512, 8, 2, 256),    # passes split by output columns (d % 512 == 0)
 ]
 
 

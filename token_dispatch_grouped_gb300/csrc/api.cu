@@ -93,6 +93,49 @@ int check_shape(const moe_shape& s) {
 
 int nchunks_of(const moe_shape& s, int tc) { return (s.T + tc - 1) / tc; }
 
+// How a down projection (forward) or dX pass (backward) is split so that its
+// transient [rows, columns] output buffer holds at most a quarter of T*K*d
+// once T >= 1024. Splitting by token chunks streams the expert weights once
+// per chunk; splitting by output-column chunks streams the activation
+// operand once per chunk instead. The split that re-reads fewer bytes wins.
+struct Plan {
+    int n;         // passes
+    bool by_cols;  // column chunks (else token chunks)
+    int tc;        // tokens per token chunk
+    int dc;        // columns per column chunk
+};
+
+Plan make_plan(const moe_shape& s, double weight_bytes, double act_bytes) {
+    Plan p{1, false, s.T, s.d};
+    if (s.T < 1024) return p;
+    p.n = 4;
+    p.tc = moe_chunk_tokens(s);
+    p.n = nchunks_of(s, p.tc);
+    const bool cols_ok = s.d % (4 * 128) == 0;
+    if (cols_ok && act_bytes < weight_bytes) {
+        p.n = 4;
+        p.by_cols = true;
+        p.tc = s.T;
+        p.dc = s.d / 4;
+    }
+    return p;
+}
+
+Plan plan_down(const moe_shape& s) {
+    const double TK = static_cast<double>(s.T) * s.K;
+    return make_plan(s, 2.0 * s.E * s.d * s.h, 2.0 * TK * s.h);
+}
+
+Plan plan_dx(const moe_shape& s) {
+    const double TK = static_cast<double>(s.T) * s.K;
+    return make_plan(s, 4.0 * s.E * s.d * s.h, 4.0 * TK * s.h);
+}
+
+size_t chunk_buffer_elems(const moe_shape& s, const Plan& p) {
+    const size_t TK = static_cast<size_t>(s.T) * s.K;
+    return p.by_cols ? TK * p.dc : static_cast<size_t>(p.tc) * s.K * s.d;
+}
+
 struct FwdWs {
     Seg* segs;
     __nv_bfloat16* Aact;
@@ -103,6 +146,7 @@ struct BwdWs {
     float* wrow;
     float* dS_part;
     float* dz;
+    float* dz_row;
     __nv_bfloat16* Ap;
     __nv_bfloat16* dH;
     __nv_bfloat16* dXc;
@@ -118,7 +162,7 @@ size_t layout_fwd(const moe_shape& s, void* ws, FwdWs* o) {
     FwdWs w;
     w.segs = c.take<Seg>(static_cast<size_t>(nc + 1) * s.E);
     w.Aact = c.take<__nv_bfloat16>(TK * s.h);
-    w.Yc = c.take<__nv_bfloat16>(static_cast<size_t>(tc) * s.K * s.d);
+    w.Yc = c.take<__nv_bfloat16>(chunk_buffer_elems(s, plan_down(s)));
     if (o) *o = w;
     return align_up(c.off, 256);
 }
@@ -128,7 +172,6 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     const int nc = nchunks_of(s, tc);
     const size_t TK = static_cast<size_t>(s.T) * s.K;
     const int nparts = s.h / gemm_bn(G3_DH, s);
-    const int ndwg = (s.T + dwg_token_chunk() - 1) / dwg_token_chunk();
     Carve c;
     c.base = static_cast<char*>(ws);
     BwdWs w;
@@ -136,10 +179,11 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     w.wrow = c.take<float>(TK);
     w.dS_part = c.take<float>(TK * nparts);
     w.dz = c.take<float>(TK);
+    w.dz_row = c.take<float>(TK);
     w.Ap = c.take<__nv_bfloat16>(TK * s.h);
     w.dH = c.take<__nv_bfloat16>(TK * 2 * s.h);
-    w.dXc = c.take<__nv_bfloat16>(static_cast<size_t>(tc) * s.K * s.d);
-    w.dwg_part = c.take<float>(static_cast<size_t>(ndwg) * s.E * s.d);
+    w.dXc = c.take<__nv_bfloat16>(chunk_buffer_elems(s, plan_dx(s)));
+    w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
     if (o) *o = w;
     return align_up(c.off, 256);
 }
@@ -299,8 +343,9 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
     g1.err = err;
     MOE_TRY(launch_gemm(g1, st));
 
-    for (int c = 0; c < nc; ++c) {
-        const Seg* sc = w.segs + static_cast<size_t>(c) * s.E;
+    const Plan pl = plan_down(s);
+    for (int c = 0; c < pl.n; ++c) {
+        const Seg* sc = pl.by_cols ? full : w.segs + static_cast<size_t>(c) * s.E;
         GemmProblem g2{};
         g2.kind = G2_DOWN;
         g2.s = s;
@@ -309,10 +354,12 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
         g2.a_src = w.Aact;
         g2.b_src0 = W2;
         g2.out0 = w.Yc;
+        g2.n_off = pl.by_cols ? c * pl.dc : 0;
+        g2.n_cols = pl.by_cols ? pl.dc : s.d;
         g2.err = err;
         MOE_TRY(launch_gemm(g2, st));
-        const int t0 = c * tc, t1 = std::min(s.T, t0 + tc);
-        MOE_TRY(launch_combine(s, t0, t1, topk_ids, topk_w, tim, sc, w.Yc,
+        const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
+        MOE_TRY(launch_combine(s, t0, t1, g2.n_off, g2.n_cols, topk_ids, topk_w, tim, sc, w.Yc,
                                static_cast<__nv_bfloat16*>(y), err, st));
     }
     return MOE_OK;
@@ -360,7 +407,7 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
     g3.err = err;
     MOE_TRY(launch_gemm(g3, st));
     const int nparts = s.h / gemm_bn(G3_DH, s);
-    MOE_TRY(launch_router_dz(s, nparts, w.dS_part, topk_w, tim, dS, w.dz, err, st));
+    MOE_TRY(launch_router_dz(s, nparts, w.dS_part, topk_w, tim, dS, w.dz, w.dz_row, err, st));
 
     GemmProblem g4{};
     g4.kind = G4_DW2;
@@ -378,15 +425,16 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
     g5.s = s;
     g5.segs = full;
     g5.eti = eti;
-    g5.a_src = w.dH;
-    g5.b_src0 = x;
+    g5.a_src = x;
+    g5.b_src0 = w.dH;
     g5.out0 = dW1;
     g5.out1 = dW3;
     g5.err = err;
     MOE_TRY(launch_gemm(g5, st));
 
-    for (int c = 0; c < nc; ++c) {
-        const Seg* sc = w.segs + static_cast<size_t>(c) * s.E;
+    const Plan pl = plan_dx(s);
+    for (int c = 0; c < pl.n; ++c) {
+        const Seg* sc = pl.by_cols ? full : w.segs + static_cast<size_t>(c) * s.E;
         GemmProblem g6{};
         g6.kind = G6_DX;
         g6.s = s;
@@ -396,13 +444,15 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
         g6.b_src0 = W1;
         g6.b_src1 = W3;
         g6.out0 = w.dXc;
+        g6.n_off = pl.by_cols ? c * pl.dc : 0;
+        g6.n_cols = pl.by_cols ? pl.dc : s.d;
         g6.err = err;
         MOE_TRY(launch_gemm(g6, st));
-        const int t0 = c * tc, t1 = std::min(s.T, t0 + tc);
-        MOE_TRY(launch_dx_combine(s, t0, t1, topk_ids, w.dz, tim, sc, w.dXc, Wg,
-                                  static_cast<__nv_bfloat16*>(dx), err, st));
+        const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
+        MOE_TRY(launch_dx_combine(s, t0, t1, g6.n_off, g6.n_cols, topk_ids, w.dz, tim, sc,
+                                  w.dXc, Wg, static_cast<__nv_bfloat16*>(dx), err, st));
     }
-    MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), topk_ids, w.dz,
+    MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), eti, offsets, w.dz_row,
                               w.dwg_part, dWg, err, st));
     return MOE_OK;
 }

@@ -66,20 +66,20 @@ cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchu
                                   cudaStream_t st);
 cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const int32_t* tim,
                                float* wrow, int* err, cudaStream_t st);
-cudaError_t launch_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
+cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st);
 cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
-                             int* err, cudaStream_t st);
-cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
-                              const float* dz, const int32_t* tim, const Seg* seg,
-                              const __nv_bfloat16* dXc, const float* Wg, __nv_bfloat16* dx,
-                              int* err, cudaStream_t st);
-int dwg_token_chunk();
-cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* ids,
-                              const float* dz, float* part, float* dWg, int* err,
-                              cudaStream_t st);
+                             float* dz_row, int* err, cudaStream_t st);
+cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc,
+                              const int32_t* ids, const float* dz, const int32_t* tim,
+                              const Seg* seg, const __nv_bfloat16* dXc, const float* Wg,
+                              __nv_bfloat16* dx, int* err, cudaStream_t st);
+int dwg_parts();
+cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
+                              const int32_t* offsets, const float* dz_row, float* part,
+                              float* dWg, int* err, cudaStream_t st);
 
 // gemm.cu — the grouped tcgen05 GEMMs.
 enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5 };
@@ -90,8 +90,8 @@ struct GemmProblem {
     const Seg* segs;          // [E] rows of each expert (VM: this chunk's rows)
     const int32_t* eti;       // expert_token_indices (gather rows)
     // operands (bf16 unless noted)
-    const void* a_src;        // x (G1) | A_act (G2) | dy (G3) | dy (G4) | dH (G5) | dH (G6)
-    const void* b_src0;       // W1 (G1) | W2 (G2) | W2 (G3) | A' (G4) | x (G5) | W1 (G6)
+    const void* a_src;        // x (G1) | A_act (G2) | dy (G3) | dy (G4) | x (G5) | dH (G6)
+    const void* b_src0;       // W1 (G1) | W2 (G2) | W2 (G3) | A' (G4) | dH (G5) | W1 (G6)
     const void* b_src1;       // W3 (G1, G6)
     // epilogue
     void* out0;               // H (G1) | Yc (G2) | dH (G3) | dW2 (G4) | dW1 (G5) | dXc (G6)
@@ -99,6 +99,8 @@ struct GemmProblem {
     const void* aux0;         // H (G3)
     const float* wrow;        // per-row routing weight (G3)
     float* dS_part;           // [h/BN][TK] (G3)
+    int n_off = 0;            // G2/G6: first output column computed by this launch
+    int n_cols = 0;           // G2/G6: output columns of this launch (= row stride of out0)
     int* err;
 };
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t st);

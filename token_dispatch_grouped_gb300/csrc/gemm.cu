@@ -2,11 +2,14 @@
 //
 // One persistent, warp-specialised kernel template serves the six expert
 // GEMMs of the layer. Per CTA (192 threads, one CTA per SM):
-//   warp 0      producer: TMA loads of the A and B tiles into a ring of
-//               shared-memory stages; token rows are fetched through
-//               expert_token_indices with tile::gather4 (four rows per
-//               instruction, one instruction per lane), so no routed copy of
-//               the activations exists anywhere.
+//   warp 0      producer: TMA tile loads of the operands that are stored
+//               contiguously (weights, SwiGLU output, dH, A') into a ring of
+//               shared-memory stages.
+//   warps 6..9  (gathering kinds) cp.async gather of the token-row operand
+//               through expert_token_indices, 16 bytes per thread, written in
+//               the 128-byte-swizzled layout the MMA descriptors expect; rows
+//               past an expert's end are zero-filled. No routed copy of the
+//               activations exists anywhere.
 //   warp 1      allocates TMEM; one thread issues tcgen05.mma (128 x BN x 16,
 //               bf16 in, fp32 accumulate) and tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
@@ -28,12 +31,14 @@
 //       Algorithm 1 lines for grad A, grad B with SiLU recomputed)
 //   G4  dW2_e [d, h] = dy_e^T A'_e   varlen-K over T_e; gather dy (MN-major A),
 //       A' rows (MN-major B). (SonicMoE 3.4.1 dW2 = A'^T dO)
-//   G5  [dW1_e; dW3_e] [2h, d] = dH_e^T x_e   varlen-K; dH rows (MN-major A),
-//       gather x (MN-major B). (MoEBlaze Algorithm 1, FusedBwdW)
+//   G5  (x_e^T dH_e) [d, 2h] = [dW1_e; dW3_e]^T   varlen-K; gather x (MN-major
+//       A, M = d), dH rows (MN-major B); the epilogue stores the transpose.
+//       (MoEBlaze Algorithm 1, FusedBwdW)
 //   G6  dX~ [T_e, d] = da W1_e + db W3_e   one accumulator over K = 2h
 //       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer)
-// Rows past an expert's end are zero-filled (gather of an out-of-range row)
-// on the gathered operand, so ragged tails need no padding buffers.
+// Rows past an expert's end are zero-filled on the gathered operand, so
+// ragged tails need no padding buffers (the other operand's extra rows are
+// multiplied by zeros).
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,18 +51,20 @@ using namespace ptx;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr int kMaxE = 256;
 
 template <GemmKind KIND>
 struct Tr;
-template <> struct Tr<G1_UP>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 1, B_G = 0; };
-template <> struct Tr<G2_DOWN> { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 0, B_G = 0; };
-template <> struct Tr<G3_DH>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 1, B_G = 0; };
-template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1, B_G = 0; };
-template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 0, B_G = 1; };
-template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0, B_G = 0; };
+// VK: varlen-K (weight gradients); A_MN/B_MN: operand is MN-major in shared
+// memory; A_G: the A operand is gathered row by row through
+// expert_token_indices by the cp.async gather warps.
+template <> struct Tr<G1_UP>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 1; };
+template <> struct Tr<G2_DOWN> { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 0, A_G = 0; };
+template <> struct Tr<G3_DH>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 1; };
+template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
+template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
+template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0; };
 
 template <int BN>
 struct Cfg {
@@ -70,13 +77,22 @@ struct Cfg {
     static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC;
 };
 
+// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..5 epilogue,
+// 6..9 cp.async gather of the A operand (gathered kinds only).
+constexpr int kGatherThreads = 128;
+template <GemmKind KIND>
+constexpr int threads_of() { return Tr<KIND>::A_G ? 192 + kGatherThreads : 192; }
+
 struct Params {
     int T, TK, d, h, E;
     int Kdim;      // VM: reduction length
     int M;         // VK: rows of the output per expert
     int n_tiles;   // tiles along N
+    int n_off;     // G2/G6: first output column of this launch (column chunk)
+    int ldo;       // G2/G6: row stride of the output chunk buffer (elements)
     const Seg* segs;
     const int32_t* eti;
+    const __nv_bfloat16* gsrc;  // gathered rows: x or dy, [T, d]
     void* out0;
     void* out1;
     const void* aux0;
@@ -89,8 +105,11 @@ struct Tile {
     int e, m_blk, n_blk, lo, hi, out;
 };
 
+// Tile order inside one expert: M fastest, so tiles that run at the same time
+// share their B panel (a weight panel for the VM kinds, the A' or dH panel
+// for the weight gradients).
 __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const Seg* segs, int E,
-                                            int n_tiles, bool vk, int m_tiles_vk) {
+                                            bool vk, int m_tiles_vk) {
     int lo = 0, hi = E;  // largest e with prefix[e] <= tile
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -104,14 +123,9 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
     t.hi = s.hi;
     t.out = s.out;
     const int local = tile - prefix[lo];
-    if (vk) {
-        t.m_blk = local % m_tiles_vk;
-        t.n_blk = local / m_tiles_vk;
-    } else {
-        const int mt = (s.hi - s.lo + BM - 1) / BM;
-        t.m_blk = local % mt;
-        t.n_blk = local / mt;
-    }
+    const int mt = vk ? m_tiles_vk : (s.hi - s.lo + BM - 1) / BM;
+    t.m_blk = local % mt;
+    t.n_blk = local / mt;
     return t;
 }
 
@@ -164,7 +178,7 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
 }
 
 template <GemmKind KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<KIND>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB0,
                     const __grid_constant__ CUtensorMap mapB1, const Params p) {
@@ -173,6 +187,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     constexpr bool VK = TR::VK;
     constexpr int NMMA = BN;  // MMA N (for G1: 128 gate + 128 up columns)
     constexpr uint32_t IDESC = idesc_bf16(BM, NMMA, TR::A_MN, TR::B_MN);
+    // Bytes the TMA producer brings per stage (the gather warps bring A otherwise).
+    constexpr uint32_t TMA_BYTES = TR::A_G ? C::B_BYTES : C::A_BYTES + C::B_BYTES;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -200,7 +216,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     if (has_error(p.err)) return;
 
     // ---- setup: segments, tile prefix, barriers, TMEM
-    for (int e = threadIdx.x; e < E; e += kThreads) s_segs[e] = p.segs[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
@@ -211,7 +227,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         }
         s_prefix[E] = run;
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), 1 + (TR::A_G ? kGatherThreads : 0));
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -237,63 +253,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int num_tiles = s_prefix[E];
 
     if (warp == 0) {
-        // =========================== producer
+        // =========================== TMA producer
         int stage = 0;
         uint32_t phase = 0;
         bool stop = false;
         for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
-            // VM: rows of this M tile; lane l gathers rows 4l..4l+3.
             const int row0 = t.lo + t.m_blk * BM;
-            int gi[4] = {0, 0, 0, 0};
-            if constexpr (!VK && TR::A_G) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = row0 + 4 * lane + i;
-                    gi[i] = r < t.hi ? p.eti[r] : p.T;
-                }
-            }
-            // VK: lane l owns row group (l & 15) of each 64-row K block.
-            int nx[4] = {0, 0, 0, 0};
-            auto load_vk_idx = [&](int kb, int (&dst)[4]) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = t.lo + kb * BK + 4 * (lane & 15) + i;
-                    dst[i] = r < t.hi ? p.eti[r] : p.T;
-                }
-            };
-            if constexpr (VK && (TR::A_G || TR::B_G)) {
-                if (num_kb > 0) load_vk_idx(0, gi);
-            }
             for (int kb = 0; kb < num_kb; ++kb) {
-                if constexpr (VK && (TR::A_G || TR::B_G)) {
-                    if (kb + 1 < num_kb) load_vk_idx(kb + 1, nx);
-                }
                 if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), C::A_BYTES + C::B_BYTES);
+                if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), TMA_BYTES);
                 __syncwarp();
                 const uint32_t a_dst = sA + stage * C::A_BYTES;
                 const uint32_t b_dst = sB + stage * C::B_BYTES;
                 const uint32_t fb = full_bar(stage);
                 const int k0 = kb * BK;
-                if constexpr (KIND == G1_UP || KIND == G3_DH) {
-                    // A: 128 gathered rows x 64 columns, K-major.
-                    tma_gather4(a_dst + lane * 512, &mapA, fb, k0, gi[0], gi[1], gi[2], gi[3]);
-                } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
+                if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
                     if (lane == 0) tma_load_2d(a_dst, &mapA, fb, k0, row0);
-                } else if constexpr (KIND == G4_DW2) {
-                    // A (MN-major): two 64-column chunks x 16 row groups.
-                    const int c = lane >> 4, g = lane & 15;
-                    tma_gather4(a_dst + c * 8192 + g * 512, &mapA, fb, t.m_blk * BM + c * 64,
-                                gi[0], gi[1], gi[2], gi[3]);
-                } else {  // G5
-                    if (lane < 2)
-                        tma_load_2d(a_dst + lane * 8192, &mapA, fb, t.m_blk * BM + lane * 64,
-                                    t.lo + k0);
                 }
                 if constexpr (KIND == G1_UP) {
                     if (lane == 0) {
@@ -302,35 +282,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         tma_load_2d(b_dst + 16384, &mapB1, fb, k0, brow);
                     }
                 } else if constexpr (KIND == G2_DOWN) {
-                    if (lane == 0) tma_load_2d(b_dst, &mapB0, fb, k0, t.e * p.d + t.n_blk * BN);
+                    if (lane == 0)
+                        tma_load_2d(b_dst, &mapB0, fb, k0, t.e * p.d + p.n_off + t.n_blk * BN);
                 } else if constexpr (KIND == G3_DH) {
                     if (lane < BN / 64)
                         tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
                                     t.e * p.d + k0);
-                } else if constexpr (KIND == G4_DW2) {
+                } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13) {
+                    // B rows of this expert (A' for dW2, dH for dW1/dW3), MN-major.
                     if (lane < BN / 64)
                         tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
                                     t.lo + k0);
-                } else if constexpr (KIND == G5_DW13) {
-                    // B (MN-major): BN/64 column chunks x 16 row groups, gathered.
-#pragma unroll
-                    for (int j = 0; j < BN / 128; ++j) {
-                        const int q = lane + 32 * j;
-                        const int c = q >> 4, g = q & 15;
-                        tma_gather4(b_dst + c * 8192 + g * 512, &mapB0, fb,
-                                    t.n_blk * BN + c * 64, gi[0], gi[1], gi[2], gi[3]);
-                    }
                 } else {  // G6: K = 2h, first h from W1, then W3.
                     if (lane < BN / 64) {
                         const bool up = k0 >= p.h;
                         const int brow = t.e * p.h + (up ? k0 - p.h : k0);
                         tma_load_2d(b_dst + lane * 8192, up ? &mapB1 : &mapB0, fb,
-                                    t.n_blk * BN + lane * 64, brow);
+                                    p.n_off + t.n_blk * BN + lane * 64, brow);
                     }
-                }
-                if constexpr (VK && (TR::A_G || TR::B_G)) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) gi[i] = nx[i];
                 }
                 if (++stage == C::STAGES) {
                     stage = 0;
@@ -344,7 +313,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         uint32_t phase = 0;
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
@@ -357,6 +326,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     ok = false;
                     break;
                 }
+                // cp.async wrote A through the generic proxy; the MMA reads it
+                // through the async proxy.
+                if constexpr (TR::A_G) fence_proxy_async_smem();
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t a_s = sA + stage * C::A_BYTES;
@@ -381,14 +353,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             if (lane == 0) mma_commit(tfull_bar(acc));
             __syncwarp();
         }
-    } else {
+    } else if (warp < 6) {
         // =========================== epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, p.n_tiles, VK, m_tiles_vk);
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
@@ -421,7 +393,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 const bool valid = r < t.hi;
                 const int n0 = t.n_blk * BN;
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
-                                     static_cast<size_t>(t.out + (r - t.lo)) * p.d + n0;
+                                     static_cast<size_t>(t.out + (r - t.lo)) * p.ldo + n0;
 #pragma unroll 1
                 for (int j = 0; j < BN; j += 32) {
                     tmem_ld32f(tacc + j, v);
@@ -462,21 +434,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                 }
                 if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
-            } else {  // G4, G5: weight gradients, one output row per thread
+            } else if constexpr (KIND == G4_DW2) {
+                // dW2_e [d, h]: this thread owns row m (a d index), BN h-columns.
                 const bool empty = t.hi <= t.lo;
                 const int m = t.m_blk * BM + row_in_tile;
-                const int n0 = t.n_blk * BN;
-                __nv_bfloat16* out;
-                if constexpr (KIND == G4_DW2) {
-                    out = static_cast<__nv_bfloat16*>(p.out0) +
-                          (static_cast<size_t>(t.e) * p.d + m) * p.h + n0;
-                } else {
-                    out = (m < p.h ? static_cast<__nv_bfloat16*>(p.out0) +
-                                         (static_cast<size_t>(t.e) * p.h + m) * p.d
-                                   : static_cast<__nv_bfloat16*>(p.out1) +
-                                         (static_cast<size_t>(t.e) * p.h + (m - p.h)) * p.d) +
-                          n0;
-                }
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
+                                     (static_cast<size_t>(t.e) * p.d + m) * p.h + t.n_blk * BN;
 #pragma unroll 1
                 for (int j = 0; j < BN; j += 32) {
                     if (empty) {
@@ -487,11 +450,116 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                     store32_bf16(out + j, v);
                 }
+            } else {  // G5: tile of (x^T dH)_e [d, 2h]; transposed into dW1/dW3 [h, d]
+                const bool empty = t.hi <= t.lo;
+                const int m = t.m_blk * BM + row_in_tile;  // d index
+                const int n0 = t.n_blk * BN;               // index into [0, 2h)
+                __nv_bfloat16* out =
+                    n0 < p.h ? static_cast<__nv_bfloat16*>(p.out0) +
+                                   (static_cast<size_t>(t.e) * p.h + n0) * p.d + m
+                             : static_cast<__nv_bfloat16*>(p.out1) +
+                                   (static_cast<size_t>(t.e) * p.h + (n0 - p.h)) * p.d + m;
+#pragma unroll 1
+                for (int j = 0; j < BN; j += 32) {
+                    if (empty) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    } else {
+                        tmem_ld32f(tacc + j, v);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        out[static_cast<size_t>(j + i) * p.d] = __float2bfloat16_rn(v[i]);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
+    } else if constexpr (TR::A_G) {
+        // =========================== cp.async gather of A (warps 6..9)
+        // Shared layout is the 128-byte swizzle that the MMA descriptors expect:
+        // 16-byte chunk c of a 128-byte smem row r lives at chunk c ^ (r & 7).
+        const int g = threadIdx.x - 192;  // 0..127
+        const int col16 = g & 7;
+        const size_t rowbytes = static_cast<size_t>(p.d) * 2;
+        const char* src0 = reinterpret_cast<const char*>(p.gsrc);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool stop = false;
+        for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
+            const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+            if constexpr (!VK) {
+                // K-major A: 128 rows x 64 columns; this thread copies 16-byte
+                // chunk col16 of rows rb + 16 j, j = 0..7 (same rows every k-block).
+                const int rb = g >> 3;
+                int idx[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int r = t.lo + t.m_blk * BM + rb + 16 * j;
+                    idx[j] = r < t.hi ? p.eti[r] : -1;
+                }
+                const uint32_t soff = static_cast<uint32_t>(rb * 128 + ((col16 ^ (rb & 7)) << 4));
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
+                    const size_t coff = static_cast<size_t>(kb * BK) * 2 + col16 * 16;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
+                        cp_async16(a_dst + j * 16 * 128, src, idx[j] >= 0 ? 16u : 0u);
+                    }
+                    cp_async_arrive_noinc(full_bar(stage));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else {
+                // MN-major A: 64 k-rows (tokens) x 128 m-columns in two 64-column
+                // chunks of 8 KB; this thread copies 16-byte chunk col16 of column
+                // chunk ch for token rows rb + 8 j, j = 0..7.
+                const int ch = (g >> 3) & 1;
+                const int rb = g >> 4;
+                const uint32_t soff =
+                    static_cast<uint32_t>(ch * 8192 + rb * 128 + ((col16 ^ (rb & 7)) << 4));
+                const size_t coff = static_cast<size_t>(t.m_blk * BM + ch * 64) * 2 + col16 * 16;
+                int idx[8], nxt[8];
+                auto load_idx = [&](int kb, int (&dst)[8]) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int r = t.lo + kb * BK + rb + 8 * j;
+                        dst[j] = r < t.hi ? p.eti[r] : -1;
+                    }
+                };
+                if (num_kb > 0) load_idx(0, idx);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (kb + 1 < num_kb) load_idx(kb + 1, nxt);
+                    if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
+                        cp_async16(a_dst + j * 8 * 128, src, idx[j] >= 0 ? 16u : 0u);
+                    }
+                    cp_async_arrive_noinc(full_bar(stage));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) idx[j] = nxt[j];
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        cp_async_wait_all();
     }
 
     // ---- teardown
@@ -523,7 +591,7 @@ cudaError_t launch_kind(const GemmProblem& g, const Maps& mp, const Params& prm,
     if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(num_sms(), max_tiles));
     LaunchScope ls(name, st);
-    kfn<<<grid, kThreads, C::SMEM_TOTAL, st>>>(mp.a, mp.b0, mp.b1, prm);
+    kfn<<<grid, threads_of<KIND>(), C::SMEM_TOTAL, st>>>(mp.a, mp.b0, mp.b1, prm);
     return cudaGetLastError();
 }
 
@@ -533,18 +601,20 @@ int gemm_bn(GemmKind kind, const moe_shape& s) {
     switch (kind) {
         case G1_UP: return 256;  // 128 gate + 128 up columns
         case G2_DOWN:
-        case G5_DW13:
         case G6_DX: return s.d % 256 == 0 ? 256 : 128;
         case G3_DH:
-        case G4_DW2: return s.h % 256 == 0 ? 256 : 128;
+        case G4_DW2:
+        case G5_DW13: return s.h % 256 == 0 ? 256 : 128;  // N tiles never straddle W1 | W3
     }
     return 128;
 }
 
 cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     const moe_shape& s = g.s;
-    const int BN = gemm_bn(g.kind, s);
-    const uint64_t T = s.T, TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
+    // G2/G6 may cover a column chunk; their N tile must divide it.
+    const int BN = (g.kind == G2_DOWN || g.kind == G6_DX) ? (g.n_cols % 256 == 0 ? 256 : 128)
+                                                          : gemm_bn(g.kind, s);
+    const uint64_t TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
     Maps mp;
     bool ok = true;
     Params prm{};
@@ -566,52 +636,57 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     const int vm_mtiles = static_cast<int>(TK / BM) + s.E;
     int max_tiles = 0;
     switch (g.kind) {
-        case G1_UP:
-            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+        case G1_UP:  // A = x gathered; B = W1 | W3 [E*h, d], K-major
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 128);
             ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
+            mp.a = mp.b0;
             prm.Kdim = s.d;
             prm.n_tiles = s.h / 128;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
-        case G2_DOWN:
+        case G2_DOWN:  // A = SwiGLU output rows; B = W2 [E*d, h], K-major
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, h, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, BN);
             mp.b1 = mp.b0;
             prm.Kdim = s.h;
-            prm.n_tiles = s.d / BN;
+            prm.n_off = g.n_off;
+            prm.ldo = g.n_cols;
+            prm.n_tiles = g.n_cols / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
-        case G3_DH:
-            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+        case G3_DH:  // A = dy gathered; B = W2 [E*d, h] read MN-major
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, 64);
-            mp.b1 = mp.b0;
+            mp.a = mp.b1 = mp.b0;
             prm.Kdim = s.d;
             prm.n_tiles = s.h / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
-        case G4_DW2:
-            ok &= make_tmap_bf16(&mp.a, g.a_src, T, d, 64, 1);
+        case G4_DW2:  // A = dy gathered (MN-major, M = d); B = A' rows [TK, h]
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, h, 64, 64);
-            mp.b1 = mp.b0;
+            mp.a = mp.b1 = mp.b0;
             prm.M = s.d;
             prm.n_tiles = s.h / BN;
             max_tiles = s.E * (s.d / BM) * prm.n_tiles;
             break;
-        case G5_DW13:
-            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 64);
-            ok &= make_tmap_bf16(&mp.b0, g.b_src0, T, d, 64, 1);
-            mp.b1 = mp.b0;
-            prm.M = 2 * s.h;
-            prm.n_tiles = s.d / BN;
-            max_tiles = s.E * (2 * s.h / BM) * prm.n_tiles;
+        case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, 2h]
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, 2 * h, 64, 64);
+            mp.a = mp.b1 = mp.b0;
+            prm.M = s.d;
+            prm.n_tiles = 2 * s.h / BN;
+            max_tiles = s.E * (s.d / BM) * prm.n_tiles;
             break;
-        case G6_DX:
+        case G6_DX:  // A = dH rows [TK, 2h]; B = W1 | W3 [E*h, d] read MN-major
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 64);
             ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
             prm.Kdim = 2 * s.h;
-            prm.n_tiles = s.d / BN;
+            prm.n_off = g.n_off;
+            prm.ldo = g.n_cols;
+            prm.n_tiles = g.n_cols / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
     }

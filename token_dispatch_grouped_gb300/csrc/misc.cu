@@ -12,7 +12,8 @@
 //   dx_combine(C2)  dx_t = sum_k (dX~[row(t,k)] + dz_{t,k} W_g[e_{t,k}]), fp32,
 //                   k ascending. MoEBlaze paper notes 3.2 (token gradient
 //                   accumulation over the K routed rows).
-//   router_dwg(R2b) dW_g = dz^T x, as per-chunk partials then a fixed-order sum.
+//   router_dwg(R2b) dW_g = dz^T x as per-expert sums over the expert's rows
+//                   (partials over 32 row parts, then a fixed-order sum).
 // All sums run in a fixed order, so results are bit-reproducible.
 #include "common.cuh"
 
@@ -91,8 +92,10 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 constexpr int kCombThreads = 128;
 
 // One CTA per token of the chunk; each thread owns 8 columns per pass.
+// Y rows of the chunk buffer hold columns [c0, c0 + nc) of the expert outputs;
+// row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo).
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
+combine_kernel(int t0, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ Yc,
                __nv_bfloat16* __restrict__ y, int* err) {
@@ -105,11 +108,11 @@ combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
         const int e = ids[i];
         const Seg sg = seg[e];
         const int r = tim[i];
-        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (r - sg.lo)) * d;
+        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (r - sg.lo)) * nc;
         wk[threadIdx.x] = topk_w[i];
     }
     __syncthreads();
-    for (int c = threadIdx.x * 8; c < d; c += kCombThreads * 8) {
+    for (int c = threadIdx.x * 8; c < nc; c += kCombThreads * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = 0; k < K; ++k) {
             float f[8];
@@ -118,21 +121,24 @@ combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
         }
-        *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c) = f32_to_bf16x8(acc);
+        *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
     }
 }
 
 __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* __restrict__ dS_part,
                                  const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
-                                 float* __restrict__ dS, float* __restrict__ dz, int* err) {
+                                 float* __restrict__ dS, float* __restrict__ dz,
+                                 float* __restrict__ dz_row, int* err) {
     if (has_error(err)) return;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     float s[8], w[8];
+    int rows[8];
     float sbar = 0.f;
     for (int k = 0; k < K; ++k) {
         const size_t i = static_cast<size_t>(t) * K + k;
         const int r = tim[i];
+        rows[k] = r;
         float acc = 0.f;
         for (int p = 0; p < nparts; ++p) acc += dS_part[static_cast<size_t>(p) * TK + r];
         s[k] = acc;
@@ -141,13 +147,15 @@ __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* 
     }
     for (int k = 0; k < K; ++k) {
         const size_t i = static_cast<size_t>(t) * K + k;
+        const float z = w[k] * (s[k] - sbar);
         dS[i] = s[k];
-        dz[i] = w[k] * (s[k] - sbar);
+        dz[i] = z;
+        dz_row[rows[k]] = z;
     }
 }
 
 __global__ void __launch_bounds__(kCombThreads)
-dx_combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
+dx_combine_kernel(int t0, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
                   const float* __restrict__ dz, const int32_t* __restrict__ tim,
                   const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ dXc,
                   const float* __restrict__ Wg, __nv_bfloat16* __restrict__ dx, int* err) {
@@ -160,17 +168,17 @@ dx_combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
         const size_t i = static_cast<size_t>(t) * K + threadIdx.x;
         const int e = ids[i];
         const Seg sg = seg[e];
-        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * d;
+        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
         ek[threadIdx.x] = e;
         zk[threadIdx.x] = dz[i];
     }
     __syncthreads();
-    for (int c = threadIdx.x * 8; c < d; c += kCombThreads * 8) {
+    for (int c = threadIdx.x * 8; c < nc; c += kCombThreads * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = 0; k < K; ++k) {
             float f[8];
             bf16x8_to_f32(*reinterpret_cast<const uint4*>(dXc + row_off[k] + c), f);
-            const float* wg = Wg + static_cast<size_t>(ek[k]) * d + c;
+            const float* wg = Wg + static_cast<size_t>(ek[k]) * d + c0 + c;
             const float4 g0 = *reinterpret_cast<const float4*>(wg);
             const float4 g1 = *reinterpret_cast<const float4*>(wg + 4);
             const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
@@ -178,43 +186,66 @@ dx_combine_kernel(int t0, int d, int E, int K, const int32_t* __restrict__ ids,
 #pragma unroll
             for (int j = 0; j < 8; ++j) acc[j] += f[j] + z * gz[j];
         }
-        *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c) = f32_to_bf16x8(acc);
+        *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
     }
 }
 
-constexpr int kDwgCols = 64;
-constexpr int kDwgChunk = 2048;
+constexpr int kDwgParts = 32;      // row parts per expert
+constexpr int kDwgCols = 2048;     // columns per CTA (256 threads x 8)
 
-// grid (d / 64, nchunks); 64 threads, one column each; fp32 accumulators for
-// all E experts of the CTA's 64 columns live in shared memory.
-__global__ void __launch_bounds__(kDwgCols)
-router_dwg_part_kernel(int T, int d, int E, int K, const __nv_bfloat16* __restrict__ x,
-                       const int32_t* __restrict__ ids, const float* __restrict__ dz,
-                       float* __restrict__ part, int* err) {
+// dW_g[e] = sum over expert e's rows r of dz_row[r] * x[eti[r]] (the router
+// gradient dz^T x, with dz non-zero only at the chosen experts). grid =
+// (E, ceil(d / 2048), 32): CTA (e, cb, z) sums the z-th of 32 equal parts of
+// e's rows for 2048 columns, 8 per thread, rows in ascending order.
+__global__ void __launch_bounds__(256)
+router_dwg_part_kernel(int d, int E, const __nv_bfloat16* __restrict__ x,
+                       const int32_t* __restrict__ eti, const int32_t* __restrict__ offsets,
+                       const float* __restrict__ dz_row, float* __restrict__ part, int* err) {
     if (has_error(err)) return;
-    extern __shared__ float acc[];  // [E][64]
-    const int c = blockIdx.x * kDwgCols + threadIdx.x;
-    for (int e = 0; e < E; ++e) acc[e * kDwgCols + threadIdx.x] = 0.f;
-    const int ta = blockIdx.y * kDwgChunk;
-    const int tb = min(T, ta + kDwgChunk);
-    for (int t = ta; t < tb; ++t) {
-        const float xv = __bfloat162float(x[static_cast<size_t>(t) * d + c]);
-        for (int k = 0; k < K; ++k) {
-            const size_t i = static_cast<size_t>(t) * K + k;
-            acc[ids[i] * kDwgCols + threadIdx.x] += dz[i] * xv;
+    const int e = blockIdx.x;
+    const int c = blockIdx.y * kDwgCols + threadIdx.x * 8;
+    const int z = blockIdx.z;
+    const int lo = offsets[e], len = offsets[e + 1] - lo;
+    const int r0 = lo + static_cast<int>(static_cast<long long>(len) * z / kDwgParts);
+    const int r1 = lo + static_cast<int>(static_cast<long long>(len) * (z + 1) / kDwgParts);
+    if (c >= d) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int r = r0;
+    for (; r + 4 <= r1; r += 4) {
+        uint4 v[4];
+        float zz[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r + q]) * d + c);
+            zz[q] = dz_row[r + q];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float f[8];
+            bf16x8_to_f32(v[q], f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(zz[q], f[j], acc[j]);
         }
     }
-    float* out = part + static_cast<size_t>(blockIdx.y) * E * d;
-    for (int e = 0; e < E; ++e) out[static_cast<size_t>(e) * d + c] = acc[e * kDwgCols + threadIdx.x];
+    for (; r < r1; ++r) {
+        float f[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r]) * d + c), f);
+        const float zq = dz_row[r];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = fmaf(zq, f[j], acc[j]);
+    }
+    float* out = part + (static_cast<size_t>(z) * E + e) * d + c;
+    *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(out + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-__global__ void router_dwg_reduce_kernel(int n, int nchunks, const float* __restrict__ part,
+__global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
                                          float* __restrict__ dWg, int* err) {
     if (has_error(err)) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     float s = 0.f;
-    for (int q = 0; q < nchunks; ++q) s += part[static_cast<size_t>(q) * n + i];
+    for (int q = 0; q < kDwgParts; ++q) s += part[static_cast<size_t>(q) * n + i];
     dWg[i] = s;
 }
 
@@ -237,57 +268,51 @@ cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const in
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
+cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("combine", st);
-    combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, s.d, s.E, s.K, ids, topk_w, tim, seg, Yc,
-                                                     y, err);
+    combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, c0, nc, s.d, s.K, ids, topk_w, tim, seg,
+                                                     Yc, y, err);
     return cudaGetLastError();
 }
 
 cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
-                             int* err, cudaStream_t st) {
+                             float* dz_row, int* err, cudaStream_t st) {
     LaunchScope ls("router_dz", st);
     router_dz_kernel<<<(s.T + 127) / 128, 128, 0, st>>>(s.T, s.K, s.T * s.K, nparts, dS_part,
-                                                        topk_w, tim, dS, dz, err);
+                                                        topk_w, tim, dS, dz, dz_row, err);
     return cudaGetLastError();
 }
 
-cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, const int32_t* ids,
-                              const float* dz, const int32_t* tim, const Seg* seg,
-                              const __nv_bfloat16* dXc, const float* Wg, __nv_bfloat16* dx,
-                              int* err, cudaStream_t st) {
+cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc,
+                              const int32_t* ids, const float* dz, const int32_t* tim,
+                              const Seg* seg, const __nv_bfloat16* dXc, const float* Wg,
+                              __nv_bfloat16* dx, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("dx_combine", st);
-    dx_combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, s.d, s.E, s.K, ids, dz, tim, seg, dXc,
-                                                        Wg, dx, err);
+    dx_combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, c0, nc, s.d, s.K, ids, dz, tim, seg,
+                                                        dXc, Wg, dx, err);
     return cudaGetLastError();
 }
 
-int dwg_token_chunk() { return kDwgChunk; }
+int dwg_parts() { return kDwgParts; }
 
-cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* ids,
-                              const float* dz, float* part, float* dWg, int* err,
-                              cudaStream_t st) {
-    const int nchunks = (s.T + kDwgChunk - 1) / kDwgChunk;
-    const size_t smem = sizeof(float) * s.E * kDwgCols;
-    cudaError_t e = cudaFuncSetAttribute(router_dwg_part_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
+cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
+                              const int32_t* offsets, const float* dz_row, float* part,
+                              float* dWg, int* err, cudaStream_t st) {
     {
         LaunchScope ls("router_dwg", st);
-        router_dwg_part_kernel<<<dim3(s.d / kDwgCols, nchunks), kDwgCols, smem, st>>>(
-            s.T, s.d, s.E, s.K, x, ids, dz, part, err);
+        router_dwg_part_kernel<<<dim3(s.E, (s.d + kDwgCols - 1) / kDwgCols, kDwgParts), 256, 0,
+                                 st>>>(s.d, s.E, x, eti, offsets, dz_row, part, err);
     }
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n = s.E * s.d;
     LaunchScope ls("router_dwg_reduce", st);
-    router_dwg_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, nchunks, part, dWg, err);
+    router_dwg_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, part, dWg, err);
     return cudaGetLastError();
 }
 

@@ -7,11 +7,15 @@
 // Sources: MoEBlaze paper notes 2.1 (TopK(softmax(W_g x))); Dropless MoE, in
 // depth, "A reference implementation" (renormalise over the chosen k).
 //
-// Layout: one CTA of 256 threads owns BT tokens and all (padded) EP experts.
-// Thread (tg, eg) accumulates TT tokens x 8 experts in registers while a
-// K-chunk of x and W_g is staged transposed in shared memory. The EG threads
-// that share a token group sit in consecutive lanes of one warp, so the top-K
-// is a butterfly arg-max over those lanes, repeated K times.
+// Layout: one CTA of 256 threads owns BT tokens and all EP (padded) experts.
+// Thread (ks, tg, eg) accumulates TT tokens x 8 experts over a 1/KS slice of
+// every KC-wide chunk of the reduction; chunks of x and W_g are staged
+// transposed in shared memory, and the next chunk is already in registers
+// while the current one is used. The KS partial sums are added in a fixed
+// order through shared memory. The EG threads of one token group sit in
+// consecutive lanes of one warp, so the top-K is a butterfly arg-max over
+// those lanes, repeated K times. Few tokens per CTA (16..64) keep the grid
+// large for small T.
 #include <cfloat>
 
 #include "common.cuh"
@@ -20,15 +24,22 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKC = 32;  // reduction chunk staged per step
 
 template <int EP>
 struct RouterCfg {
-    static constexpr int TE = 8;
-    static constexpr int EG = EP / TE;
-    static constexpr int TG = kThreads / EG;
-    static constexpr int TT = EP == 8 ? 1 : EP == 16 ? 1 : EP == 32 ? 2 : EP == 64 ? 4 : 8;
+    static constexpr int EG = EP / 8;
+    static constexpr int KS = EP == 8 ? 16 : EP == 16 ? 8 : EP == 32 ? 4 : EP == 64 ? 2 : 1;
+    static constexpr int TG = kThreads / (EG * KS);
+    static constexpr int TT = EP <= 32 ? 1 : EP == 64 ? 2 : 4;
     static constexpr int BT = TG * TT;
+    static constexpr int KC = EP == 256 ? 64 : 128;
+    static constexpr int XU = BT * KC / 8;    // 16-byte x units per chunk
+    static constexpr int WU = EP * KC / 4;    // float4 W_g units per chunk
+    static constexpr int XPT = (XU + kThreads - 1) / kThreads;
+    static constexpr int WPT = (WU + kThreads - 1) / kThreads;
+    static constexpr int SMEM_STAGE = (KC * BT + KC * EP) * 4;
+    static constexpr int SMEM_RED = KS > 1 ? KS * BT * EP * 4 : 0;
+    static constexpr int SMEM = SMEM_STAGE > SMEM_RED ? SMEM_STAGE : SMEM_RED;
 };
 
 template <int EP>
@@ -40,12 +51,13 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
     using C = RouterCfg<EP>;
     if (has_error(err)) return;
     extern __shared__ __align__(16) float sm[];
-    float* Xs = sm;                  // [kKC][BT]
-    float* Ws = sm + kKC * C::BT;    // [kKC][EP]
+    float* Xs = sm;                   // [KC][BT]
+    float* Ws = sm + C::KC * C::BT;   // [KC][EP]
 
     const int tid = threadIdx.x;
     const int eg = tid % C::EG;
-    const int tg = tid / C::EG;
+    const int tg = (tid / C::EG) % C::TG;
+    const int ks = tid / (C::EG * C::TG);
     const int t0 = blockIdx.x * C::BT;
 
     float acc[C::TT][8];
@@ -54,49 +66,108 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
 
-    for (int k0 = 0; k0 < d; k0 += kKC) {
-        // x chunk: BT rows x 32 columns, 16-byte loads, stored transposed.
-        for (int c = tid; c < C::BT * (kKC / 8); c += kThreads) {
-            const int r = c / (kKC / 8);
-            const int cc = (c % (kKC / 8)) * 8;
-            const int t = t0 + r;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < T) v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0 + cc);
-            const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&v);
+    uint4 xr[C::XPT];
+    float4 wr[C::WPT];
+    auto fetch = [&](int k0) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) Xs[(cc + j) * C::BT + r] = __bfloat162float(b[j]);
+        for (int u = 0; u < C::XPT; ++u) {
+            const int c = tid + u * kThreads;
+            xr[u] = make_uint4(0, 0, 0, 0);
+            if (c < C::XU) {
+                const int r = c / (C::KC / 8);
+                const int t = t0 + r;
+                if (t < T)
+                    xr[u] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0 +
+                                                            (c % (C::KC / 8)) * 8);
+            }
         }
-        // W_g chunk: EP rows x 32 columns (rows >= E are zero), transposed.
-        for (int c = tid; c < EP * (kKC / 4); c += kThreads) {
-            const int e = c / (kKC / 4);
-            const int cc = (c % (kKC / 4)) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < E) v = *reinterpret_cast<const float4*>(Wg + static_cast<size_t>(e) * d + k0 + cc);
-            Ws[(cc + 0) * EP + e] = v.x;
-            Ws[(cc + 1) * EP + e] = v.y;
-            Ws[(cc + 2) * EP + e] = v.z;
-            Ws[(cc + 3) * EP + e] = v.w;
+#pragma unroll
+        for (int u = 0; u < C::WPT; ++u) {
+            const int c = tid + u * kThreads;
+            wr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c < C::WU) {
+                const int e = c / (C::KC / 4);
+                if (e < E)
+                    wr[u] = *reinterpret_cast<const float4*>(Wg + static_cast<size_t>(e) * d + k0 +
+                                                             (c % (C::KC / 4)) * 4);
+            }
         }
+    };
+    auto stage = [&]() {
+#pragma unroll
+        for (int u = 0; u < C::XPT; ++u) {
+            const int c = tid + u * kThreads;
+            if (c < C::XU) {
+                const int r = c / (C::KC / 8);
+                const int cc = (c % (C::KC / 8)) * 8;
+                const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&xr[u]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) Xs[(cc + j) * C::BT + r] = __bfloat162float(b[j]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < C::WPT; ++u) {
+            const int c = tid + u * kThreads;
+            if (c < C::WU) {
+                const int e = c / (C::KC / 4);
+                const int cc = (c % (C::KC / 4)) * 4;
+                Ws[(cc + 0) * EP + e] = wr[u].x;
+                Ws[(cc + 1) * EP + e] = wr[u].y;
+                Ws[(cc + 2) * EP + e] = wr[u].z;
+                Ws[(cc + 3) * EP + e] = wr[u].w;
+            }
+        }
+    };
+
+    fetch(0);
+    for (int k0 = 0; k0 < d; k0 += C::KC) {
+        __syncthreads();  // previous chunk fully consumed
+        stage();
         __syncthreads();
-#pragma unroll 4
-        for (int kk = 0; kk < kKC; ++kk) {
-            float xv[C::TT];
-            float wv[8];
+        if (k0 + C::KC < d) fetch(k0 + C::KC);  // in flight while this chunk is used
+        constexpr int KPT = C::KC / C::KS;
+#pragma unroll 8
+        for (int q = 0; q < KPT; ++q) {
+            const int kk = ks * KPT + q;
             const float4 w0 = *reinterpret_cast<const float4*>(Ws + kk * EP + eg * 8);
             const float4 w1 = *reinterpret_cast<const float4*>(Ws + kk * EP + eg * 8 + 4);
-            wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
-            wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int i = 0; i < C::TT; ++i) xv[i] = Xs[kk * C::BT + tg * C::TT + i];
+            for (int i = 0; i < C::TT; ++i) {
+                const float xv = Xs[kk * C::BT + tg * C::TT + i];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv, wv[j], acc[i][j]);
+            }
+        }
+    }
+
+    // Sum the KS partial results in a fixed order (ks = 0, 1, ...).
+    if constexpr (C::KS > 1) {
+        __syncthreads();
+        float* red = sm;  // [KS][BT][EP]
+#pragma unroll
+        for (int i = 0; i < C::TT; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                red[(ks * C::BT + tg * C::TT + i) * EP + eg * 8 + j] = acc[i][j];
+        __syncthreads();
+        if (ks == 0) {
 #pragma unroll
             for (int i = 0; i < C::TT; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+                for (int j = 0; j < 8; ++j) {
+                    float v = 0.f;
+                    for (int q = 0; q < C::KS; ++q)
+                        v += red[(q * C::BT + tg * C::TT + i) * EP + eg * 8 + j];
+                    acc[i][j] = v;
+                }
         }
-        __syncthreads();
     }
+    // Threads of the warps that hold ks == 0 finish; lanes with ks != 0 in such a
+    // warp take part in the shuffles but write nothing.
+    if ((tid / 32) * 32 >= C::EG * C::TG) return;
+    const bool owner = ks == 0;
 
-    // Bias, optional logits output.
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int e = eg * 8 + j;
@@ -104,7 +175,7 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
 #pragma unroll
         for (int i = 0; i < C::TT; ++i) acc[i][j] += b;
     }
-    if (logits != nullptr) {
+    if (logits != nullptr && owner) {
 #pragma unroll
         for (int i = 0; i < C::TT; ++i) {
             const int t = t0 + tg * C::TT + i;
@@ -117,14 +188,12 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
         }
     }
 
-    // Top-K per token: K rounds of a butterfly arg-max over the EG lanes.
 #pragma unroll
     for (int i = 0; i < C::TT; ++i) {
         const int t = t0 + tg * C::TT + i;
         uint32_t taken = 0;
         float zsel[8];
         int isel[8];
-        float z0 = 0.f;
 #pragma unroll 1
         for (int k = 0; k < K; ++k) {
             float bv = -INFINITY;
@@ -151,13 +220,12 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
             if (bi / 8 == eg && bi < E) taken |= 1u << (bi % 8);
             zsel[k] = bv;
             isel[k] = bi;
-            if (k == 0) z0 = bv;
         }
-        if (eg == 0 && t < T) {
+        if (owner && eg == 0 && t < T) {
             float den = 0.f;
             float ex[8];
             for (int k = 0; k < K; ++k) {
-                ex[k] = expf(zsel[k] - z0);
+                ex[k] = expf(zsel[k] - zsel[0]);
                 den += ex[k];
             }
             const float inv = 1.f / den;
@@ -178,7 +246,8 @@ cudaError_t launch_ep(const moe_shape& s, const __nv_bfloat16* x, const float* W
                       const float* bias, float* logits, int32_t* ids, float* w, int* err,
                       cudaStream_t st) {
     using C = RouterCfg<EP>;
-    const size_t smem = sizeof(float) * kKC * (C::BT + EP);
+    static_assert(C::EG * C::KS * C::TG == kThreads, "thread layout");
+    const size_t smem = C::SMEM;
     cudaError_t e = cudaFuncSetAttribute(router_kernel<EP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

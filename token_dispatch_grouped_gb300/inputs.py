@@ -46,6 +46,9 @@ WORKLOADS = {
     "fine": Shape(16384, 2048, 64, 6, 1408),
     "skew": Shape(32768, 2048, 128, 8, 768),
     "long": Shape(131072, 4096, 16, 4, 2048),
+    # Profiling-size case: the Mixtral-shaped experts (1024 rows each, d=4096,
+    # h=14336) with only 2 experts, so an ncu capture holds ~2 GB on the device.
+    "mixtral_e2": Shape(1024, 4096, 2, 2, 14336),
 }
 
 # Fixed per-tensor stream ids, so adding a tensor never shifts another one.
