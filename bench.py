@@ -79,44 +79,58 @@ def max_over_ranks(v: float, world: int) -> float:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons; start() before the
+    warm-up, mark() around the timed region, stop() keeps the samples taken
+    inside the marked window (at least the one nearest to it)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, dev_index: int):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.win = [None, None]
+        self.t_start = time.time()
         try:
             self.p = subprocess.Popen(
-                ["nvidia-smi", "-i", str(dev_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["nvidia-smi", "-i", str(dev_index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.p = None
 
+    def mark(self, i: int):
+        self.win[i] = time.time()
+
     def stop(self) -> dict:
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
         self.p.terminate()
         self.p.wait(timeout=10)
         self.f.flush()
         self.f.seek(0)
         rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        samples = []
         for r in rows:
             try:
-                sm.append(float(r[0]))
-                mx.append(float(r[1]))
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                samples.append((ts, float(r[1]), float(r[2]), [v.strip().lower() for v in r[4:8]]))
             except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, r[3:7]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        loaded = [v for v in sm if v > 0.5 * max(sm)] if sm else []
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        a, b = self.win
+        inside = [x for x in samples if a is not None and a <= x[0] <= b]
+        if not inside:  # window shorter than the sampling period: nearest sample
+            mid = 0.5 * (a + b) if a is not None else samples[-1][0]
+            inside = [min(samples, key=lambda x: abs(x[0] - mid))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for x in inside for n, v in zip(names, x[3]) if v == "active"})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "reasons": reasons,
+                "samples": len(inside)}
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline)
@@ -172,7 +186,7 @@ def workload_config(s, name):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="mixtral", choices=sorted(I.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -244,22 +258,24 @@ def main():
               "allocator_peak_delta_bytes": torch.cuda.max_memory_allocated(dev) - base_alloc}
 
     # ---- device-resident timing
+    clocks = ClockSampler(local)
     for _ in range(args.warmup):
         step(dv["x"], dv["dO"])
     torch.cuda.synchronize(dev)
     L.check_error()
-    clocks = ClockSampler(local)
     launches0 = B.moe_launch_count()
     B.moe_timing_enable(True)
     barrier(world)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark(0)
     e0.record(st)
     for _ in range(args.steps):
         step(dv["x"], dv["dO"])
     e1.record(st)
     torch.cuda.synchronize(dev)
+    clocks.mark(1)
     barrier(world)
     ms = e0.elapsed_time(e1)
     launches = B.moe_launch_count() - launches0

@@ -52,6 +52,7 @@ SMALL = [
     I.Shape(1500, 128, 16, 1, 256),   # K = 1 (router gradient is zero), 4 token chunks
     I.Shape(129, 384, 8, 8, 128),     # K = E = 8
     I.Shape(1100, 512, 8, 2, 256),    # passes split by output columns (d % 512 == 0)
+    I.Shape(2100, 512, 4, 2, 512),    # ~1000 rows per expert: CTA-pair (M = 256) tiles
 ]
 
 

@@ -37,9 +37,9 @@ struct LaunchScope {
 };
 
 // Tensor map of a 2D row-major bf16 array [rows, cols] with a box of
-// box_cols x box_rows and 128-byte swizzle. Returns false on failure.
+// box_cols x box_rows and 128-byte swizzle (or none). Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_cols, uint32_t box_rows);
+                    uint32_t box_cols, uint32_t box_rows, bool swizzle128 = true);
 
 int num_sms();
 

@@ -1,19 +1,25 @@
 // gemm.cu — grouped expert GEMMs on tcgen05 tensor cores (sm_103a).
 //
 // One persistent, warp-specialised kernel template serves the six expert
-// GEMMs of the layer. Per CTA (192 threads, one CTA per SM):
+// GEMMs of the layer. It runs either one CTA per tile (CTAS = 1, M = 128) or a
+// CTA pair per tile (CTAS = 2, cluster of two CTAs, tcgen05 cta_group::2,
+// M = 256 split 128/128, the B tile split by N so each SM stages half of it).
+// Warp roles in every CTA:
 //   warp 0      producer: TMA tile loads of the operands that are stored
 //               contiguously (weights, SwiGLU output, dH, A') into a ring of
 //               shared-memory stages.
+//   warp 1      TMEM owner; in the tile's first CTA one thread issues
+//               tcgen05.mma (bf16 in, fp32 accumulate) and tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               output row per thread), fused element-wise work, stores.
 //   warps 6..9  (gathering kinds) cp.async gather of the token-row operand
 //               through expert_token_indices, 16 bytes per thread, written in
 //               the 128-byte-swizzled layout the MMA descriptors expect; rows
 //               past an expert's end are zero-filled. No routed copy of the
 //               activations exists anywhere.
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma (128 x BN x 16,
-//               bf16 in, fp32 accumulate) and tcgen05.commit.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               output row per thread), fused element-wise work, bf16 stores.
+//   warp 10     (gathering kinds, second CTA of a pair) relays the completion
+//               of that CTA's gathers to the pair's MMA issuer: cp.async can
+//               only signal a barrier of its own CTA.
 // The accumulator is double-buffered in TMEM, so the epilogue of one tile
 // overlaps the main loop of the next. Tiles are walked in a static
 // round-robin over a device-side tile list derived from the per-expert row
@@ -40,6 +46,7 @@
 // ragged tails need no padding buffers (the other operand's extra rows are
 // multiplied by zeros).
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -49,8 +56,8 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BM = 128;                      // rows per CTA
+constexpr int BK = 64;                       // reduction depth per stage
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr int kMaxE = 256;
 
@@ -66,22 +73,27 @@ template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static conste
 template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
 template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0; };
 
-template <int BN>
+template <int BN, int CTAS>
 struct Cfg {
+    static constexpr int BNL = BN / CTAS;           // B rows (N) staged by this CTA
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int B_BYTES = BNL * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_TILES = STAGES * (A_BYTES + B_BYTES);
-    static constexpr int SMEM_MISC = 1024 + 16 * kMaxE + 4 * (kMaxE + 1);
-    static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC;
+    static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
+    static constexpr int SMEM_MISC = 7168;        // barriers, TMEM slot, segments, tile prefix
+    static constexpr int SMEM_EPI = 4 * 2 * 2048;  // per epilogue warp: two 32x32 bf16 boxes
+    static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC + SMEM_EPI;
+    static_assert(1024 + 16 * kMaxE + 4 * (kMaxE + 1) <= SMEM_MISC, "misc region");
+    static_assert(8 * (3 * STAGES + 4) + 16 <= 1024, "barrier region");
 };
 
-// Warp roles: 0 TMA producer, 1 MMA issuer (and TMEM owner), 2..5 epilogue,
-// 6..9 cp.async gather of the A operand (gathered kinds only).
 constexpr int kGatherThreads = 128;
-template <GemmKind KIND>
-constexpr int threads_of() { return Tr<KIND>::A_G ? 192 + kGatherThreads : 192; }
+template <GemmKind KIND, int CTAS>
+constexpr int threads_of() {
+    return 192 + (Tr<KIND>::A_G ? kGatherThreads : 0) + (Tr<KIND>::A_G && CTAS == 2 ? 32 : 0);
+}
 
 struct Params {
     int T, TK, d, h, E;
@@ -107,9 +119,9 @@ struct Tile {
 
 // Tile order inside one expert: M fastest, so tiles that run at the same time
 // share their B panel (a weight panel for the VM kinds, the A' or dH panel
-// for the weight gradients).
+// for the weight gradients). bmc = rows per tile (128 or 256).
 __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const Seg* segs, int E,
-                                            bool vk, int m_tiles_vk) {
+                                            bool vk, int m_tiles_vk, int bmc) {
     int lo = 0, hi = E;  // largest e with prefix[e] <= tile
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -123,7 +135,7 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
     t.hi = s.hi;
     t.out = s.out;
     const int local = tile - prefix[lo];
-    const int mt = vk ? m_tiles_vk : (s.hi - s.lo + BM - 1) / BM;
+    const int mt = vk ? m_tiles_vk : (s.hi - s.lo + bmc - 1) / bmc;
     t.m_blk = local % mt;
     t.n_blk = local / mt;
     return t;
@@ -177,17 +189,21 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <GemmKind KIND, int BN>
-__global__ void __launch_bounds__(threads_of<KIND>(), 1)
+template <GemmKind KIND, int BN, int CTAS>
+__global__ void __launch_bounds__(threads_of<KIND, CTAS>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB0,
-                    const __grid_constant__ CUtensorMap mapB1, const Params p) {
+                    const __grid_constant__ CUtensorMap mapB1,
+                    const __grid_constant__ CUtensorMap mapO, const Params p) {
     using TR = Tr<KIND>;
-    using C = Cfg<BN>;
+    using C = Cfg<BN, CTAS>;
     constexpr bool VK = TR::VK;
-    constexpr int NMMA = BN;  // MMA N (for G1: 128 gate + 128 up columns)
-    constexpr uint32_t IDESC = idesc_bf16(BM, NMMA, TR::A_MN, TR::B_MN);
-    // Bytes the TMA producer brings per stage (the gather warps bring A otherwise).
+    constexpr bool PAIR = CTAS == 2;
+    constexpr int BMC = BM * CTAS;  // rows per tile
+    constexpr int NMMA = BN;        // MMA N (for G1: 128 gate + 128 up columns)
+    constexpr int BNL = C::BNL;     // N columns whose B rows this CTA stages
+    constexpr uint32_t IDESC = idesc_bf16(BMC, NMMA, TR::A_MN, TR::B_MN);
+    // Bytes one CTA's TMA producer brings per stage (gather warps bring A otherwise).
     constexpr uint32_t TMA_BYTES = TR::A_G ? C::B_BYTES : C::A_BYTES + C::B_BYTES;
 
     extern __shared__ uint8_t smem_raw[];
@@ -197,23 +213,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const uint32_t sA = base_addr;
     const uint32_t sB = base_addr + C::STAGES * C::A_BYTES;
     uint8_t* misc = base + C::SMEM_TILES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);  // full[S], empty[S], tfull[2], tempty[2]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(misc);
     const uint32_t bar0 = smem_u32(bars);
+    // full[S], empty[S], gfull[S] (pair: this CTA's gathers), tfull[2], tempty[2]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * C::STAGES + 4));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * (2 * C::STAGES + 4) + 8);
+    auto gfull_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * C::STAGES + 2 + a); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (3 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * (3 * C::STAGES + 4) + 8);
     Seg* s_segs = reinterpret_cast<Seg*>(misc + 1024);
     int* s_prefix = reinterpret_cast<int*>(misc + 1024 + 16 * kMaxE);
+    uint8_t* epi = misc + C::SMEM_MISC;  // epilogue staging (TMA-store source)
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int E = p.E;
-    const int m_tiles_vk = VK ? p.M / BM : 0;
+    const int m_tiles_vk = VK ? p.M / BMC : 0;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int tile0 = blockIdx.x / CTAS;   // first tile of this CTA (pair)
+    const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
 
-    if (has_error(p.err)) return;
+    if (has_error(p.err)) return;  // uniform over the grid: both CTAs of a pair return
 
     // ---- setup: segments, tile prefix, barriers, TMEM
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];
@@ -223,16 +246,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int e = 0; e < E; ++e) {
             s_prefix[e] = run;
             const int rows = s_segs[e].hi - s_segs[e].lo;
-            run += VK ? m_tiles_vk * p.n_tiles : ((rows + BM - 1) / BM) * p.n_tiles;
+            run += VK ? m_tiles_vk * p.n_tiles : ((rows + BMC - 1) / BMC) * p.n_tiles;
         }
         s_prefix[E] = run;
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full_bar(s), 1 + (TR::A_G ? kGatherThreads : 0));
+            // full: the producer's expect-tx arrival, this CTA's gather threads,
+            // and in a pair the relay of the second CTA's gathers.
+            mbar_init(full_bar(s), 1 + (TR::A_G ? kGatherThreads : 0) + (TR::A_G && PAIR ? 1 : 0));
             mbar_init(empty_bar(s), 1);
+            mbar_init(gfull_bar(s), kGatherThreads);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), 4 * CTAS);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -241,64 +267,81 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         prefetch_tensormap(&mapA);
         prefetch_tensormap(&mapB0);
         prefetch_tensormap(&mapB1);
+        prefetch_tensormap(&mapO);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // the peer's barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = s_prefix[E];
+    // Barrier that collects a stage's loads for the MMA: the first CTA's full[s].
+    auto full_target = [&](int s) { return PAIR ? mapa_shared(full_bar(s), 0) : full_bar(s); };
 
     if (warp == 0) {
         // =========================== TMA producer
         int stage = 0;
         uint32_t phase = 0;
         bool stop = false;
-        for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
+        for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
-            const int row0 = t.lo + t.m_blk * BM;
+            const int row0 = t.lo + t.m_blk * BMC + rank * BM;   // VM: this CTA's A rows
+            const int ncol = t.n_blk * BN + rank * BNL;          // this CTA's B columns
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                     stop = true;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(full_bar(stage), TMA_BYTES);
+                if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(stage), CTAS * TMA_BYTES);
                 __syncwarp();
                 const uint32_t a_dst = sA + stage * C::A_BYTES;
                 const uint32_t b_dst = sB + stage * C::B_BYTES;
-                const uint32_t fb = full_bar(stage);
+                const uint32_t fb = full_target(stage);
                 const int k0 = kb * BK;
+                auto load = [&](uint32_t dst, const CUtensorMap* m, int c0, int c1) {
+                    if constexpr (PAIR) tma_load_2d_pair(dst, m, fb, c0, c1);
+                    else tma_load_2d(dst, m, fb, c0, c1);
+                };
                 if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
-                    if (lane == 0) tma_load_2d(a_dst, &mapA, fb, k0, row0);
+                    if (lane == 0) load(a_dst, &mapA, k0, row0);
                 }
                 if constexpr (KIND == G1_UP) {
+                    // B = 128 gate rows (W1) then 128 up rows (W3); in a pair the
+                    // first CTA stages W1's rows and the second W3's.
                     if (lane == 0) {
                         const int brow = t.e * p.h + t.n_blk * 128;
-                        tma_load_2d(b_dst, &mapB0, fb, k0, brow);
-                        tma_load_2d(b_dst + 16384, &mapB1, fb, k0, brow);
+                        if constexpr (PAIR) {
+                            load(b_dst, leader ? &mapB0 : &mapB1, k0, brow);
+                        } else {
+                            load(b_dst, &mapB0, k0, brow);
+                            load(b_dst + 16384, &mapB1, k0, brow);
+                        }
                     }
                 } else if constexpr (KIND == G2_DOWN) {
-                    if (lane == 0)
-                        tma_load_2d(b_dst, &mapB0, fb, k0, t.e * p.d + p.n_off + t.n_blk * BN);
+                    if (lane == 0) load(b_dst, &mapB0, k0, t.e * p.d + p.n_off + ncol);
                 } else if constexpr (KIND == G3_DH) {
-                    if (lane < BN / 64)
-                        tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
-                                    t.e * p.d + k0);
+                    if (lane < BNL / 64)
+                        load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.e * p.d + k0);
                 } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13) {
                     // B rows of this expert (A' for dW2, dH for dW1/dW3), MN-major.
-                    if (lane < BN / 64)
-                        tma_load_2d(b_dst + lane * 8192, &mapB0, fb, t.n_blk * BN + lane * 64,
-                                    t.lo + k0);
+                    if (lane < BNL / 64)
+                        load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.lo + k0);
                 } else {  // G6: K = 2h, first h from W1, then W3.
-                    if (lane < BN / 64) {
+                    if (lane < BNL / 64) {
                         const bool up = k0 >= p.h;
                         const int brow = t.e * p.h + (up ? k0 - p.h : k0);
-                        tma_load_2d(b_dst + lane * 8192, up ? &mapB1 : &mapB0, fb,
-                                    p.n_off + t.n_blk * BN + lane * 64, brow);
+                        load(b_dst + lane * 8192, up ? &mapB1 : &mapB0, p.n_off + ncol + lane * 64,
+                             brow);
                     }
                 }
                 if (++stage == C::STAGES) {
@@ -308,67 +351,78 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             }
         }
     } else if (warp == 1) {
-        // =========================== MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        int it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
-            const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
-            const int acc = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
-            if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + acc * NMMA;
-            bool ok = true;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!warp_wait(full_bar(stage), phase, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                // cp.async wrote A through the generic proxy; the MMA reads it
-                // through the async proxy.
-                if constexpr (TR::A_G) fence_proxy_async_smem();
+        // =========================== MMA issuer (first CTA of a pair)
+        if (leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
+                const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
+                const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_s = sA + stage * C::A_BYTES;
-                    const uint32_t b_s = sB + stage * C::B_BYTES;
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = TR::A_MN ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
-                                                     : sdesc_sw128(a_s + k * 32, 16, 1024);
-                        const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, 8192, 1024)
-                                                     : sdesc_sw128(b_s + k * 32, 16, 1024);
-                        mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                const uint32_t d_tmem = tmem_base + acc * NMMA;
+                bool ok = true;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!warp_wait(full_bar(stage), phase, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(empty_bar(stage));
+                    // cp.async wrote A through the generic proxy; the MMA reads it
+                    // through the async proxy.
+                    if constexpr (TR::A_G) fence_proxy_async_smem();
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a_s = sA + stage * C::A_BYTES;
+                        const uint32_t b_s = sB + stage * C::B_BYTES;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = TR::A_MN ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
+                                                         : sdesc_sw128(a_s + k * 32, 16, 1024);
+                            const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, 8192, 1024)
+                                                         : sdesc_sw128(b_s + k * 32, 16, 1024);
+                            if constexpr (PAIR) mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0);
+                            else mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        if constexpr (PAIR) mma_commit_pair(empty_bar(stage));
+                        else mma_commit(empty_bar(stage));
+                    }
+                    __syncwarp();
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    if constexpr (PAIR) mma_commit_pair(tfull_bar(acc));
+                    else mma_commit(tfull_bar(acc));
                 }
                 __syncwarp();
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(tfull_bar(acc));
-            __syncwarp();
         }
     } else if (warp < 6) {
         // =========================== epilogue (warps 2..5)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t* stg = epi + (warp - 2) * 4096;  // this warp's two 2 KB staging boxes
+        int nstore = 0;                           // TMA stores issued by this warp
         int it = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
+        for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
+            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + acc * NMMA;
+            const int rbase = t.lo + t.m_blk * BMC + rank * BM;  // VM: first row of this CTA
+            const int mbase = t.m_blk * BMC + rank * BM;         // VK: first output row
             float v[32];
             if constexpr (KIND == G1_UP) {
-                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
                 const int n0 = t.n_blk * 128;
                 __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0);
@@ -384,12 +438,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         store32_bf16(H + hrow + p.h + n0 + j, b);
                         float o[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = v[i] / (1.f + __expf(-v[i])) * b[i];
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __fdividef(v[i], 1.f + __expf(-v[i])) * b[i];
                         store32_bf16(Aact + static_cast<size_t>(r) * p.h + n0 + j, o);
                     }
                 }
             } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
-                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
                 const int n0 = t.n_blk * BN;
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
@@ -400,7 +455,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     if (valid) store32_bf16(out + j, v);
                 }
             } else if constexpr (KIND == G3_DH) {
-                const int r = t.lo + t.m_blk * BM + row_in_tile;
+                const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
                 const int n0 = t.n_blk * BN;
                 const size_t hrow = static_cast<size_t>(valid ? r : t.lo) * (2 * p.h);
@@ -419,7 +474,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         load32_bf16(H + p.h + n0 + j, b);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const float sg = 1.f / (1.f + __expf(-a[i]));
+                            const float sg = __fdividef(1.f, 1.f + __expf(-a[i]));
                             const float si = a[i] * sg;
                             const float Av = si * b[i];
                             dsum = fmaf(v[i], Av, dsum);
@@ -435,131 +490,231 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 }
                 if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
             } else if constexpr (KIND == G4_DW2) {
-                // dW2_e [d, h]: this thread owns row m (a d index), BN h-columns.
+                // dW2_e [d, h]: the warp's 32 rows x 32 columns at a time go through
+                // a shared-memory box and one TMA store (whole lines, asynchronous).
                 const bool empty = t.hi <= t.lo;
-                const int m = t.m_blk * BM + row_in_tile;
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
-                                     (static_cast<size_t>(t.e) * p.d + m) * p.h + t.n_blk * BN;
+                const int grow = t.e * p.d + mbase + q * 32;  // row in [E*d, h]
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32) {
+                for (int j = 0; j < BN; j += 32, ++nstore) {
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.f;
                     } else {
                         tmem_ld32f(tacc + j, v);
                     }
-                    store32_bf16(out + j, v);
+                    uint8_t* box = stg + (nstore & 1) * 2048;
+                    if (lane == 0) bulk_wait_group_read<1>();  // this box's previous store read it
+                    __syncwarp();
+                    store32_bf16(box + lane * 64, v);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&mapO, smem_u32(box), t.n_blk * BN + j, grow);
+                        bulk_commit_group();
+                    }
                 }
             } else {  // G5: tile of (x^T dH)_e [d, 2h]; transposed into dW1/dW3 [h, d]
+                // The warp's 32 d-rows x 32 n-columns are written transposed into
+                // a shared-memory box [n][m] and stored with one TMA store into
+                // dW1 or dW3 viewed as [E*h, d].
                 const bool empty = t.hi <= t.lo;
-                const int m = t.m_blk * BM + row_in_tile;  // d index
-                const int n0 = t.n_blk * BN;               // index into [0, 2h)
-                __nv_bfloat16* out =
-                    n0 < p.h ? static_cast<__nv_bfloat16*>(p.out0) +
-                                   (static_cast<size_t>(t.e) * p.h + n0) * p.d + m
-                             : static_cast<__nv_bfloat16*>(p.out1) +
-                                   (static_cast<size_t>(t.e) * p.h + (n0 - p.h)) * p.d + m;
+                const int n0 = t.n_blk * BN;  // index into [0, 2h); never straddles h
+                const bool first_half = n0 < p.h;
+                const int nrow = t.e * p.h + (first_half ? n0 : n0 - p.h);
+                const int mcol = mbase + q * 32;
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32) {
+                for (int j = 0; j < BN; j += 32, ++nstore) {
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.f;
                     } else {
                         tmem_ld32f(tacc + j, v);
                     }
+                    uint8_t* box = stg + (nstore & 1) * 2048;
+                    if (lane == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    __nv_bfloat16* bx = reinterpret_cast<__nv_bfloat16*>(box);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        out[static_cast<size_t>(j + i) * p.d] = __float2bfloat16_rn(v[i]);
+                    for (int i = 0; i < 32; ++i) bx[i * 32 + lane] = __float2bfloat16_rn(v[i]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(first_half ? &mapO : &mapB1, smem_u32(box), mcol, nrow + j);
+                        bulk_commit_group();
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                else mbar_arrive(tempty_bar(acc));
+            }
         }
-    } else if constexpr (TR::A_G) {
-        // =========================== cp.async gather of A (warps 6..9)
-        // Shared layout is the 128-byte swizzle that the MMA descriptors expect:
-        // 16-byte chunk c of a 128-byte smem row r lives at chunk c ^ (r & 7).
-        const int g = threadIdx.x - 192;  // 0..127
-        const int col16 = g & 7;
-        const size_t rowbytes = static_cast<size_t>(p.d) * 2;
-        const char* src0 = reinterpret_cast<const char*>(p.gsrc);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool stop = false;
-        for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
-            const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk);
-            const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    } else if (warp < 10) {
+        if constexpr (TR::A_G) {
+            // =========================== cp.async gather of A (warps 6..9)
+            // Shared layout is the 128-byte swizzle that the MMA descriptors
+            // expect: 16-byte chunk c of a 128-byte smem row r lives at chunk
+            // c ^ (r & 7). In a pair the second CTA's gathers complete on its own
+            // gfull barrier, which the relay warp forwards.
+            const int g = threadIdx.x - 192;  // 0..127
+            const int col16 = g & 7;
+            const size_t rowbytes = static_cast<size_t>(p.d) * 2;
+            const char* src0 = reinterpret_cast<const char*>(p.gsrc);
+            auto done_bar = [&](int s) { return leader ? full_bar(s) : gfull_bar(s); };
+            int stage = 0;
+            uint32_t phase = 0;
+            bool stop = false;
             if constexpr (!VK) {
-                // K-major A: 128 rows x 64 columns; this thread copies 16-byte
-                // chunk col16 of rows rb + 16 j, j = 0..7 (same rows every k-block).
+                // K-major A: 128 rows x 64 columns; this thread copies 16-byte chunk
+                // col16 of rows rb + 16 j, j = 0..7 (the same rows for every k-block
+                // of a tile). The next tile's row indices load while this one streams.
                 const int rb = g >> 3;
-                int idx[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int r = t.lo + t.m_blk * BM + rb + 16 * j;
-                    idx[j] = r < t.hi ? p.eti[r] : -1;
-                }
                 const uint32_t soff = static_cast<uint32_t>(rb * 128 + ((col16 ^ (rb & 7)) << 4));
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
-                        stop = true;
-                        break;
-                    }
-                    const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
-                    const size_t coff = static_cast<size_t>(kb * BK) * 2 + col16 * 16;
+                auto load_idx = [&](const Tile& tt, int (&dst)[8]) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
-                        cp_async16(a_dst + j * 16 * 128, src, idx[j] >= 0 ? 16u : 0u);
+                        const int r = tt.lo + tt.m_blk * BMC + rank * BM + rb + 16 * j;
+                        dst[j] = r < tt.hi ? p.eti[r] : -1;
                     }
-                    cp_async_arrive_noinc(full_bar(stage));
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                };
+                int idx[8], nidx[8];
+                int tile = tile0;
+                if (tile < num_tiles)
+                    load_idx(decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC), idx);
+                for (; tile < num_tiles && !stop; tile += tstep) {
+                    const int ntile = tile + tstep;
+                    if (ntile < num_tiles)
+                        load_idx(decode_tile(ntile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC),
+                                 nidx);
+                    const int num_kb = p.Kdim / BK;
+                    for (int kb = 0; kb < num_kb; ++kb) {
+                        if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
+                        const size_t coff = static_cast<size_t>(kb * BK) * 2 + col16 * 16;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
+                            cp_async16(a_dst + j * 16 * 128, src, idx[j] >= 0 ? 16u : 0u);
+                        }
+                        cp_async_arrive_noinc(done_bar(stage));
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) idx[j] = nidx[j];
                 }
             } else {
                 // MN-major A: 64 k-rows (tokens) x 128 m-columns in two 64-column
                 // chunks of 8 KB; this thread copies 16-byte chunk col16 of column
-                // chunk ch for token rows rb + 8 j, j = 0..7.
+                // chunk ch for token rows rb + 8 j, j = 0..7. Work items (tile,
+                // k-block) are walked with a one-item lookahead for the row indices;
+                // tiles of experts without rows have no k-blocks and are skipped.
                 const int ch = (g >> 3) & 1;
                 const int rb = g >> 4;
                 const uint32_t soff =
                     static_cast<uint32_t>(ch * 8192 + rb * 128 + ((col16 ^ (rb & 7)) << 4));
-                const size_t coff = static_cast<size_t>(t.m_blk * BM + ch * 64) * 2 + col16 * 16;
-                int idx[8], nxt[8];
-                auto load_idx = [&](int kb, int (&dst)[8]) {
+                struct Pos {
+                    int tile, kb, nkb;
+                    Tile t;
+                };
+                auto first_from = [&](int tile, Pos& ps) -> bool {
+                    for (; tile < num_tiles; tile += tstep) {
+                        const Tile tt = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
+                        const int nk = (tt.hi - tt.lo + BK - 1) / BK;
+                        if (nk > 0) {
+                            ps.tile = tile;
+                            ps.kb = 0;
+                            ps.nkb = nk;
+                            ps.t = tt;
+                            return true;
+                        }
+                    }
+                    return false;
+                };
+                auto load_idx = [&](const Pos& ps, int (&dst)[8]) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int r = t.lo + kb * BK + rb + 8 * j;
-                        dst[j] = r < t.hi ? p.eti[r] : -1;
+                        const int r = ps.t.lo + ps.kb * BK + rb + 8 * j;
+                        dst[j] = r < ps.t.hi ? p.eti[r] : -1;
                     }
                 };
-                if (num_kb > 0) load_idx(0, idx);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (kb + 1 < num_kb) load_idx(kb + 1, nxt);
+                Pos cur{};
+                bool have = first_from(tile0, cur);
+                int idx[8], nxt[8];
+                if (have) load_idx(cur, idx);
+                while (have && !stop) {
+                    Pos nx = cur;
+                    bool have_next;
+                    if (cur.kb + 1 < cur.nkb) {
+                        nx.kb = cur.kb + 1;
+                        have_next = true;
+                    } else {
+                        have_next = first_from(cur.tile + tstep, nx);
+                    }
+                    if (have_next) load_idx(nx, nxt);
                     if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         stop = true;
                         break;
                     }
                     const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
+                    const size_t coff =
+                        static_cast<size_t>(cur.t.m_blk * BMC + rank * BM + ch * 64) * 2 +
+                        col16 * 16;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
                         cp_async16(a_dst + j * 8 * 128, src, idx[j] >= 0 ? 16u : 0u);
                     }
-                    cp_async_arrive_noinc(full_bar(stage));
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) idx[j] = nxt[j];
+                    cp_async_arrive_noinc(done_bar(stage));
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) idx[j] = nxt[j];
+                    cur = nx;
+                    have = have_next;
+                }
+            }
+            cp_async_wait_all();
+        }
+    } else {
+        if constexpr (TR::A_G && PAIR) {
+            // =========================== relay (warp 10 of the second CTA)
+            // Waits for this CTA's gathered stage, makes it visible to the async
+            // proxy and arrives on the first CTA's full barrier.
+            if (!leader) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool stop = false;
+                for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
+                    const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
+                    const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
+                    for (int kb = 0; kb < num_kb; ++kb) {
+                        if (!warp_wait(gfull_bar(stage), phase, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(stage), 0));
+                        __syncwarp();
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
                 }
             }
         }
-        cp_async_wait_all();
     }
 
     // ---- teardown
@@ -572,27 +727,78 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // no peer still reads our smem or arrives on our barriers
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (warp == 1) {
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
 }
 
 // ------------------------------------------------------------------ host side
 struct Maps {
-    CUtensorMap a, b0, b1;
+    CUtensorMap a, b0, b1, o;
 };
 
-template <GemmKind KIND, int BN>
-cudaError_t launch_kind(const GemmProblem& g, const Maps& mp, const Params& prm, int max_tiles,
-                        cudaStream_t st, const char* name) {
-    using C = Cfg<BN>;
-    auto kfn = grouped_gemm_kernel<KIND, BN>;
+template <GemmKind KIND, int BN, int CTAS>
+cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
+                        const char* name) {
+    using C = Cfg<BN, CTAS>;
+    auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    const int grid = std::max(1, std::min(num_sms(), max_tiles));
+    const int units = std::max(1, std::min(num_sms() / CTAS, max_tiles));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(units * CTAS);
+    cfg.blockDim = dim3(threads_of<KIND, CTAS>());
+    cfg.dynamicSmemBytes = C::SMEM_TOTAL;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     LaunchScope ls(name, st);
-    kfn<<<grid, threads_of<KIND>(), C::SMEM_TOTAL, st>>>(mp.a, mp.b0, mp.b1, prm);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b0, mp.b1, mp.o, prm);
+}
+
+template <GemmKind KIND, int CTAS>
+cudaError_t launch_bn(int BN, const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
+                      const char* name) {
+    if constexpr (KIND == G1_UP) {
+        return launch_kind<KIND, 256, CTAS>(mp, prm, max_tiles, st, name);
+    } else {
+        return BN == 256 ? launch_kind<KIND, 256, CTAS>(mp, prm, max_tiles, st, name)
+                         : launch_kind<KIND, 128, CTAS>(mp, prm, max_tiles, st, name);
+    }
+}
+
+template <GemmKind KIND>
+cudaError_t launch_ctas(int ctas, int BN, const Maps& mp, const Params& prm, int max_tiles,
+                        cudaStream_t st, const char* name) {
+    return ctas == 2 ? launch_bn<KIND, 2>(BN, mp, prm, max_tiles, st, name)
+                     : launch_bn<KIND, 1>(BN, mp, prm, max_tiles, st, name);
+}
+
+// CTA pairs halve each SM's share of the B tile (more stages in flight) but
+// double the tile height. Measured on GB300 (Mixtral-shaped layer): the pair
+// speeds up the TMA-fed GEMMs (G2, G6) by 8-14% once experts hold a few
+// hundred rows, while the gathered kinds run 2-3x slower through the relay of
+// the second CTA's cp.async completions, so those stay on single CTAs.
+// MOE_GEMM_CTAS=1|2 forces one mode wherever it is legal (VK needs d % 256 == 0).
+int choose_ctas(GemmKind kind, const moe_shape& s) {
+    static const char* force = std::getenv("MOE_GEMM_CTAS");
+    const bool vk = kind == G4_DW2 || kind == G5_DW13;
+    const bool ok2 = vk ? (s.d % 256 == 0) : true;
+    if (force != nullptr && (force[0] == '1' || force[0] == '2'))
+        return (force[0] == '2' && ok2) ? 2 : 1;
+    const bool gathered = kind == G1_UP || kind == G3_DH || kind == G4_DW2 || kind == G5_DW13;
+    if (!ok2 || gathered) return 1;
+    const long long rows_per_expert = static_cast<long long>(s.T) * s.K / s.E;
+    return rows_per_expert >= 384 ? 2 : 1;
 }
 
 }  // namespace
@@ -614,7 +820,9 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     // G2/G6 may cover a column chunk; their N tile must divide it.
     const int BN = (g.kind == G2_DOWN || g.kind == G6_DX) ? (g.n_cols % 256 == 0 ? 256 : 128)
                                                           : gemm_bn(g.kind, s);
+    const int ctas = choose_ctas(g.kind, s);
     const uint64_t TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
+    const uint32_t bnl = static_cast<uint32_t>(BN / ctas);  // B rows staged per CTA
     Maps mp;
     bool ok = true;
     Params prm{};
@@ -633,22 +841,23 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     prm.err = g.err;
     // Upper bound on the tile count (rows of all experts + one partial tile
     // per expert), only used to size the persistent grid.
-    const int vm_mtiles = static_cast<int>(TK / BM) + s.E;
+    const int bmc = BM * ctas;
+    const int vm_mtiles = static_cast<int>(TK / bmc) + s.E;
     int max_tiles = 0;
     switch (g.kind) {
         case G1_UP:  // A = x gathered; B = W1 | W3 [E*h, d], K-major
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 128);
             ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
-            mp.a = mp.b0;
+            mp.a = mp.o = mp.b0;
             prm.Kdim = s.d;
             prm.n_tiles = s.h / 128;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
         case G2_DOWN:  // A = SwiGLU output rows; B = W2 [E*d, h], K-major
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, h, 64, 128);
-            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, BN);
-            mp.b1 = mp.b0;
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, bnl);
+            mp.b1 = mp.o = mp.b0;
             prm.Kdim = s.h;
             prm.n_off = g.n_off;
             prm.ldo = g.n_cols;
@@ -658,31 +867,35 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
         case G3_DH:  // A = dy gathered; B = W2 [E*d, h] read MN-major
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, 64);
-            mp.a = mp.b1 = mp.b0;
+            mp.a = mp.b1 = mp.o = mp.b0;
             prm.Kdim = s.d;
             prm.n_tiles = s.h / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
-        case G4_DW2:  // A = dy gathered (MN-major, M = d); B = A' rows [TK, h]
+        case G4_DW2:  // A = dy gathered (MN-major, M = d); B = A' rows [TK, h]; TMA-stored dW2
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, h, 64, 64);
+            ok &= make_tmap_bf16(&mp.o, g.out0, E * d, h, 32, 32, false);
             mp.a = mp.b1 = mp.b0;
             prm.M = s.d;
             prm.n_tiles = s.h / BN;
-            max_tiles = s.E * (s.d / BM) * prm.n_tiles;
+            max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
-        case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, 2h]
+        case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, 2h]; TMA-stored
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, 2 * h, 64, 64);
-            mp.a = mp.b1 = mp.b0;
+            ok &= make_tmap_bf16(&mp.o, g.out0, E * h, d, 32, 32, false);   // dW1
+            ok &= make_tmap_bf16(&mp.b1, g.out1, E * h, d, 32, 32, false);  // dW3
+            mp.a = mp.b0;
             prm.M = s.d;
             prm.n_tiles = 2 * s.h / BN;
-            max_tiles = s.E * (s.d / BM) * prm.n_tiles;
+            max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
         case G6_DX:  // A = dH rows [TK, 2h]; B = W1 | W3 [E*h, d] read MN-major
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 64);
             ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
+            mp.o = mp.b0;
             prm.Kdim = 2 * s.h;
             prm.n_off = g.n_off;
             prm.ldo = g.n_cols;
@@ -692,22 +905,12 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     }
     if (!ok) return cudaErrorInvalidValue;
     switch (g.kind) {
-        case G1_UP: return launch_kind<G1_UP, 256>(g, mp, prm, max_tiles, st, "g1_up_swiglu");
-        case G2_DOWN:
-            return BN == 256 ? launch_kind<G2_DOWN, 256>(g, mp, prm, max_tiles, st, "g2_down")
-                             : launch_kind<G2_DOWN, 128>(g, mp, prm, max_tiles, st, "g2_down");
-        case G3_DH:
-            return BN == 256 ? launch_kind<G3_DH, 256>(g, mp, prm, max_tiles, st, "g3_dh")
-                             : launch_kind<G3_DH, 128>(g, mp, prm, max_tiles, st, "g3_dh");
-        case G4_DW2:
-            return BN == 256 ? launch_kind<G4_DW2, 256>(g, mp, prm, max_tiles, st, "g4_dw2")
-                             : launch_kind<G4_DW2, 128>(g, mp, prm, max_tiles, st, "g4_dw2");
-        case G5_DW13:
-            return BN == 256 ? launch_kind<G5_DW13, 256>(g, mp, prm, max_tiles, st, "g5_dw13")
-                             : launch_kind<G5_DW13, 128>(g, mp, prm, max_tiles, st, "g5_dw13");
-        case G6_DX:
-            return BN == 256 ? launch_kind<G6_DX, 256>(g, mp, prm, max_tiles, st, "g6_dx")
-                             : launch_kind<G6_DX, 128>(g, mp, prm, max_tiles, st, "g6_dx");
+        case G1_UP: return launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu");
+        case G2_DOWN: return launch_ctas<G2_DOWN>(ctas, BN, mp, prm, max_tiles, st, "g2_down");
+        case G3_DH: return launch_ctas<G3_DH>(ctas, BN, mp, prm, max_tiles, st, "g3_dh");
+        case G4_DW2: return launch_ctas<G4_DW2>(ctas, BN, mp, prm, max_tiles, st, "g4_dw2");
+        case G5_DW13: return launch_ctas<G5_DW13>(ctas, BN, mp, prm, max_tiles, st, "g5_dw13");
+        case G6_DX: return launch_ctas<G6_DX>(ctas, BN, mp, prm, max_tiles, st, "g6_dx");
     }
     return cudaErrorInvalidValue;
 }
