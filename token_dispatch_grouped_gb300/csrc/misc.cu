@@ -15,6 +15,8 @@
 //   router_dwg(R2b) dW_g = dz^T x as per-expert sums over the expert's rows
 //                   (partials over 32 row parts, then a fixed-order sum).
 // All sums run in a fixed order, so results are bit-reproducible.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -89,39 +91,43 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
     return v;
 }
 
-constexpr int kCombThreads = 128;
+constexpr int kCombThreads = 256;   // 8 warps; one warp per token at a time
+constexpr int kCombWarps = kCombThreads / 32;
 
-// One CTA per token of the chunk; each thread owns 8 columns per pass.
-// Y rows of the chunk buffer hold columns [c0, c0 + nc) of the expert outputs;
+// Weighted combine of one chunk. Each warp takes a token (grid-stride), reads
+// its K (expert, position, weight) triples once, then every lane sums 8-column
+// pieces of the K expert-output rows in slot order and stores bf16. The chunk
+// buffer's rows hold columns [c0, c0 + nc) of the expert outputs, and
 // row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo).
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int t0, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
+combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ Yc,
                __nv_bfloat16* __restrict__ y, int* err) {
     if (has_error(err)) return;
-    const int t = t0 + blockIdx.x;
-    __shared__ size_t row_off[8];
-    __shared__ float wk[8];
-    if (threadIdx.x < K) {
-        const size_t i = static_cast<size_t>(t) * K + threadIdx.x;
-        const int e = ids[i];
-        const Seg sg = seg[e];
-        const int r = tim[i];
-        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (r - sg.lo)) * nc;
-        wk[threadIdx.x] = topk_w[i];
-    }
-    __syncthreads();
-    for (int c = threadIdx.x * 8; c < nc; c += kCombThreads * 8) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K; ++k) {
-            float f[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(Yc + row_off[k] + c), f);
-            const float w = wk[k];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
+    const int lane = threadIdx.x & 31;
+    for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
+         t += gridDim.x * kCombWarps) {
+        size_t off = 0;
+        float wl = 0.f;
+        if (lane < K) {
+            const size_t i = static_cast<size_t>(t) * K + lane;
+            const Seg sg = seg[ids[i]];
+            off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
+            wl = topk_w[i];
         }
-        *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
+        for (int c = lane * 8; c < nc; c += 32 * 8) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < K; ++k) {
+                const size_t ok = __shfl_sync(0xffffffffu, off, k);
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(Yc + ok + c), f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
+            }
+            *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
+        }
     }
 }
 
@@ -154,39 +160,45 @@ __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* 
     }
 }
 
+// Token-gradient sum of one chunk plus the router term:
+// dx_t = sum_k (dX~[row(t,k)] + dz_{t,k} W_g[e_{t,k}]), fp32, k ascending.
 __global__ void __launch_bounds__(kCombThreads)
-dx_combine_kernel(int t0, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
+dx_combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
                   const float* __restrict__ dz, const int32_t* __restrict__ tim,
                   const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ dXc,
                   const float* __restrict__ Wg, __nv_bfloat16* __restrict__ dx, int* err) {
     if (has_error(err)) return;
-    const int t = t0 + blockIdx.x;
-    __shared__ size_t row_off[8];
-    __shared__ int ek[8];
-    __shared__ float zk[8];
-    if (threadIdx.x < K) {
-        const size_t i = static_cast<size_t>(t) * K + threadIdx.x;
-        const int e = ids[i];
-        const Seg sg = seg[e];
-        row_off[threadIdx.x] = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
-        ek[threadIdx.x] = e;
-        zk[threadIdx.x] = dz[i];
-    }
-    __syncthreads();
-    for (int c = threadIdx.x * 8; c < nc; c += kCombThreads * 8) {
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int k = 0; k < K; ++k) {
-            float f[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(dXc + row_off[k] + c), f);
-            const float* wg = Wg + static_cast<size_t>(ek[k]) * d + c0 + c;
-            const float4 g0 = *reinterpret_cast<const float4*>(wg);
-            const float4 g1 = *reinterpret_cast<const float4*>(wg + 4);
-            const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const float z = zk[k];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] += f[j] + z * gz[j];
+    const int lane = threadIdx.x & 31;
+    for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
+         t += gridDim.x * kCombWarps) {
+        size_t off = 0;
+        int el = 0;
+        float zl = 0.f;
+        if (lane < K) {
+            const size_t i = static_cast<size_t>(t) * K + lane;
+            el = ids[i];
+            const Seg sg = seg[el];
+            off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
+            zl = dz[i];
         }
-        *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
+        for (int c = lane * 8; c < nc; c += 32 * 8) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int k = 0; k < K; ++k) {
+                const size_t ok = __shfl_sync(0xffffffffu, off, k);
+                const int e = __shfl_sync(0xffffffffu, el, k);
+                const float z = __shfl_sync(0xffffffffu, zl, k);
+                float f[8];
+                bf16x8_to_f32(*reinterpret_cast<const uint4*>(dXc + ok + c), f);
+                const float* wg = Wg + static_cast<size_t>(e) * d + c0 + c;
+                const float4 g0 = *reinterpret_cast<const float4*>(wg);
+                const float4 g1 = *reinterpret_cast<const float4*>(wg + 4);
+                const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += f[j] + z * gz[j];
+            }
+            *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) =
+                f32_to_bf16x8(acc);
+        }
     }
 }
 
@@ -268,13 +280,19 @@ cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const in
     return cudaGetLastError();
 }
 
+int comb_grid(int tokens) {
+    const int per_sm = 8;  // resident 256-thread CTAs per SM
+    const int need = (tokens + kCombWarps - 1) / kCombWarps;
+    return std::max(1, std::min(need, num_sms() * per_sm));
+}
+
 cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("combine", st);
-    combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, c0, nc, s.d, s.K, ids, topk_w, tim, seg,
-                                                     Yc, y, err);
+    combine_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, s.K, ids,
+                                                                topk_w, tim, seg, Yc, y, err);
     return cudaGetLastError();
 }
 
@@ -293,8 +311,8 @@ cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc
                               __nv_bfloat16* dx, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("dx_combine", st);
-    dx_combine_kernel<<<t1 - t0, kCombThreads, 0, st>>>(t0, c0, nc, s.d, s.K, ids, dz, tim, seg,
-                                                        dXc, Wg, dx, err);
+    dx_combine_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, s.K, ids,
+                                                                   dz, tim, seg, dXc, Wg, dx, err);
     return cudaGetLastError();
 }
 

@@ -76,9 +76,9 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
             if (c < C::XU) {
                 const int r = c / (C::KC / 8);
                 const int t = t0 + r;
-                if (t < T)
-                    xr[u] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0 +
-                                                            (c % (C::KC / 8)) * 8);
+                const int col = k0 + (c % (C::KC / 8)) * 8;  // chunks may run past d: zeros
+                if (t < T && col < d)
+                    xr[u] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + col);
             }
         }
 #pragma unroll
@@ -87,9 +87,9 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
             wr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (c < C::WU) {
                 const int e = c / (C::KC / 4);
-                if (e < E)
-                    wr[u] = *reinterpret_cast<const float4*>(Wg + static_cast<size_t>(e) * d + k0 +
-                                                             (c % (C::KC / 4)) * 4);
+                const int col = k0 + (c % (C::KC / 4)) * 4;
+                if (e < E && col < d)
+                    wr[u] = *reinterpret_cast<const float4*>(Wg + static_cast<size_t>(e) * d + col);
             }
         }
     };
