@@ -177,6 +177,11 @@ int moe_get_error(void* stream);
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 
+/* After a call returned MOE_ERR_CUDA: "<kernel>: <CUDA error string>" of that
+ * failure on the calling thread (empty if none). The pending launch error has
+ * already been cleared, so later calls are not affected by it. */
+const char* moe_last_cuda_error(void);
+
 /* ---- Instrumentation (host-side; off by default) ------------------------ */
 
 /* Number of kernels this library has launched in this process. */

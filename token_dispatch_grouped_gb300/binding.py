@@ -43,7 +43,10 @@ class MoeKernelTime(ctypes.Structure):
 class MoeError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        extra = ""
+        if code == MOE_ERR_CUDA:
+            extra = f" [{LIB.moe_last_cuda_error().decode()}]"
+        super().__init__(f"{where}: {status_string(code)} (status {code}){extra}")
 
 
 def _load() -> ctypes.CDLL:
@@ -63,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "moe_backward": (I, [MoeShape] + [P] * 19 + [S, P]),
         "moe_get_error": (I, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
+        "moe_last_cuda_error": (ctypes.c_char_p, []),
         "moe_launch_count": (L, []),
         "moe_timing_enable": (I, [I]),
         "moe_timing_collect": (I, [ctypes.POINTER(MoeKernelTime), I]),

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -197,16 +198,28 @@ size_t layout_dispatch(const moe_shape& s, void* ws, int32_t** hist) {
     return align_up(c.off, 256);
 }
 
-#define MOE_TRY(expr)                                \
-    do {                                             \
-        cudaError_t _e = (expr);                     \
-        if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
+// Last CUDA failure of a launch sequence, for moe_last_cuda_error().
+thread_local char g_last_cuda_error[160] = "";
+thread_local const char* g_current_launch = "";
+
+int record_cuda_error(cudaError_t e) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", g_current_launch,
+                  cudaGetErrorString(e));
+    cudaGetLastError();  // clear a non-sticky launch error so later calls start clean
+    return MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(expr)                                          \
+    do {                                                       \
+        cudaError_t _e = (expr);                               \
+        if (_e != cudaSuccess) return record_cuda_error(_e);   \
     } while (0)
 
 }  // namespace
 
 LaunchScope::LaunchScope(const char* name, cudaStream_t st) : name_(name), st_(st), slot_(-1) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    g_current_launch = name;
     if (!g_timing) return;
     std::lock_guard<std::mutex> lk(g_mu);
     Rec r;
@@ -487,6 +500,8 @@ const char* moe_status_string(int status) {
 }
 
 long long moe_launch_count(void) { return g_launches.load(); }
+
+const char* moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 int moe_timing_enable(int on) {
     std::lock_guard<std::mutex> lk(g_mu);

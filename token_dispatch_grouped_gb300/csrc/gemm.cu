@@ -73,7 +73,7 @@ template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static conste
 template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
 template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0; };
 
-template <int BN, int CTAS>
+template <int BN, int CTAS, int EPI_BOXES = 2>
 struct Cfg {
     static constexpr int BNL = BN / CTAS;           // B rows (N) staged by this CTA
     static constexpr int A_BYTES = BM * BK * 2;
@@ -83,13 +83,16 @@ struct Cfg {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
     static constexpr int SMEM_MISC = 7168;        // barriers, TMEM slot, segments, tile prefix
-    static constexpr int SMEM_EPI = 4 * 2 * 2048;  // per epilogue warp: two 32x32 bf16 boxes
+    static constexpr int SMEM_EPI = 4 * EPI_BOXES * 2048;  // per epilogue warp: 32x32 bf16 boxes
     static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC + SMEM_EPI;
     static_assert(1024 + 16 * kMaxE + 4 * (kMaxE + 1) <= SMEM_MISC, "misc region");
     static_assert(8 * (3 * STAGES + 4) + 16 <= 1024, "barrier region");
 };
 
 constexpr int kGatherThreads = 128;
+// Shared 2 KB staging boxes per epilogue warp (G3 writes three outputs per chunk).
+template <GemmKind KIND>
+constexpr int epi_boxes() { return KIND == G3_DH ? 3 : 2; }
 template <GemmKind KIND, int CTAS>
 constexpr int threads_of() {
     return 192 + (Tr<KIND>::A_G ? kGatherThreads : 0) + (Tr<KIND>::A_G && CTAS == 2 ? 32 : 0);
@@ -181,12 +184,116 @@ __device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
     }
 }
 
+__device__ __forceinline__ void load32_bf16(const uint4 (&u)[4], float (&v)[32]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            v[8 * q + 2 * j] = f.x;
+            v[8 * q + 2 * j + 1] = f.y;
+        }
+    }
+}
+
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     tmem_ld32(taddr, r);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- warp-cooperative row staging for the epilogues
+// A warp's 32 rows (one per lane) x 32 bf16 columns pass through a 2 KB shared
+// box so that global traffic is issued four lanes per 64-byte row segment (8
+// rows per instruction) instead of one lane per row. Inside the box, 16-byte
+// piece c of row l sits at piece c ^ ((l >> 1) & 3): row-wise writes by the
+// 32 lanes then hit 8 distinct 16-byte bank groups per 8 lanes.
+__device__ __forceinline__ uint32_t box_off(int row, int c16) {
+    return static_cast<uint32_t>(row * 64 + ((c16 ^ ((row >> 1) & 3)) << 4));
+}
+
+// Lane's own row (32 fp32 -> bf16) into the box.
+__device__ __forceinline__ void box_put_row(uint8_t* box, int lane, const float (&v)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 u;
+        u.x = pack_bf16(v[8 * c + 0], v[8 * c + 1]);
+        u.y = pack_bf16(v[8 * c + 2], v[8 * c + 3]);
+        u.z = pack_bf16(v[8 * c + 4], v[8 * c + 5]);
+        u.w = pack_bf16(v[8 * c + 6], v[8 * c + 7]);
+        *reinterpret_cast<uint4*>(box + box_off(lane, c)) = u;
+    }
+}
+
+// Stores the box to rows base + row * ld (row < nvalid), 16 bytes per lane.
+__device__ __forceinline__ void box_store_rows(const uint8_t* box, int lane, __nv_bfloat16* base,
+                                               size_t ld, int nvalid) {
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pc = lane + 32 * i;
+        const int row = pc >> 2, c16 = pc & 3;
+        if (row < nvalid)
+            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * ld + c16 * 8) =
+                *reinterpret_cast<const uint4*>(box + box_off(row, c16));
+    }
+    __syncwarp();
+}
+
+// Global pieces of rows base + row * ld (zeros for row >= nvalid) into registers.
+__device__ __forceinline__ void rows_fetch(uint4 (&pc4)[4], int lane, const __nv_bfloat16* base,
+                                           size_t ld, int nvalid) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pc = lane + 32 * i;
+        const int row = pc >> 2, c16 = pc & 3;
+        pc4[i] = row < nvalid ? *reinterpret_cast<const uint4*>(base + static_cast<size_t>(row) * ld +
+                                                                c16 * 8)
+                              : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Fetched pieces -> box -> the lane's own row as 4 x 8 packed bf16.
+__device__ __forceinline__ void box_get_row_raw(uint8_t* box, int lane, const uint4 (&pc4)[4],
+                                                uint4 (&u)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pc = lane + 32 * i;
+        *reinterpret_cast<uint4*>(box + box_off(pc >> 2, pc & 3)) = pc4[i];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const uint4*>(box + box_off(lane, c));
+    __syncwarp();
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 x = __bfloat1622float2(b[j]);
+        f[2 * j] = x.x;
+        f[2 * j + 1] = x.y;
+    }
+}
+
+// Fetched pieces -> box -> the lane's own row as 32 fp32.
+__device__ __forceinline__ void box_get_row(uint8_t* box, int lane, const uint4 (&pc4)[4],
+                                            float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int pc = lane + 32 * i;
+        *reinterpret_cast<uint4*>(box + box_off(pc >> 2, pc & 3)) = pc4[i];
+    }
+    __syncwarp();
+    uint4 u[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const uint4*>(box + box_off(lane, c));
+    __syncwarp();
+    load32_bf16(u, v);
 }
 
 template <GemmKind KIND, int BN, int CTAS>
@@ -196,7 +303,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB1,
                     const __grid_constant__ CUtensorMap mapO, const Params p) {
     using TR = Tr<KIND>;
-    using C = Cfg<BN, CTAS>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
     constexpr bool VK = TR::VK;
     constexpr bool PAIR = CTAS == 2;
     constexpr int BMC = BM * CTAS;  // rows per tile
@@ -408,7 +515,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* stg = epi + (warp - 2) * 4096;  // this warp's two 2 KB staging boxes
+        uint8_t* stg = epi + (warp - 2) * epi_boxes<KIND>() * 2048;  // this warp's boxes
         int nstore = 0;                           // TMA stores issued by this warp
         int it = 0;
         for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
@@ -422,70 +529,114 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const int mbase = t.m_blk * BMC + rank * BM;         // VK: first output row
             float v[32];
             if constexpr (KIND == G1_UP) {
-                const int r = rbase + row_in_tile;
-                const bool valid = r < t.hi;
+                const int row0w = rbase + q * 32;  // this warp's first row
+                const int nvalid = t.hi - row0w;
                 const int n0 = t.n_blk * 128;
-                __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0);
-                __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1);
+                __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) +
+                                   static_cast<size_t>(row0w > 0 ? row0w : 0) * (2 * p.h) + n0;
+                __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) +
+                                      static_cast<size_t>(row0w > 0 ? row0w : 0) * p.h + n0;
 #pragma unroll 1
                 for (int j = 0; j < 128; j += 32) {
                     float b[32];
                     tmem_ld32f(tacc + j, v);
                     tmem_ld32f(tacc + 128 + j, b);
-                    if (valid) {
-                        const size_t hrow = static_cast<size_t>(r) * (2 * p.h);
-                        store32_bf16(H + hrow + n0 + j, v);
-                        store32_bf16(H + hrow + p.h + n0 + j, b);
-                        float o[32];
+                    if (nvalid > 0) {
+                        box_put_row(stg, lane, v);
+                        box_store_rows(stg, lane, H + j, 2 * p.h, nvalid);
+                        box_put_row(stg, lane, b);
+                        box_store_rows(stg, lane, H + p.h + j, 2 * p.h, nvalid);
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            o[i] = __fdividef(v[i], 1.f + __expf(-v[i])) * b[i];
-                        store32_bf16(Aact + static_cast<size_t>(r) * p.h + n0 + j, o);
+                            v[i] = __fdividef(v[i], 1.f + __expf(-v[i])) * b[i];
+                        box_put_row(stg, lane, v);
+                        box_store_rows(stg, lane, Aact + j, p.h, nvalid);
                     }
                 }
             } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
-                const int r = rbase + row_in_tile;
-                const bool valid = r < t.hi;
-                const int n0 = t.n_blk * BN;
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out0) +
-                                     static_cast<size_t>(t.out + (r - t.lo)) * p.ldo + n0;
+                const int row0w = rbase + q * 32;
+                const int nvalid = t.hi - row0w;
+                __nv_bfloat16* out =
+                    static_cast<__nv_bfloat16*>(p.out0) +
+                    static_cast<size_t>(t.out + (row0w - t.lo)) * p.ldo + t.n_blk * BN;
 #pragma unroll 1
                 for (int j = 0; j < BN; j += 32) {
                     tmem_ld32f(tacc + j, v);
-                    if (valid) store32_bf16(out + j, v);
+                    if (nvalid > 0) {
+                        box_put_row(stg, lane, v);
+                        box_store_rows(stg, lane, out + j, p.ldo, nvalid);
+                    }
                 }
             } else if constexpr (KIND == G3_DH) {
                 const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
+                const int row0w = rbase + q * 32;
+                const int nvalid = t.hi - row0w;
                 const int n0 = t.n_blk * BN;
-                const size_t hrow = static_cast<size_t>(valid ? r : t.lo) * (2 * p.h);
-                const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.aux0) + hrow;
-                __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(p.out0) + hrow;
-                __nv_bfloat16* Ap = static_cast<__nv_bfloat16*>(p.out1) +
-                                    static_cast<size_t>(valid ? r : t.lo) * p.h;
+                const size_t r0 = static_cast<size_t>(row0w > 0 ? row0w : 0);
+                const __nv_bfloat16* Hw =
+                    static_cast<const __nv_bfloat16*>(p.aux0) + r0 * (2 * p.h) + n0;
+                __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * (2 * p.h) + n0;
+                __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
                 const float w = valid ? p.wrow[r] : 0.f;
                 float dsum = 0.f;
+                uint8_t* box_da = stg;
+                uint8_t* box_db = stg + 2048;
+                uint8_t* box_ap = stg + 4096;
+                // H (a | b) of the next 32 columns is fetched while this chunk is
+                // computed.
+                uint4 pa[4], pb[4];
+                if (nvalid > 0) {
+                    rows_fetch(pa, lane, Hw, 2 * p.h, nvalid);
+                    rows_fetch(pb, lane, Hw + p.h, 2 * p.h, nvalid);
+                }
 #pragma unroll 1
                 for (int j = 0; j < BN; j += 32) {
-                    tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
-                    if (valid) {
-                        float a[32], b[32], da[32], db[32], ap[32];
-                        load32_bf16(H + n0 + j, a);
-                        load32_bf16(H + p.h + n0 + j, b);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float sg = __fdividef(1.f, 1.f + __expf(-a[i]));
-                            const float si = a[i] * sg;
-                            const float Av = si * b[i];
-                            dsum = fmaf(v[i], Av, dsum);
-                            const float dA = w * v[i];
-                            da[i] = dA * b[i] * (sg + a[i] * sg * (1.f - sg));
-                            db[i] = dA * si;
-                            ap[i] = w * Av;
+                    uint4 ua[4], ub[4];
+                    if (nvalid > 0) {
+                        box_get_row_raw(box_da, lane, pa, ua);
+                        box_get_row_raw(box_db, lane, pb, ub);
+                        if (j + 32 < BN) {
+                            rows_fetch(pa, lane, Hw + j + 32, 2 * p.h, nvalid);
+                            rows_fetch(pb, lane, Hw + p.h + j + 32, 2 * p.h, nvalid);
                         }
-                        store32_bf16(dH + n0 + j, da);
-                        store32_bf16(dH + p.h + n0 + j, db);
-                        store32_bf16(Ap + n0 + j, ap);
+                    }
+                    tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
+                    if (nvalid > 0) {
+                        // 8 columns at a time: dA = w dA'; da = dA b SiLU'(a);
+                        // db = dA SiLU(a); A' = w SiLU(a) b; packed straight into
+                        // the three boxes.
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            float a8[8], b8[8], da8[8], db8[8], ap8[8];
+                            unpack8(ua[c], a8);
+                            unpack8(ub[c], b8);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float vk = v[8 * c + i];
+                                const float sg = __fdividef(1.f, 1.f + __expf(-a8[i]));
+                                const float si = a8[i] * sg;
+                                const float Av = si * b8[i];
+                                dsum = fmaf(vk, Av, dsum);
+                                const float dA = w * vk;
+                                da8[i] = dA * b8[i] * (sg + a8[i] * sg * (1.f - sg));
+                                db8[i] = dA * si;
+                                ap8[i] = w * Av;
+                            }
+                            uint4 u;
+                            u.x = pack_bf16(da8[0], da8[1]); u.y = pack_bf16(da8[2], da8[3]);
+                            u.z = pack_bf16(da8[4], da8[5]); u.w = pack_bf16(da8[6], da8[7]);
+                            *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = u;
+                            u.x = pack_bf16(db8[0], db8[1]); u.y = pack_bf16(db8[2], db8[3]);
+                            u.z = pack_bf16(db8[4], db8[5]); u.w = pack_bf16(db8[6], db8[7]);
+                            *reinterpret_cast<uint4*>(box_db + box_off(lane, c)) = u;
+                            u.x = pack_bf16(ap8[0], ap8[1]); u.y = pack_bf16(ap8[2], ap8[3]);
+                            u.z = pack_bf16(ap8[4], ap8[5]); u.w = pack_bf16(ap8[6], ap8[7]);
+                            *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = u;
+                        }
+                        box_store_rows(box_da, lane, dHw + j, 2 * p.h, nvalid);
+                        box_store_rows(box_db, lane, dHw + p.h + j, 2 * p.h, nvalid);
+                        box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
                     }
                 }
                 if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
@@ -743,7 +894,7 @@ struct Maps {
 template <GemmKind KIND, int BN, int CTAS>
 cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                         const char* name) {
-    using C = Cfg<BN, CTAS>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
     auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
