@@ -31,6 +31,9 @@ again in the design notes):
   * The renormalised weights equal a softmax over the K chosen logits (the
     full-softmax denominator cancels), so the router backward is the Jacobian
     of that K-way softmax, with zero gradient for unchosen experts.
+  * Non-gated experts ([MB-notes] 2.2, E_i(x) = W_2,i s(W_1,i x), with the
+    SiLU or ReLU activation of the MoEBlaze configurations): a = W1 x,
+    A = act(a), Y = W2 A; W3 is absent and the saved pre-activation is a.
 
 Everything is computed in float64 on the given values (the callers round
 activations and weights to bf16 first).
@@ -148,28 +151,59 @@ def silu_grad(u: np.ndarray) -> np.ndarray:
     return s + u * s * (1.0 - s)
 
 
-def expert_ffn(xe: np.ndarray, W1e: np.ndarray, W3e: np.ndarray, W2e: np.ndarray):
-    """One expert on its rows: a = xe W1e^T, b = xe W3e^T, A = SiLU(a) * b,
-    Y = A W2e^T. W1e, W3e are [h, d]; W2e is [d, h] (out x in)."""
+EXPERTS = ("swiglu", "silu", "relu")
+
+
+def relu(u: np.ndarray) -> np.ndarray:
+    return np.maximum(u, 0.0)
+
+
+def relu_grad(u: np.ndarray) -> np.ndarray:
+    return (u > 0).astype(np.float64)
+
+
+def act(u: np.ndarray, expert: str) -> np.ndarray:
+    """Activation of a non-gated expert."""
+    return silu(u) if expert == "silu" else relu(u)
+
+
+def act_grad(u: np.ndarray, expert: str) -> np.ndarray:
+    return silu_grad(u) if expert == "silu" else relu_grad(u)
+
+
+def expert_ffn(xe: np.ndarray, W1e: np.ndarray, W3e, W2e: np.ndarray, expert: str = "swiglu"):
+    """One expert on its rows. SwiGLU: a = xe W1e^T, b = xe W3e^T,
+    A = SiLU(a) * b, Y = A W2e^T. Non-gated: a = xe W1e^T, A = act(a),
+    Y = A W2e^T (b is None). W1e, W3e are [h, d]; W2e is [d, h] (out x in)."""
     a = xe @ W1e.T
-    b = xe @ W3e.T
-    A = silu(a) * b
+    if expert == "swiglu":
+        b = xe @ W3e.T
+        A = silu(a) * b
+    else:
+        b = None
+        A = act(a, expert)
     Y = A @ W2e.T
     return a, b, A, Y
 
 
-def layer_forward(x, W1, W3, W2, ids, w):
+def _w3(W3, expert):
+    return _as64(W3) if expert == "swiglu" else None
+
+
+def layer_forward(x, W1, W3, W2, ids, w, expert: str = "swiglu"):
     """Dropless forward with given routing. Returns dict with
-    y [T,d], H [TK, 2h] (a | b per sorted row), A [TK,h], Y [TK,d] (sorted row
-    order) and the dispatch index."""
+    y [T,d], H (saved pre-activations per sorted row: [TK, 2h] = (a | b) for
+    SwiGLU, [TK, h] = a otherwise), A [TK,h], Y [TK,d] (sorted row order) and
+    the dispatch index."""
     x = _as64(x)
-    W1, W3, W2 = _as64(W1), _as64(W3), _as64(W2)
+    W1, W3, W2 = _as64(W1), _w3(W3, expert), _as64(W2)
     ids = _asint(ids)
     w = _as64(w)
     T, K = ids.shape
     E, h, d = W1.shape
+    gated = expert == "swiglu"
     eti, offsets, tim, counts = build_dispatch(ids, E)
-    H = np.zeros((T * K, 2 * h))
+    H = np.zeros((T * K, 2 * h if gated else h))
     A = np.zeros((T * K, h))
     Y = np.zeros((T * K, d))
     for e in range(E):
@@ -177,9 +211,10 @@ def layer_forward(x, W1, W3, W2, ids, w):
         if hi == lo:
             continue
         xe = x[eti[lo:hi]]                       # read rows in place, no routed copy kept
-        a, b, Ae, Ye = expert_ffn(xe, W1[e], W3[e], W2[e])
+        a, b, Ae, Ye = expert_ffn(xe, W1[e], W3[e] if gated else None, W2[e], expert)
         H[lo:hi, :h] = a
-        H[lo:hi, h:] = b
+        if gated:
+            H[lo:hi, h:] = b
         A[lo:hi] = Ae
         Y[lo:hi] = Ye
     # [MB-notes] 2.3: y = sum over chosen experts of g_i(x) E_i(x), slot order.
@@ -190,11 +225,11 @@ def layer_forward(x, W1, W3, W2, ids, w):
     return dict(y=y, H=H, A=A, Y=Y, eti=eti, offsets=offsets, tim=tim, counts=counts)
 
 
-def dense_forward(x, W1, W3, W2, ids, w):
+def dense_forward(x, W1, W3, W2, ids, w, expert: str = "swiglu"):
     """Every expert on every token, then masked by the routing weights (a
     dense restatement used to pin the sparse forward on small inputs)."""
     x = _as64(x)
-    W1, W3, W2 = _as64(W1), _as64(W3), _as64(W2)
+    W1, W3, W2 = _as64(W1), _w3(W3, expert), _as64(W2)
     ids = _asint(ids)
     w = _as64(w)
     T, K = ids.shape
@@ -204,7 +239,7 @@ def dense_forward(x, W1, W3, W2, ids, w):
         gate[np.arange(T), ids[:, k]] += w[:, k]
     y = np.zeros((T, x.shape[1]))
     for e in range(E):
-        _, _, _, Ye = expert_ffn(x, W1[e], W3[e], W2[e])
+        _, _, _, Ye = expert_ffn(x, W1[e], None if W3 is None else W3[e], W2[e], expert)
         y += gate[:, e:e + 1] * Ye
     return y
 
@@ -227,19 +262,21 @@ def router_backward_dz(w: np.ndarray, dS: np.ndarray) -> np.ndarray:
     return dz
 
 
-def layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd=None):
+def layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd=None, expert: str = "swiglu"):
     """Hand-written backward with given routing. Returns dict with
-    dx [T,d], dWg [E,d], dW1, dW3 [E,h,d], dW2 [E,d,h], dS [T,K], dz [T,K]."""
+    dx [T,d], dWg [E,d], dW1, dW3 [E,h,d] (dW3 None for non-gated experts),
+    dW2 [E,d,h], dS [T,K], dz [T,K]."""
     dO = _as64(dO)
     x = _as64(x)
     Wg = _as64(Wg)
-    W1, W3, W2 = _as64(W1), _as64(W3), _as64(W2)
+    W1, W3, W2 = _as64(W1), _w3(W3, expert), _as64(W2)
     ids = _asint(ids)
     w = _as64(w)
     T, K = ids.shape
     E, h, d = W1.shape
+    gated = expert == "swiglu"
     if fwd is None:
-        fwd = layer_forward(x, W1, W3, W2, ids, w)
+        fwd = layer_forward(x, W1, W3, W2, ids, w, expert)
     eti, offsets, tim = fwd["eti"], fwd["offsets"], fwd["tim"]
     H, Y = fwd["H"], fwd["Y"]
     timm = tim.reshape(T, K)
@@ -254,7 +291,7 @@ def layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd=None):
     wrow = np.zeros(T * K)
     wrow[timm.reshape(-1)] = w.reshape(-1)
     dW1 = np.zeros_like(W1)
-    dW3 = np.zeros_like(W3)
+    dW3 = np.zeros_like(W3) if gated else None
     dW2 = np.zeros_like(W2)
     dxr = np.zeros((T * K, d))
     for e in range(E):
@@ -265,15 +302,20 @@ def layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd=None):
         xe = x[toks]
         dY = wrow[lo:hi, None] * dO[toks]
         a = H[lo:hi, :h]
-        b = H[lo:hi, h:]
-        A = silu(a) * b
         dA = dY @ W2[e]                     # Y = A W2e^T  =>  dA = dY W2e
-        da = dA * b * silu_grad(a)
-        db = dA * silu(a)
+        if gated:
+            b = H[lo:hi, h:]
+            A = silu(a) * b
+            da = dA * b * silu_grad(a)
+            db = dA * silu(a)
+            dW3[e] = db.T @ xe
+            dxr[lo:hi] = da @ W1[e] + db @ W3[e]
+        else:
+            A = act(a, expert)
+            da = dA * act_grad(a, expert)
+            dxr[lo:hi] = da @ W1[e]
         dW2[e] = dY.T @ A
         dW1[e] = da.T @ xe
-        dW3[e] = db.T @ xe
-        dxr[lo:hi] = da @ W1[e] + db @ W3[e]
     # Token-gradient accumulation over the K routed rows, slot order.
     dx = np.zeros((T, d))
     for k in range(K):
@@ -289,11 +331,11 @@ def layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd=None):
     return dict(dx=dx, dWg=dWg, dW1=dW1, dW3=dW3, dW2=dW2, dS=dS, dz=dzk)
 
 
-def layer_step(x, Wg, W1, W3, W2, dO, K: int, bias=None):
+def layer_step(x, Wg, W1, W3, W2, dO, K: int, bias=None, expert: str = "swiglu"):
     """Route, dispatch, forward and backward of one layer step (all fp64)."""
     z, p, ids, w = route(x, Wg, K, bias)
-    fwd = layer_forward(x, W1, W3, W2, ids, w)
-    bwd = layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd)
+    fwd = layer_forward(x, W1, W3, W2, ids, w, expert)
+    bwd = layer_backward(dO, x, Wg, W1, W3, W2, ids, w, fwd, expert)
     return dict(z=z, p=p, ids=ids, w=w, fwd=fwd, bwd=bwd)
 
 
@@ -302,7 +344,7 @@ def layer_step(x, Wg, W1, W3, W2, dO, K: int, bias=None):
 # the whole layer is too slow on the CPU). Each is the plain definition above,
 # restricted to the requested tokens or hidden units.
 # --------------------------------------------------------------------------
-def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
+def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w, expert: str = "swiglu"):
     """For the given tokens: y_t, dS_t, the expert part of dx_t, and dx_t with
     the router term. Works one token at a time with matrix-vector products."""
     tokens = _asint(tokens)
@@ -316,9 +358,11 @@ def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
     out_dx = np.zeros((len(tokens), d))
     cache = {}
 
-    def expert(e):
+    gated = expert == "swiglu"
+
+    def weights(e):
         if e not in cache:
-            cache[e] = (_as64(W1[e]), _as64(W3[e]), _as64(W2[e]))
+            cache[e] = (_as64(W1[e]), _as64(W3[e]) if gated else None, _as64(W2[e]))
         return cache[e]
 
     for i, t in enumerate(tokens):
@@ -328,17 +372,24 @@ def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
         dx_e = np.zeros(d)
         for k in range(K):
             e = int(ids[t, k])
-            W1e, W3e, W2e = expert(e)
+            W1e, W3e, W2e = weights(e)
             a = W1e @ xt
-            b = W3e @ xt
-            A = silu(a) * b
+            if gated:
+                b = W3e @ xt
+                A = silu(a) * b
+            else:
+                A = act(a, expert)
             Yk = W2e @ A
             Ys.append(Yk)
             out_y[i] += w[t, k] * Yk
             dA = W2e.T @ (w[t, k] * dOt)
-            da = dA * b * silu_grad(a)
-            db = dA * silu(a)
-            dx_e += W1e.T @ da + W3e.T @ db
+            if gated:
+                da = dA * b * silu_grad(a)
+                db = dA * silu(a)
+                dx_e += W1e.T @ da + W3e.T @ db
+            else:
+                da = dA * act_grad(a, expert)
+                dx_e += W1e.T @ da
         dS = np.array([dOt @ Yk for Yk in Ys])
         out_dS[i] = dS
         dzk = router_backward_dz(w[t:t + 1], dS[None, :])[0]
@@ -349,23 +400,28 @@ def tokens_forward_backward(tokens, x, dO, Wg, W1, W3, W2, ids, w):
     return out_y, out_dS, out_dx
 
 
-def hidden_unit_grads(e: int, j: int, x, dO, W1, W3, W2, ids, w):
-    """For expert e and hidden unit j: dW1[e][j,:], dW3[e][j,:] and
-    dW2[e][:,j], each summed over the tokens routed to e."""
+def hidden_unit_grads(e: int, j: int, x, dO, W1, W3, W2, ids, w, expert: str = "swiglu"):
+    """For expert e and hidden unit j: dW1[e][j,:], dW3[e][j,:] (None for
+    non-gated experts) and dW2[e][:,j], each summed over the tokens routed to e."""
     ids = _asint(ids)
     w = _as64(w)
     T, K = ids.shape
     sel_t, sel_k = np.nonzero(ids == e)
     d = W1.shape[2]
+    gated = expert == "swiglu"
     if len(sel_t) == 0:
-        return np.zeros(d), np.zeros(d), np.zeros(d)
+        return np.zeros(d), (np.zeros(d) if gated else None), np.zeros(d)
     xe = _as64(x[sel_t])
     dY = w[sel_t, sel_k][:, None] * _as64(dO[sel_t])
     W2e_j = _as64(W2[e][:, j])
     a = xe @ _as64(W1[e][j])
-    b = xe @ _as64(W3[e][j])
-    A = silu(a) * b
     dA = dY @ W2e_j
-    da = dA * b * silu_grad(a)
-    db = dA * silu(a)
-    return da @ xe, db @ xe, dY.T @ A
+    if gated:
+        b = xe @ _as64(W3[e][j])
+        A = silu(a) * b
+        da = dA * b * silu_grad(a)
+        db = dA * silu(a)
+        return da @ xe, db @ xe, dY.T @ A
+    A = act(a, expert)
+    da = dA * act_grad(a, expert)
+    return da @ xe, None, dY.T @ A

@@ -163,9 +163,20 @@ def test_forward_matches_sort_permute_pipeline():
 
 
 # ---------------------------------------------------------------- backward
-def _torch_layer(x, Wg, W1, W3, W2, ids, bias=None):
+def _torch_expert(xe, W1e, W3e, W2e, expert):
+    a = xe @ W1e.T
+    if expert == "swiglu":
+        A = torch.nn.functional.silu(a) * (xe @ W3e.T)
+    elif expert == "silu":
+        A = torch.nn.functional.silu(a)
+    else:
+        A = torch.relu(a)
+    return A @ W2e.T
+
+
+def _torch_layer(x, Wg, W1, W3, W2, ids, bias=None, expert="swiglu"):
     """Whole layer (full softmax, gather of the fixed top-K, renormalise,
-    per-expert SwiGLU, weighted sum) for torch autograd."""
+    per-expert FFN, weighted sum) for torch autograd."""
     z = x @ Wg.T
     if bias is not None:
         z = z + bias
@@ -179,15 +190,17 @@ def _torch_layer(x, Wg, W1, W3, W2, ids, bias=None):
             m = ids[:, k] == e
             if m.any():
                 xe = x[m]
-                Ye = (torch.nn.functional.silu(xe @ W1[e].T) * (xe @ W3[e].T)) @ W2[e].T
+                Ye = _torch_expert(xe, W1[e], None if W3 is None else W3[e], W2[e], expert)
                 y = y.index_add(0, torch.nonzero(m).squeeze(1), w[m, k:k + 1] * Ye)
     return y
 
 
-def _autograd_reference(inp, ids, bias=None):
-    leaves = {k: inp[k].double().clone().requires_grad_(True) for k in ("x", "Wg", "W1", "W3", "W2")}
-    y = _torch_layer(leaves["x"], leaves["Wg"], leaves["W1"], leaves["W3"], leaves["W2"],
-                     torch.from_numpy(ids), None if bias is None else torch.from_numpy(bias))
+def _autograd_reference(inp, ids, bias=None, expert="swiglu"):
+    names = ("x", "Wg", "W1", "W3", "W2") if expert == "swiglu" else ("x", "Wg", "W1", "W2")
+    leaves = {k: inp[k].double().clone().requires_grad_(True) for k in names}
+    y = _torch_layer(leaves["x"], leaves["Wg"], leaves["W1"], leaves.get("W3"), leaves["W2"],
+                     torch.from_numpy(ids), None if bias is None else torch.from_numpy(bias),
+                     expert)
     (y * inp["dO"].double()).sum().backward()
     return y.detach().numpy(), {k: v.grad.numpy() for k, v in leaves.items()}
 
@@ -318,3 +331,78 @@ def test_pins_catch_planted_router_sign(monkeypatch):
     monkeypatch.undo()
     assert not np.allclose(bad.sum(axis=1), 0.0)       # the sum-zero pin fails
     assert np.allclose(good.sum(axis=1), 0.0)
+
+
+# ---------------------------------------------------------------- non-gated experts
+@pytest.mark.parametrize("expert", ["silu", "relu"])
+def test_non_gated_matches_dense_and_autograd(expert):
+    s, inp = _small(T=36, d=12, E=5, K=3, h=20, seed=7)
+    st = O.layer_step(inp["x"], inp["Wg"], inp["W1"], None, inp["W2"], inp["dO"], s.K,
+                      expert=expert)
+    assert st["fwd"]["H"].shape == (s.T * s.K, s.h)
+    yd = O.dense_forward(inp["x"], inp["W1"], None, inp["W2"], st["ids"], st["w"], expert)
+    assert np.allclose(st["fwd"]["y"], yd, rtol=1e-12, atol=1e-12)
+    y_ref, g = _autograd_reference(inp, st["ids"], expert=expert)
+    assert np.allclose(st["fwd"]["y"], y_ref, rtol=1e-10, atol=1e-12)
+    b = st["bwd"]
+    assert b["dW3"] is None
+    for ours, ref in (("dx", "x"), ("dWg", "Wg"), ("dW1", "W1"), ("dW2", "W2")):
+        assert np.allclose(b[ours], g[ref], rtol=1e-9, atol=1e-11), ours
+
+
+def test_non_gated_finite_differences_silu():
+    s, inp = _small(T=10, d=6, E=4, K=2, h=8, seed=13)
+    st = O.layer_step(inp["x"], inp["Wg"], inp["W1"], None, inp["W2"], inp["dO"], 2,
+                      expert="silu")
+    base = {k: O._as64(inp[k]) for k in ("x", "Wg", "W1", "W2")}
+    dO = O._as64(inp["dO"])
+
+    def loss(v):
+        z, p, ids, w = O.route(v["x"], v["Wg"], 2)
+        assert np.array_equal(ids, st["ids"])
+        return float(np.sum(O.layer_forward(v["x"], v["W1"], None, v["W2"], ids, w, "silu")["y"] * dO))
+
+    rng = np.random.default_rng(3)
+    eps = 1e-6
+    for name, gname in (("x", "dx"), ("Wg", "dWg"), ("W1", "dW1"), ("W2", "dW2")):
+        for _ in range(4):
+            idx = tuple(rng.integers(0, n) for n in base[name].shape)
+            if name in ("W1", "W2"):
+                idx = (int(st["ids"][0, 0]),) + idx[1:]
+            vp = {k: v.copy() for k, v in base.items()}
+            vm = {k: v.copy() for k, v in base.items()}
+            vp[name][idx] += eps
+            vm[name][idx] -= eps
+            fd = (loss(vp) - loss(vm)) / (2 * eps)
+            an = st["bwd"][gname][idx]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, idx, fd, an)
+
+
+@pytest.mark.parametrize("expert", ["silu", "relu"])
+def test_non_gated_sampled_definitions(expert):
+    s, inp = _small(T=20, d=10, E=4, K=2, h=14, seed=9)
+    st = O.layer_step(inp["x"], inp["Wg"], inp["W1"], None, inp["W2"], inp["dO"], 2,
+                      expert=expert)
+    toks = [1, 8, 19]
+    y, dS, dx = O.tokens_forward_backward(toks, inp["x"], inp["dO"], inp["Wg"], inp["W1"], None,
+                                          inp["W2"], st["ids"], st["w"], expert)
+    assert np.allclose(y, st["fwd"]["y"][toks], rtol=1e-11, atol=1e-12)
+    assert np.allclose(dS, st["bwd"]["dS"][toks], rtol=1e-11, atol=1e-12)
+    assert np.allclose(dx, st["bwd"]["dx"][toks], rtol=1e-10, atol=1e-12)
+    for e in range(4):
+        g1, g3, g2 = O.hidden_unit_grads(e, 5, inp["x"], inp["dO"], inp["W1"], None, inp["W2"],
+                                         st["ids"], st["w"], expert)
+        assert g3 is None
+        assert np.allclose(g1, st["bwd"]["dW1"][e, 5], rtol=1e-10, atol=1e-12)
+        assert np.allclose(g2, st["bwd"]["dW2"][e, :, 5], rtol=1e-10, atol=1e-12)
+
+
+def test_pins_catch_planted_relu_grad_error(monkeypatch):
+    s, inp = _small(T=12, d=8, E=4, K=2, h=8)
+    z, p, ids, w = O.route(inp["x"], inp["Wg"], 2)
+    monkeypatch.setattr(O, "relu_grad", lambda u: np.ones_like(u))     # identity slope
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], None, inp["W2"], ids, w,
+                         expert="relu")
+    monkeypatch.undo()
+    _, g = _autograd_reference(inp, ids, expert="relu")
+    assert not np.allclose(b["dW1"], g["W1"], rtol=1e-6, atol=1e-8)
