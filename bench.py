@@ -31,13 +31,20 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 
 # Algorithmic FLOPs per step of each kernel family, in units of TK*d*h
-# (expert GEMMs: 18 TK d h in total; SonicMoE 3.4.5 counts (6 + 12) d n per token-expert).
+# (SwiGLU expert GEMMs: 18 TK d h in total; SonicMoE 3.4.5 counts (6 + 12) d n
+# per token-expert). Non-gated experts have no W3: 12 TK d h in total.
 GEMM_FLOP_UNITS = {"g1_up_swiglu": 4, "g2_down": 2, "g3_dh": 2, "g4_dw2": 2, "g5_dw13": 4,
                    "g6_dx": 4}
+GEMM_FLOP_UNITS_NON_GATED = {"g1_up_act": 2, "g2_down": 2, "g3_dh_act": 2, "g4_dw2": 2,
+                             "g5_dw13": 2, "g6_dx": 2}
+
+
+def gemm_flop_units(s) -> dict:
+    return GEMM_FLOP_UNITS if s.gated else GEMM_FLOP_UNITS_NON_GATED
 
 
 def flops_per_step(s) -> float:
-    return 18.0 * s.T * s.K * s.d * s.h + 6.0 * s.T * s.d * s.E
+    return sum(gemm_flop_units(s).values()) * s.T * s.K * s.d * s.h + 6.0 * s.T * s.d * s.E
 
 
 def load_peaks():
@@ -141,7 +148,7 @@ def cpu_oracle_sample(s, inp, tokens: int) -> tuple[float, int]:
     sl = slice(0, tokens)
     t0 = time.perf_counter()
     O.layer_step(inp["x"][sl], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], inp["dO"][sl], s.K,
-                 inp.get("bias"))
+                 inp.get("bias"), s.expert)
     return time.perf_counter() - t0, tokens
 
 
@@ -177,8 +184,9 @@ def run_reference(args, s, name):
 
 
 def workload_config(s, name):
-    return {"workload": f"{name}: T={s.T} d={s.d} E={s.E} K={s.K} h={s.h}", "T": s.T, "d": s.d,
-            "E": s.E, "K": s.K, "h": s.h, "global_batch_tokens": s.T,
+    return {"workload": f"{name}: T={s.T} d={s.d} E={s.E} K={s.K} h={s.h} expert={s.expert}",
+            "T": s.T, "d": s.d, "E": s.E, "K": s.K, "h": s.h, "expert": s.expert,
+            "global_batch_tokens": s.T,
             "l2": "working set > L2 (expert weights alone exceed 129 MB and are streamed every step)"}
 
 
@@ -212,7 +220,7 @@ def main():
 
     inp = I.make_layer_inputs(s, seed=0, with_bias=(name == "skew"))
     dv = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    L = MoELayer(s.T, s.d, s.E, s.K, s.h, device=dev)
+    L = MoELayer(s.T, s.d, s.E, s.K, s.h, device=dev, expert=s.expert)
     TK = s.T * s.K
     # Preallocated outputs (gradients are written, not accumulated).
     logits = torch.empty(s.T, s.E, dtype=torch.float32, device=dev)
@@ -223,7 +231,7 @@ def main():
                   torch.empty(s.E + 1, dtype=torch.int32, device=dev),
                   torch.empty(TK, dtype=torch.int32, device=dev))
     y = torch.empty(s.T, s.d, dtype=torch.bfloat16, device=dev)
-    H = torch.empty(TK, 2 * s.h, dtype=torch.bfloat16, device=dev)
+    H = torch.empty(TK, L.hs, dtype=torch.bfloat16, device=dev)
     grads = L.alloc_grads()
     bias = dv["bias"]
     st = torch.cuda.current_stream(dev)
@@ -292,8 +300,9 @@ def main():
     top = max(per_kernel.items(), key=lambda kv: kv[1][1])
     kname, (klaunches, kms) = top
     roof = None
-    if kname in GEMM_FLOP_UNITS:
-        per_launch_flop = GEMM_FLOP_UNITS[kname] * TK * s.d * s.h * args.steps / klaunches
+    units = gemm_flop_units(s)
+    if kname in units:
+        per_launch_flop = units[kname] * TK * s.d * s.h * args.steps / klaunches
         achieved = per_launch_flop / (kms / klaunches / 1e3) / 1e12
         peak = peaks["bf16_sus"]
         traffic = None

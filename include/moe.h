@@ -15,6 +15,9 @@
  *                       Y = A W2^T, read through expert_token_indices (no routed
  *                       copy of x); y_t = sum_k w_{t,k} Y_{t,k}.
  *                       [MoEBlaze paper notes 2.3, 5.1, Algorithm 1; SonicMoE 3.4.1]
+ *                       Non-gated experts (moe_shape.expert = SiLU or ReLU):
+ *                       A = act(a), no W3. [MoEBlaze paper notes 2.2, the
+ *                       two-layer expert E_i(x) = W_2,i s(W_1,i x)]
  *   moe_backward        dx, dW_g, dW1, dW3, dW2 and the router-score gradient
  *                       dS_{t,k} = <dO_t, Y_{t,k}> (computed as <dO W2, A>).
  *                       [MoEBlaze paper notes 3.2, Algorithm 1; SonicMoE 3.4.1]
@@ -29,7 +32,9 @@
  *     W1, W3, dW1, dW3: [E, h, d] bf16. W2, dW2: [E, d, h] bf16 (out x in).
  *     topk_ids: [T, K] int32, slot 0 = largest weight. topk_w, dS: [T, K] fp32.
  *     expert_token_indices, token_index_map: [TK] int32. offsets: [E+1] int32.
- *     H_saved: [TK, 2h] bf16, row r = (a | b) of the r-th expert-sorted row.
+ *     H_saved: [TK, hs] bf16 with hs = 2h for SwiGLU experts (row r = (a | b) of
+ *     the r-th expert-sorted row) and hs = h for non-gated experts (row r = a).
+ *     Non-gated experts have no W3: W3 and dW3 are ignored and may be NULL.
  *   - Ownership: the caller allocates and owns every buffer and the workspace.
  *     The library allocates no device memory and keeps no state between calls
  *     other than the optional kernel timer below.
@@ -44,9 +49,9 @@
  *     bounded wait that ran out) set a sticky device status word; kernels that
  *     start after it is set do nothing, and moe_get_error() reports it.
  *     No call traps or aborts the process.
- *   - Supported shapes: 1 <= T <= 2^24, 1 <= K <= 8, K <= E <= 256,
- *     d and h multiples of 128, d, h <= 32768, TK * 2h < 2^31 elements is NOT
- *     required (64-bit addressing is used throughout).
+ *   - Supported shapes: 1 <= T <= 2^24, 1 <= K <= 8, K <= E <= 256, TK < 2^31,
+ *     d and h multiples of 128 (h a multiple of 256 for non-gated experts),
+ *     d, h <= 32768. Buffers may exceed 2^31 elements (64-bit addressing).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -58,8 +63,16 @@
 extern "C" {
 #endif
 
+/* Expert function (moe_shape.expert). A zero-initialised shape is SwiGLU. */
+enum moe_expert_kind {
+    MOE_EXPERT_SWIGLU = 0, /* A = SiLU(x W1^T) * (x W3^T)          */
+    MOE_EXPERT_SILU = 1,   /* A = SiLU(x W1^T), no W3               */
+    MOE_EXPERT_RELU = 2    /* A = max(x W1^T, 0), no W3; ReLU'(0) = 0 */
+};
+
 typedef struct {
     int32_t T, d, E, K, h;
+    int32_t expert; /* enum moe_expert_kind */
 } moe_shape;
 
 enum moe_status_code {
@@ -146,9 +159,10 @@ int moe_build_dispatch_noalloc(moe_shape s, const int32_t* topk_ids,
                                int32_t* expert_token_indices, int32_t* expert_token_offsets,
                                int32_t* token_index_map, void* stream);
 
-/* Forward. Inputs: x, W1, W3, W2, the routing (topk_ids, topk_w) and its
- * dispatch index. Outputs: y [T,d] bf16 and H_saved [TK,2h] bf16 (the
- * pre-activations kept for the backward; SiLU is recomputed there).
+/* Forward. Inputs: x, W1, W3 (NULL allowed for non-gated experts), W2, the
+ * routing (topk_ids, topk_w) and its dispatch index. Outputs: y [T,d] bf16
+ * and H_saved [TK,hs] bf16 (the pre-activations kept for the backward; the
+ * activation is recomputed there).
  * No [TK,d] copy of the routed tokens is made: expert rows are gathered from x
  * through expert_token_indices by the GEMM's loads. */
 int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, const void* W2,
@@ -158,7 +172,8 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
                 void* y, void* H_saved, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward with upstream gradient dy [T,d] bf16. Outputs: dx [T,d] bf16
- * (expert and router paths), dWg [E,d] fp32, dW1, dW3 [E,h,d] bf16,
+ * (expert and router paths), dWg [E,d] fp32, dW1, dW3 [E,h,d] bf16 (dW3 is
+ * not written, and W3 not read, for non-gated experts),
  * dW2 [E,d,h] bf16 (an expert with no tokens gets exact zeros) and
  * dS [T,K] fp32 = <dy_t, Y_{t,k}>. Gradients are written, not accumulated. */
 int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg,

@@ -67,3 +67,38 @@ def test_oracle_is_not_imported_by_the_product():
     for py in glob.glob(os.path.join(pkg, "**", "*.py"), recursive=True):
         src = open(py).read()
         assert "oracle" not in re.findall(r"^\s*(?:from|import)\s+(\w+)", src, flags=re.M), py
+
+
+def test_non_gated_expert_shapes():
+    from token_dispatch_grouped_gb300 import binding as B
+    T, d, E, K, h = 4096, 1024, 16, 4, 4096
+    TK = T * K
+    gated = B.moe_workspace_size(B.shape(T, d, E, K, h), B.MOE_WS_BACKWARD)
+    for act in ("silu", "relu"):
+        s = B.shape(T, d, E, K, h, act)
+        assert s.expert == B.EXPERT_CODES[act]
+        bwd = B.moe_workspace_size(s, B.MOE_WS_BACKWARD)
+        # dH is [TK, h] instead of [TK, 2h]; the dX pass may also be planned differently
+        assert 0 < bwd < gated
+        assert bwd >= TK * h * 2 * 2           # dH and A' (bf16), each [TK, h]
+        assert B.moe_workspace_size(s, B.MOE_WS_FORWARD) == \
+            B.moe_workspace_size(B.shape(T, d, E, K, h), B.MOE_WS_FORWARD)
+    # a non-gated up-projection tile is 256 columns wide
+    assert B.moe_workspace_size(B.shape(T, d, E, K, 384, "silu"), B.MOE_WS_FORWARD) == 0
+    assert B.moe_workspace_size(B.shape(T, d, E, K, 384), B.MOE_WS_FORWARD) > 0
+    assert B.moe_workspace_size(B.shape(T, d, E, K, h, 3), B.MOE_WS_FORWARD) == 0
+
+
+def test_gated_expert_needs_w3_before_any_device_work():
+    from token_dispatch_grouped_gb300 import binding as B
+    s = B.shape(16, 128, 8, 2, 256)
+    fake = [256 * (i + 1) for i in range(19)]  # never dereferenced: rejected on the host
+    # moe_forward pointers: x, W1, W3, W2, ids, w, eti, offsets, tim, y, H, ws
+    args = [s, *fake[:2], None, *fake[3:12], 1 << 20, None]
+    assert B.LIB.moe_forward(*args) == B.MOE_ERR_INVALID_ARG
+    # moe_backward pointers: dy, x, Wg, W1, W3, W2, ids, w, eti, offsets, tim, H,
+    # dx, dWg, dW1, dW3, dW2, dS, ws
+    bw = [s, *fake[:4], None, *fake[5:19], 1 << 20, None]      # W3 missing
+    assert B.LIB.moe_backward(*bw) == B.MOE_ERR_INVALID_ARG
+    bw = [s, *fake[:15], None, *fake[16:19], 1 << 20, None]    # dW3 missing
+    assert B.LIB.moe_backward(*bw) == B.MOE_ERR_INVALID_ARG

@@ -21,7 +21,11 @@ GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
 def _layer(s):
     from token_dispatch_grouped_gb300.layer import MoELayer
-    return MoELayer(s.T, s.d, s.E, s.K, s.h)
+    return MoELayer(s.T, s.d, s.E, s.K, s.h, expert=s.expert)
+
+
+def _wgrad_keys(s):
+    return ("dW1", "dW3", "dW2") if s.gated else ("dW1", "dW2")
 
 
 def _check_route(z_gpu, ids_gpu, w_gpu, x, Wg, K, bias, rows=None):
@@ -53,10 +57,19 @@ SMALL = [
     I.Shape(129, 384, 8, 8, 128),     # K = E = 8
     I.Shape(1100, 512, 8, 2, 256),    # passes split by output columns (d % 512 == 0)
     I.Shape(2100, 512, 4, 2, 512),    # ~1000 rows per expert: CTA-pair (M = 256) tiles
+    # non-gated two-layer experts (SiLU / ReLU), no W3
+    I.Shape(300, 256, 6, 3, 512, "silu"),    # ragged tiles, two 256-wide up tiles
+    I.Shape(1500, 128, 16, 1, 256, "relu"),  # K = 1, 4 token chunks
+    I.Shape(1100, 512, 8, 2, 768, "relu"),   # column-split passes, three up tiles
+    I.Shape(2100, 512, 4, 2, 256, "silu"),   # CTA-pair down / dX GEMMs
 ]
 
 
-@pytest.mark.parametrize("s", SMALL, ids=lambda s: f"T{s.T}d{s.d}E{s.E}K{s.K}h{s.h}")
+def _sid(s):
+    return f"T{s.T}d{s.d}E{s.E}K{s.K}h{s.h}" + ("" if s.gated else f"-{s.expert}")
+
+
+@pytest.mark.parametrize("s", SMALL, ids=_sid)
 def test_layer_small_full_parity(s):
     inp = I.make_layer_inputs(s, seed=1)
     dv = to_dev(inp)
@@ -67,12 +80,14 @@ def test_layer_small_full_parity(s):
     _check_dispatch(r.ids, dp, s.E)
     # Layer parity on the GPU's own routing (ids and fp32 weights as inputs).
     ids, w = cpu(r.ids), cpu(r.w)
-    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w)
-    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w, s.expert)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f,
+                         s.expert)
+    assert H.shape == (s.TK, 2 * s.h if s.gated else s.h)
     assert rel_fro(cpu(H), f["H"]) <= TOL_BF16
     assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
     assert rel_fro(cpu(g["dS"]), b["dS"]) <= TOL_BF16
-    for k in ("dx", "dW1", "dW3", "dW2"):
+    for k in ("dx",) + _wgrad_keys(s):
         assert rel_fro(cpu(g[k]), b[k]) <= TOL_BF16, k
     if s.K == 1:
         assert np.all(cpu(g["dWg"]) == 0.0)
@@ -80,8 +95,9 @@ def test_layer_small_full_parity(s):
         assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
 
 
-def test_injected_routing_skewed_and_empty_experts():
-    s = I.Shape(700, 256, 16, 4, 256)
+@pytest.mark.parametrize("expert", ["swiglu", "relu"])
+def test_injected_routing_skewed_and_empty_experts(expert):
+    s = I.Shape(700, 256, 16, 4, 256, expert)
     inp = I.make_layer_inputs(s, seed=2)
     ids = I.random_ids(s.T, 12, s.K, seed=5, skew=1.5)      # experts 12..15 get no token
     w = I.random_weights(s.T, s.K, seed=5)
@@ -93,17 +109,19 @@ def test_injected_routing_skewed_and_empty_experts():
     y, H = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp)
     grads = L.alloc_grads()
     for t in grads.values():                                 # poison: every element must be written
-        t.fill_(float("nan"))
+        if t is not None:
+            t.fill_(float("nan"))
     L.backward(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r, dp, H, grads)
     L.check_error()
     _check_dispatch(r.ids, dp, s.E)
-    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w)
-    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w, expert)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f,
+                         expert)
     assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
-    for k in ("dx", "dW1", "dW3", "dW2", "dS", "dWg"):
+    for k in ("dx", "dS", "dWg") + _wgrad_keys(s):
         assert not np.isnan(cpu(grads[k])).any(), k
         assert rel_fro(cpu(grads[k]), b[k]) <= TOL_BF16, k
-    for k in ("dW1", "dW3", "dW2"):
+    for k in _wgrad_keys(s):
         assert np.all(cpu(grads[k])[12:] == 0.0)
 
 
@@ -203,7 +221,8 @@ def _full(name):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mixtral", "fine", "skew", "long"])
+@pytest.mark.parametrize("name", ["mixtral", "fine", "skew", "long", "moeblaze_conf7",
+                                  "moeblaze_conf4"])
 def test_full_workload_sampled(name):
     s, inp, r, dp, y, H, g = _full(name)
     rng = np.random.default_rng(0)
@@ -217,7 +236,7 @@ def test_full_workload_sampled(name):
     if name == "skew":
         assert (counts == 0).sum() >= 4
     ys, dSs, dxs = O.tokens_forward_backward(toks, inp["x"], inp["dO"], inp["Wg"], inp["W1"],
-                                             inp["W3"], inp["W2"], ids, w)
+                                             inp["W3"], inp["W2"], ids, w, s.expert)
     assert rel_fro(cpu(y)[toks], ys) <= TOL_BF16
     assert rel_fro(cpu(g["dS"])[toks], dSs) <= TOL_BF16
     assert rel_fro(cpu(g["dx"])[toks], dxs) <= TOL_BF16
@@ -226,9 +245,10 @@ def test_full_workload_sampled(name):
     for e in rng.choice(busy, size=min(2, len(busy)), replace=False):
         j = int(rng.integers(0, s.h))
         g1, g3, g2 = O.hidden_unit_grads(int(e), j, inp["x"], inp["dO"], inp["W1"], inp["W3"],
-                                         inp["W2"], ids, w)
+                                         inp["W2"], ids, w, s.expert)
         assert rel_fro(cpu(g["dW1"][e, j]), g1) <= TOL_BF16
-        assert rel_fro(cpu(g["dW3"][e, j]), g3) <= TOL_BF16
+        if s.gated:
+            assert rel_fro(cpu(g["dW3"][e, j]), g3) <= TOL_BF16
         assert rel_fro(cpu(g["dW2"][e, :, j]), g2) <= TOL_BF16
     # properties at any size: dW_g rows sum to zero over experts (sum_k dz_k = 0),
     # empty experts have exact-zero weight gradients, outputs are finite

@@ -29,10 +29,13 @@ MOE_NOALLOC_DISPATCH_MAX_ENTRIES = 1 << 20
 
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_FORWARD, MOE_WS_BACKWARD = 0, 1, 2, 3
 
+MOE_EXPERT_SWIGLU, MOE_EXPERT_SILU, MOE_EXPERT_RELU = 0, 1, 2
+EXPERT_CODES = {"swiglu": MOE_EXPERT_SWIGLU, "silu": MOE_EXPERT_SILU, "relu": MOE_EXPERT_RELU}
+
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("h", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("h", ctypes.c_int32), ("expert", ctypes.c_int32)]
 
 
 class MoeKernelTime(ctypes.Structure):
@@ -81,8 +84,9 @@ def _load() -> ctypes.CDLL:
 LIB = _load()
 
 
-def shape(T: int, d: int, E: int, K: int, h: int) -> MoeShape:
-    return MoeShape(T, d, E, K, h)
+def shape(T: int, d: int, E: int, K: int, h: int, expert: str | int = "swiglu") -> MoeShape:
+    code = EXPERT_CODES[expert] if isinstance(expert, str) else int(expert)
+    return MoeShape(T, d, E, K, h, code)
 
 
 def _ptr(t) -> int | None:

@@ -89,8 +89,17 @@ int check_shape(const moe_shape& s) {
     if (s.d % 128 != 0 || s.h % 128 != 0 || s.d > 32768 || s.h > 32768)
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (static_cast<long long>(s.T) * s.K >= (1ll << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s.expert != MOE_EXPERT_SWIGLU && s.expert != MOE_EXPERT_SILU && s.expert != MOE_EXPERT_RELU)
+        return MOE_ERR_INVALID_ARG;
+    // A non-gated up-projection tile is 256 columns of W1.
+    if (s.expert != MOE_EXPERT_SWIGLU && s.h % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
+
+bool gated(const moe_shape& s) { return s.expert == MOE_EXPERT_SWIGLU; }
+
+// Width of the saved pre-activation H and of its gradient dH.
+size_t hs_of(const moe_shape& s) { return gated(s) ? 2 * static_cast<size_t>(s.h) : s.h; }
 
 int nchunks_of(const moe_shape& s, int tc) { return (s.T + tc - 1) / tc; }
 
@@ -129,7 +138,8 @@ Plan plan_down(const moe_shape& s) {
 
 Plan plan_dx(const moe_shape& s) {
     const double TK = static_cast<double>(s.T) * s.K;
-    return make_plan(s, 4.0 * s.E * s.d * s.h, 4.0 * TK * s.h);
+    const double hs = static_cast<double>(hs_of(s));
+    return make_plan(s, 2.0 * s.E * s.d * hs, 2.0 * TK * hs);
 }
 
 size_t chunk_buffer_elems(const moe_shape& s, const Plan& p) {
@@ -182,7 +192,7 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     w.dz = c.take<float>(TK);
     w.dz_row = c.take<float>(TK);
     w.Ap = c.take<__nv_bfloat16>(TK * s.h);
-    w.dH = c.take<__nv_bfloat16>(TK * 2 * s.h);
+    w.dH = c.take<__nv_bfloat16>(TK * hs_of(s));
     w.dXc = c.take<__nv_bfloat16>(chunk_buffer_elems(s, plan_dx(s)));
     w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
     if (o) *o = w;
@@ -328,11 +338,12 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
                 size_t ws_bytes, void* stream) {
     int rc = check_shape(s);
     if (rc) return rc;
-    if (!x || !W1 || !W3 || !W2 || !topk_ids || !topk_w || !eti || !offsets || !tim || !y ||
-        !H_saved || !ws)
+    if (!x || !W1 || (gated(s) && !W3) || !W2 || !topk_ids || !topk_w || !eti || !offsets ||
+        !tim || !y || !H_saved || !ws)
         return MOE_ERR_INVALID_ARG;
-    for (const void* p : std::initializer_list<const void*>{x, W1, W3, W2, y, H_saved, ws})
+    for (const void* p : std::initializer_list<const void*>{x, W1, W2, y, H_saved, ws})
         if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (gated(s) && !aligned16(W3)) return MOE_ERR_MISALIGNED;
     if (ws_bytes < layout_fwd(s, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     int* err = status_ptr();
     if (!err) return MOE_ERR_NO_DEVICE;
@@ -386,14 +397,16 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
                  float* dS, void* ws, size_t ws_bytes, void* stream) {
     int rc = check_shape(s);
     if (rc) return rc;
-    if (!dy || !x || !Wg || !W1 || !W3 || !W2 || !topk_ids || !topk_w || !eti || !offsets ||
-        !tim || !H_saved || !dx || !dWg || !dW1 || !dW3 || !dW2 || !dS || !ws)
+    const bool gw = gated(s);  // W3 and dW3 exist
+    if (!dy || !x || !Wg || !W1 || (gw && !W3) || !W2 || !topk_ids || !topk_w || !eti ||
+        !offsets || !tim || !H_saved || !dx || !dWg || !dW1 || (gw && !dW3) || !dW2 || !dS || !ws)
         return MOE_ERR_INVALID_ARG;
-    for (const void* p : std::initializer_list<const void*>{dy, x, static_cast<const void*>(Wg), W1, W3, W2, H_saved,
-                          static_cast<const void*>(dx), static_cast<const void*>(dWg),
-                          static_cast<const void*>(dW1), static_cast<const void*>(dW3),
-                          static_cast<const void*>(dW2), static_cast<const void*>(ws)})
+    for (const void* p : std::initializer_list<const void*>{
+             dy, x, static_cast<const void*>(Wg), W1, W2, H_saved, static_cast<const void*>(dx),
+             static_cast<const void*>(dWg), static_cast<const void*>(dW1),
+             static_cast<const void*>(dW2), static_cast<const void*>(ws)})
         if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (gw && (!aligned16(W3) || !aligned16(dW3))) return MOE_ERR_MISALIGNED;
     if (ws_bytes < layout_bwd(s, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     int* err = status_ptr();
     if (!err) return MOE_ERR_NO_DEVICE;

@@ -82,7 +82,10 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
                               float* dWg, int* err, cudaStream_t st);
 
 // gemm.cu — the grouped tcgen05 GEMMs.
-enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5 };
+enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5,
+                // Non-gated (SiLU/ReLU) variants of G1 and G3; chosen by launch_gemm
+                // from moe_shape.expert, callers pass G1_UP / G3_DH.
+                G1_UP_ACT = 6, G3_DH_ACT = 7 };
 
 struct GemmProblem {
     GemmKind kind;

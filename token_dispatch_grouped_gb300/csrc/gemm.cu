@@ -29,19 +29,25 @@
 //   G1  [T_e, d] x [d, h|h]  gather x; B = W1_e, W3_e (K-major);
 //       epilogue: H = (a | b) saved, A = SiLU(a) * b. (MoEBlaze paper notes 5.2
 //       epilogue fusion; SonicMoE 3.4.2 SwiGLU epilogue)
+//       Non-gated experts (MoEBlaze paper notes 2.2, E(x) = W2 s(W1 x)): the
+//       256-column tile is 256 rows of W1 alone; H = a, A = act(a).
 //   G2  [T_e, h] x [h, d]    A rows contiguous; B = W2_e (K-major); Y chunk out.
 //   G3  [T_e, d] x [d, h]    gather dy; B = W2_e (MN-major): dA' = dy W2_e.
 //       epilogue: recompute sigma(a), SiLU(a), A from H; partial dS = <dA', A>;
 //       dA = w dA'; da = dA b SiLU'(a); db = dA SiLU(a); A' = w A.
+//       Non-gated: A = act(a), da = dA act'(a), dH = da alone.
 //       (SonicMoE 3.4.1 dS = <dA', A>, dA = s dA', A' = s A; MoEBlaze
 //       Algorithm 1 lines for grad A, grad B with SiLU recomputed)
 //   G4  dW2_e [d, h] = dy_e^T A'_e   varlen-K over T_e; gather dy (MN-major A),
 //       A' rows (MN-major B). (SonicMoE 3.4.1 dW2 = A'^T dO)
 //   G5  (x_e^T dH_e) [d, 2h] = [dW1_e; dW3_e]^T   varlen-K; gather x (MN-major
 //       A, M = d), dH rows (MN-major B); the epilogue stores the transpose.
-//       (MoEBlaze Algorithm 1, FusedBwdW)
+//       (MoEBlaze Algorithm 1, FusedBwdW). Non-gated: [d, h] = dW1_e^T.
 //   G6  dX~ [T_e, d] = da W1_e + db W3_e   one accumulator over K = 2h
-//       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer)
+//       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer).
+//       Non-gated: K = h, da W1_e.
+// The saved pre-activation H and its gradient dH are [TK, hs] with hs = 2h
+// (a | b) for SwiGLU and hs = h (a) for non-gated experts.
 // Rows past an expert's end are zero-filled on the gathered operand, so
 // ragged tails need no padding buffers (the other operand's extra rows are
 // multiplied by zeros).
@@ -72,6 +78,8 @@ template <> struct Tr<G3_DH>   { static constexpr bool VK = false; static conste
 template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
 template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
 template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0; };
+template <> struct Tr<G1_UP_ACT> : Tr<G1_UP> {};
+template <> struct Tr<G3_DH_ACT> : Tr<G3_DH> {};
 
 template <int BN, int CTAS, int EPI_BOXES = 2>
 struct Cfg {
@@ -92,7 +100,7 @@ struct Cfg {
 constexpr int kGatherThreads = 128;
 // Shared 2 KB staging boxes per epilogue warp (G3 writes three outputs per chunk).
 template <GemmKind KIND>
-constexpr int epi_boxes() { return KIND == G3_DH ? 3 : 2; }
+constexpr int epi_boxes() { return KIND == G3_DH || KIND == G3_DH_ACT ? 3 : 2; }
 template <GemmKind KIND, int CTAS>
 constexpr int threads_of() {
     return 192 + (Tr<KIND>::A_G ? kGatherThreads : 0) + (Tr<KIND>::A_G && CTAS == 2 ? 32 : 0);
@@ -100,6 +108,7 @@ constexpr int threads_of() {
 
 struct Params {
     int T, TK, d, h, E;
+    int act;       // expert function: 0 SwiGLU, 1 SiLU, 2 ReLU (moe_expert_kind)
     int Kdim;      // VM: reduction length
     int M;         // VK: rows of the output per expert
     int n_tiles;   // tiles along N
@@ -148,6 +157,22 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
     const bool ok = mbar_wait(bar, parity, abort, kWaitNs);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Non-gated activation and its derivative (act = 1 SiLU, 2 ReLU with
+// ReLU'(0) = 0). SiLU(u) = u sigma(u), SiLU'(u) = sigma(u) + SiLU(u) (1 - sigma(u)).
+__device__ __forceinline__ float act_fn(int act, float u) {
+    return act == 2 ? fmaxf(u, 0.f) : __fdividef(u, 1.f + __expf(-u));
+}
+__device__ __forceinline__ void act_and_grad(int act, float u, float& f, float& g) {
+    if (act == 2) {
+        f = fmaxf(u, 0.f);
+        g = u > 0.f ? 1.f : 0.f;
+    } else {
+        const float sg = __fdividef(1.f, 1.f + __expf(-u));
+        f = u * sg;
+        g = sg + f * (1.f - sg);
+    }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -296,6 +321,34 @@ __device__ __forceinline__ void box_get_row(uint8_t* box, int lane, const uint4 
     load32_bf16(u, v);
 }
 
+// Non-gated backward for one lane's 32 columns: a (packed bf16 in ua) and
+// dA' (v) give dS += <dA', act(a)>, da = w dA' act'(a) into box_da and
+// A' = w act(a) into box_ap.
+template <int ACT>
+__device__ __forceinline__ void ng_chunk(const uint4 (&ua)[4], const float (&v)[32], float w,
+                                         float& dsum, uint8_t* box_da, uint8_t* box_ap,
+                                         int lane) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float a8[8];
+        unpack8(ua[c], a8);
+        uint32_t da[4], ap[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            float f0, g0, f1, g1;
+            act_and_grad(ACT, a8[i], f0, g0);
+            act_and_grad(ACT, a8[i + 1], f1, g1);
+            const float v0 = v[8 * c + i], v1 = v[8 * c + i + 1];
+            dsum = fmaf(v0, f0, dsum);
+            dsum = fmaf(v1, f1, dsum);
+            da[i / 2] = pack_bf16(w * v0 * g0, w * v1 * g1);
+            ap[i / 2] = pack_bf16(w * f0, w * f1);
+        }
+        *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = make_uint4(da[0], da[1], da[2], da[3]);
+        *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = make_uint4(ap[0], ap[1], ap[2], ap[3]);
+    }
+}
+
 template <GemmKind KIND, int BN, int CTAS>
 __global__ void __launch_bounds__(threads_of<KIND, CTAS>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -422,30 +475,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
                     if (lane == 0) load(a_dst, &mapA, k0, row0);
                 }
-                if constexpr (KIND == G1_UP) {
-                    // B = 128 gate rows (W1) then 128 up rows (W3); in a pair the
-                    // first CTA stages W1's rows and the second W3's.
+                if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
+                    // SwiGLU: B = 128 gate rows (W1) then 128 up rows (W3); in a
+                    // pair the first CTA stages W1's rows and the second W3's.
+                    // Non-gated: B = 256 consecutive rows of W1.
                     if (lane == 0) {
-                        const int brow = t.e * p.h + t.n_blk * 128;
-                        if constexpr (PAIR) {
-                            load(b_dst, leader ? &mapB0 : &mapB1, k0, brow);
+                        if constexpr (KIND == G1_UP) {
+                            const int brow = t.e * p.h + t.n_blk * 128;
+                            if constexpr (PAIR) {
+                                load(b_dst, leader ? &mapB0 : &mapB1, k0, brow);
+                            } else {
+                                load(b_dst, &mapB0, k0, brow);
+                                load(b_dst + 16384, &mapB1, k0, brow);
+                            }
                         } else {
-                            load(b_dst, &mapB0, k0, brow);
-                            load(b_dst + 16384, &mapB1, k0, brow);
+                            const int brow = t.e * p.h + t.n_blk * 256;
+                            if constexpr (PAIR) {
+                                load(b_dst, &mapB0, k0, brow + static_cast<int>(rank) * 128);
+                            } else {
+                                load(b_dst, &mapB0, k0, brow);
+                                load(b_dst + 16384, &mapB0, k0, brow + 128);
+                            }
                         }
                     }
                 } else if constexpr (KIND == G2_DOWN) {
                     if (lane == 0) load(b_dst, &mapB0, k0, t.e * p.d + p.n_off + ncol);
-                } else if constexpr (KIND == G3_DH) {
+                } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
                     if (lane < BNL / 64)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.e * p.d + k0);
                 } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13) {
                     // B rows of this expert (A' for dW2, dH for dW1/dW3), MN-major.
                     if (lane < BNL / 64)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.lo + k0);
-                } else {  // G6: K = 2h, first h from W1, then W3.
+                } else {  // G6: K = 2h, first h from W1, then W3 (non-gated: K = h, W1).
                     if (lane < BNL / 64) {
-                        const bool up = k0 >= p.h;
+                        const bool up = p.act == 0 && k0 >= p.h;
                         const int brow = t.e * p.h + (up ? k0 - p.h : k0);
                         load(b_dst + lane * 8192, up ? &mapB1 : &mapB0, p.n_off + ncol + lane * 64,
                              brow);
@@ -528,29 +592,54 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const int rbase = t.lo + t.m_blk * BMC + rank * BM;  // VM: first row of this CTA
             const int mbase = t.m_blk * BMC + rank * BM;         // VK: first output row
             float v[32];
-            if constexpr (KIND == G1_UP) {
+            if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
                 const int row0w = rbase + q * 32;  // this warp's first row
                 const int nvalid = t.hi - row0w;
-                const int n0 = t.n_blk * 128;
-                __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) +
-                                   static_cast<size_t>(row0w > 0 ? row0w : 0) * (2 * p.h) + n0;
-                __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) +
-                                      static_cast<size_t>(row0w > 0 ? row0w : 0) * p.h + n0;
+                if constexpr (KIND == G1_UP_ACT) {
+                    // Non-gated: 256 columns of a; H = a, A = act(a), both [TK, h].
+                    const int n0 = t.n_blk * 256;
+                    const size_t r0 = static_cast<size_t>(row0w > 0 ? row0w : 0);
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + r0 * p.h + n0;
+                    __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
 #pragma unroll 1
-                for (int j = 0; j < 128; j += 32) {
-                    float b[32];
-                    tmem_ld32f(tacc + j, v);
-                    tmem_ld32f(tacc + 128 + j, b);
-                    if (nvalid > 0) {
-                        box_put_row(stg, lane, v);
-                        box_store_rows(stg, lane, H + j, 2 * p.h, nvalid);
-                        box_put_row(stg, lane, b);
-                        box_store_rows(stg, lane, H + p.h + j, 2 * p.h, nvalid);
+                    for (int j = 0; j < 256; j += 32) {
+                        tmem_ld32f(tacc + j, v);
+                        if (nvalid > 0) {
+                            box_put_row(stg, lane, v);
+                            box_store_rows(stg, lane, H + j, p.h, nvalid);
+                            if (p.act == 2) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __fdividef(v[i], 1.f + __expf(-v[i])) * b[i];
-                        box_put_row(stg, lane, v);
-                        box_store_rows(stg, lane, Aact + j, p.h, nvalid);
+                                for (int i = 0; i < 32; ++i) v[i] = act_fn(2, v[i]);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] = act_fn(1, v[i]);
+                            }
+                            box_put_row(stg, lane, v);
+                            box_store_rows(stg, lane, Aact + j, p.h, nvalid);
+                        }
+                    }
+                } else {
+                    const int n0 = t.n_blk * 128;
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) +
+                                       static_cast<size_t>(row0w > 0 ? row0w : 0) * (2 * p.h) + n0;
+                    __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) +
+                                          static_cast<size_t>(row0w > 0 ? row0w : 0) * p.h + n0;
+#pragma unroll 1
+                    for (int j = 0; j < 128; j += 32) {
+                        float b[32];
+                        tmem_ld32f(tacc + j, v);
+                        tmem_ld32f(tacc + 128 + j, b);
+                        if (nvalid > 0) {
+                            box_put_row(stg, lane, v);
+                            box_store_rows(stg, lane, H + j, 2 * p.h, nvalid);
+                            box_put_row(stg, lane, b);
+                            box_store_rows(stg, lane, H + p.h + j, 2 * p.h, nvalid);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[i] = __fdividef(v[i], 1.f + __expf(-v[i])) * b[i];
+                            box_put_row(stg, lane, v);
+                            box_store_rows(stg, lane, Aact + j, p.h, nvalid);
+                        }
                     }
                 }
             } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
@@ -567,76 +656,105 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         box_store_rows(stg, lane, out + j, p.ldo, nvalid);
                     }
                 }
-            } else if constexpr (KIND == G3_DH) {
+            } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
                 const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
                 const int row0w = rbase + q * 32;
                 const int nvalid = t.hi - row0w;
                 const int n0 = t.n_blk * BN;
                 const size_t r0 = static_cast<size_t>(row0w > 0 ? row0w : 0);
-                const __nv_bfloat16* Hw =
-                    static_cast<const __nv_bfloat16*>(p.aux0) + r0 * (2 * p.h) + n0;
-                __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * (2 * p.h) + n0;
-                __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
                 const float w = valid ? p.wrow[r] : 0.f;
                 float dsum = 0.f;
-                uint8_t* box_da = stg;
-                uint8_t* box_db = stg + 2048;
-                uint8_t* box_ap = stg + 4096;
-                // H (a | b) of the next 32 columns is fetched while this chunk is
-                // computed.
-                uint4 pa[4], pb[4];
-                if (nvalid > 0) {
-                    rows_fetch(pa, lane, Hw, 2 * p.h, nvalid);
-                    rows_fetch(pb, lane, Hw + p.h, 2 * p.h, nvalid);
-                }
+                if constexpr (KIND == G3_DH_ACT) {
+                    // Non-gated: H = a; A = act(a); dA = w dA'; da = dA act'(a);
+                    // A' = w A. dH and A' are [TK, h].
+                    const __nv_bfloat16* Hw =
+                        static_cast<const __nv_bfloat16*>(p.aux0) + r0 * p.h + n0;
+                    __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * p.h + n0;
+                    __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
+                    uint8_t* box_da = stg;
+                    uint8_t* box_ap = stg + 2048;
+                    uint8_t* box_in = stg + 4096;
+                    uint4 pa[4];
+                    if (nvalid > 0) rows_fetch(pa, lane, Hw, p.h, nvalid);
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32) {
-                    uint4 ua[4], ub[4];
-                    if (nvalid > 0) {
-                        box_get_row_raw(box_da, lane, pa, ua);
-                        box_get_row_raw(box_db, lane, pb, ub);
-                        if (j + 32 < BN) {
-                            rows_fetch(pa, lane, Hw + j + 32, 2 * p.h, nvalid);
-                            rows_fetch(pb, lane, Hw + p.h + j + 32, 2 * p.h, nvalid);
+                    for (int j = 0; j < BN; j += 32) {
+                        uint4 ua[4];
+                        if (nvalid > 0) {
+                            box_get_row_raw(box_in, lane, pa, ua);
+                            if (j + 32 < BN) rows_fetch(pa, lane, Hw + j + 32, p.h, nvalid);
+                        }
+                        tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
+                        if (nvalid > 0) {
+                            if (p.act == 2) ng_chunk<2>(ua, v, w, dsum, box_da, box_ap, lane);
+                            else ng_chunk<1>(ua, v, w, dsum, box_da, box_ap, lane);
+                            box_store_rows(box_da, lane, dHw + j, p.h, nvalid);
+                            box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
                         }
                     }
-                    tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
+                } else {
+                    const __nv_bfloat16* Hw =
+                        static_cast<const __nv_bfloat16*>(p.aux0) + r0 * (2 * p.h) + n0;
+                    __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * (2 * p.h) + n0;
+                    __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
+                    uint8_t* box_da = stg;
+                    uint8_t* box_db = stg + 2048;
+                    uint8_t* box_ap = stg + 4096;
+                    // H (a | b) of the next 32 columns is fetched while this chunk is
+                    // computed.
+                    uint4 pa[4], pb[4];
                     if (nvalid > 0) {
-                        // 8 columns at a time: dA = w dA'; da = dA b SiLU'(a);
-                        // db = dA SiLU(a); A' = w SiLU(a) b; packed straight into
-                        // the three boxes.
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            float a8[8], b8[8], da8[8], db8[8], ap8[8];
-                            unpack8(ua[c], a8);
-                            unpack8(ub[c], b8);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float vk = v[8 * c + i];
-                                const float sg = __fdividef(1.f, 1.f + __expf(-a8[i]));
-                                const float si = a8[i] * sg;
-                                const float Av = si * b8[i];
-                                dsum = fmaf(vk, Av, dsum);
-                                const float dA = w * vk;
-                                da8[i] = dA * b8[i] * (sg + a8[i] * sg * (1.f - sg));
-                                db8[i] = dA * si;
-                                ap8[i] = w * Av;
+                        rows_fetch(pa, lane, Hw, 2 * p.h, nvalid);
+                        rows_fetch(pb, lane, Hw + p.h, 2 * p.h, nvalid);
+                    }
+#pragma unroll 1
+                    for (int j = 0; j < BN; j += 32) {
+                        uint4 ua[4], ub[4];
+                        if (nvalid > 0) {
+                            box_get_row_raw(box_da, lane, pa, ua);
+                            box_get_row_raw(box_db, lane, pb, ub);
+                            if (j + 32 < BN) {
+                                rows_fetch(pa, lane, Hw + j + 32, 2 * p.h, nvalid);
+                                rows_fetch(pb, lane, Hw + p.h + j + 32, 2 * p.h, nvalid);
                             }
-                            uint4 u;
-                            u.x = pack_bf16(da8[0], da8[1]); u.y = pack_bf16(da8[2], da8[3]);
-                            u.z = pack_bf16(da8[4], da8[5]); u.w = pack_bf16(da8[6], da8[7]);
-                            *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = u;
-                            u.x = pack_bf16(db8[0], db8[1]); u.y = pack_bf16(db8[2], db8[3]);
-                            u.z = pack_bf16(db8[4], db8[5]); u.w = pack_bf16(db8[6], db8[7]);
-                            *reinterpret_cast<uint4*>(box_db + box_off(lane, c)) = u;
-                            u.x = pack_bf16(ap8[0], ap8[1]); u.y = pack_bf16(ap8[2], ap8[3]);
-                            u.z = pack_bf16(ap8[4], ap8[5]); u.w = pack_bf16(ap8[6], ap8[7]);
-                            *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = u;
                         }
-                        box_store_rows(box_da, lane, dHw + j, 2 * p.h, nvalid);
-                        box_store_rows(box_db, lane, dHw + p.h + j, 2 * p.h, nvalid);
-                        box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
+                        tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
+                        if (nvalid > 0) {
+                            // 8 columns at a time: dA = w dA'; da = dA b SiLU'(a);
+                            // db = dA SiLU(a); A' = w SiLU(a) b; packed straight into
+                            // the three boxes.
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                float a8[8], b8[8], da8[8], db8[8], ap8[8];
+                                unpack8(ua[c], a8);
+                                unpack8(ub[c], b8);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float vk = v[8 * c + i];
+                                    const float sg = __fdividef(1.f, 1.f + __expf(-a8[i]));
+                                    const float si = a8[i] * sg;
+                                    const float Av = si * b8[i];
+                                    dsum = fmaf(vk, Av, dsum);
+                                    const float dA = w * vk;
+                                    da8[i] = dA * b8[i] * (sg + a8[i] * sg * (1.f - sg));
+                                    db8[i] = dA * si;
+                                    ap8[i] = w * Av;
+                                }
+                                uint4 u;
+                                u.x = pack_bf16(da8[0], da8[1]); u.y = pack_bf16(da8[2], da8[3]);
+                                u.z = pack_bf16(da8[4], da8[5]); u.w = pack_bf16(da8[6], da8[7]);
+                                *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = u;
+                                u.x = pack_bf16(db8[0], db8[1]); u.y = pack_bf16(db8[2], db8[3]);
+                                u.z = pack_bf16(db8[4], db8[5]); u.w = pack_bf16(db8[6], db8[7]);
+                                *reinterpret_cast<uint4*>(box_db + box_off(lane, c)) = u;
+                                u.x = pack_bf16(ap8[0], ap8[1]); u.y = pack_bf16(ap8[2], ap8[3]);
+                                u.z = pack_bf16(ap8[4], ap8[5]); u.w = pack_bf16(ap8[6], ap8[7]);
+                                *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = u;
+                            }
+                            box_store_rows(box_da, lane, dHw + j, 2 * p.h, nvalid);
+                            box_store_rows(box_db, lane, dHw + p.h + j, 2 * p.h, nvalid);
+                            box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
+                        }
                     }
                 }
                 if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
@@ -919,7 +1037,7 @@ cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaSt
 template <GemmKind KIND, int CTAS>
 cudaError_t launch_bn(int BN, const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                       const char* name) {
-    if constexpr (KIND == G1_UP) {
+    if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
         return launch_kind<KIND, 256, CTAS>(mp, prm, max_tiles, st, name);
     } else {
         return BN == 256 ? launch_kind<KIND, 256, CTAS>(mp, prm, max_tiles, st, name)
@@ -973,6 +1091,8 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
                                                           : gemm_bn(g.kind, s);
     const int ctas = choose_ctas(g.kind, s);
     const uint64_t TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
+    const bool gated = s.expert == MOE_EXPERT_SWIGLU;
+    const uint64_t hs = gated ? 2 * h : h;  // width of H and dH
     const uint32_t bnl = static_cast<uint32_t>(BN / ctas);  // B rows staged per CTA
     Maps mp;
     bool ok = true;
@@ -982,6 +1102,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     prm.d = s.d;
     prm.h = s.h;
     prm.E = s.E;
+    prm.act = s.expert;
     prm.segs = g.segs;
     prm.eti = g.eti;
     prm.out0 = g.out0;
@@ -996,13 +1117,14 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     const int vm_mtiles = static_cast<int>(TK / bmc) + s.E;
     int max_tiles = 0;
     switch (g.kind) {
-        case G1_UP:  // A = x gathered; B = W1 | W3 [E*h, d], K-major
+        case G1_UP:  // A = x gathered; B = W1 | W3 [E*h, d] (or W1 alone), K-major
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 128);
-            ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
+            if (gated) ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
+            else mp.b1 = mp.b0;
             mp.a = mp.o = mp.b0;
             prm.Kdim = s.d;
-            prm.n_tiles = s.h / 128;
+            prm.n_tiles = gated ? s.h / 128 : s.h / 256;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
         case G2_DOWN:  // A = SwiGLU output rows; B = W2 [E*d, h], K-major
@@ -1032,22 +1154,24 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             prm.n_tiles = s.h / BN;
             max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
-        case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, 2h]; TMA-stored
+        case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, hs]; TMA-stored
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
-            ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, 2 * h, 64, 64);
-            ok &= make_tmap_bf16(&mp.o, g.out0, E * h, d, 32, 32, false);   // dW1
-            ok &= make_tmap_bf16(&mp.b1, g.out1, E * h, d, 32, 32, false);  // dW3
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, hs, 64, 64);
+            ok &= make_tmap_bf16(&mp.o, g.out0, E * h, d, 32, 32, false);  // dW1
+            if (gated) ok &= make_tmap_bf16(&mp.b1, g.out1, E * h, d, 32, 32, false);  // dW3
+            else mp.b1 = mp.o;
             mp.a = mp.b0;
             prm.M = s.d;
-            prm.n_tiles = 2 * s.h / BN;
+            prm.n_tiles = static_cast<int>(hs / BN);
             max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
-        case G6_DX:  // A = dH rows [TK, 2h]; B = W1 | W3 [E*h, d] read MN-major
-            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, 2 * h, 64, 128);
+        case G6_DX:  // A = dH rows [TK, hs]; B = W1 | W3 [E*h, d] (or W1) read MN-major
+            ok &= make_tmap_bf16(&mp.a, g.a_src, TK, hs, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 64);
-            ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
+            if (gated) ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
+            else mp.b1 = mp.b0;
             mp.o = mp.b0;
-            prm.Kdim = 2 * s.h;
+            prm.Kdim = static_cast<int>(hs);
             prm.n_off = g.n_off;
             prm.ldo = g.n_cols;
             prm.n_tiles = g.n_cols / BN;
@@ -1056,9 +1180,13 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     }
     if (!ok) return cudaErrorInvalidValue;
     switch (g.kind) {
-        case G1_UP: return launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu");
+        case G1_UP:
+            return gated ? launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu")
+                         : launch_ctas<G1_UP_ACT>(ctas, BN, mp, prm, max_tiles, st, "g1_up_act");
         case G2_DOWN: return launch_ctas<G2_DOWN>(ctas, BN, mp, prm, max_tiles, st, "g2_down");
-        case G3_DH: return launch_ctas<G3_DH>(ctas, BN, mp, prm, max_tiles, st, "g3_dh");
+        case G3_DH:
+            return gated ? launch_ctas<G3_DH>(ctas, BN, mp, prm, max_tiles, st, "g3_dh")
+                         : launch_ctas<G3_DH_ACT>(ctas, BN, mp, prm, max_tiles, st, "g3_dh_act");
         case G4_DW2: return launch_ctas<G4_DW2>(ctas, BN, mp, prm, max_tiles, st, "g4_dw2");
         case G5_DW13: return launch_ctas<G5_DW13>(ctas, BN, mp, prm, max_tiles, st, "g5_dw13");
         case G6_DX: return launch_ctas<G6_DX>(ctas, BN, mp, prm, max_tiles, st, "g6_dx");

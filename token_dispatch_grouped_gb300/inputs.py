@@ -12,6 +12,14 @@ Workloads (shapes from the layer configurations the method is evaluated on):
     skew     T=32768,  d=2048, E=128, K=8, h=768   (Zipf(1.2) loads via a logit bias)
     long     T=131072, d=4096, E=16,  K=4, h=2048
 
+Non-gated (SiLU) two-layer experts with h = 4d, T = batch x sequence length,
+on the MoEBlaze configurations whose sizes survive in its text:
+
+    moeblaze_conf1  T=65536 (32x2048), d=512,  E=4,  K=1, h=2048
+    moeblaze_conf3  T=65536 (32x2048), d=1024, E=16, K=4, h=4096
+    moeblaze_conf4  T=32768 (32x1024), d=2048, E=16, K=4, h=8192
+    moeblaze_conf7  T=8192  (16x512),  d=2048, E=8,  K=4, h=8192
+
 Recipe: one torch CPU generator per tensor, seeded from (seed, tensor name).
 x, dO ~ N(0, 1); W_g, W1, W3 ~ N(0, 1/d); W2 ~ N(0, 1/h). Activations and expert
 weights are rounded once to bf16 (round-to-nearest-even); the router weight
@@ -34,6 +42,11 @@ class Shape:
     E: int
     K: int
     h: int
+    expert: str = "swiglu"  # or the non-gated "silu" / "relu" (no W3)
+
+    @property
+    def gated(self) -> bool:
+        return self.expert == "swiglu"
 
     @property
     def TK(self) -> int:
@@ -49,6 +62,10 @@ WORKLOADS = {
     # Profiling-size case: the Mixtral-shaped experts (1024 rows each, d=4096,
     # h=14336) with only 2 experts, so an ncu capture holds ~2 GB on the device.
     "mixtral_e2": Shape(1024, 4096, 2, 2, 14336),
+    "moeblaze_conf1": Shape(65536, 512, 4, 1, 2048, "silu"),
+    "moeblaze_conf3": Shape(65536, 1024, 16, 4, 4096, "silu"),
+    "moeblaze_conf4": Shape(32768, 2048, 16, 4, 8192, "silu"),
+    "moeblaze_conf7": Shape(8192, 2048, 8, 4, 8192, "silu"),
 }
 
 # Fixed per-tensor stream ids, so adding a tensor never shifts another one.
@@ -86,8 +103,12 @@ def skew_bias(E: int) -> torch.Tensor | None:
 def make_layer_inputs(s: Shape, seed: int = 0, with_bias: bool = False,
                       parts=("x", "Wg", "W1", "W3", "W2", "dO")) -> dict:
     """CPU tensors of one layer step: x, dO bf16 [T,d]; W_g fp32 [E,d];
-    W1, W3 bf16 [E,h,d]; W2 bf16 [E,d,h]; optional bias fp32 [E]."""
+    W1, W3 bf16 [E,h,d] (W3 None for non-gated experts); W2 bf16 [E,d,h];
+    optional bias fp32 [E]."""
     out = {}
+    if not s.gated:
+        parts = tuple(q for q in parts if q != "W3")
+        out["W3"] = None
     if "x" in parts:
         out["x"] = randn((s.T, s.d), seed, "x").to(torch.bfloat16)
     if "Wg" in parts:

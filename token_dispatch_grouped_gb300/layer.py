@@ -27,11 +27,17 @@ class Dispatch:
 class MoELayer:
     """One dropless MoE layer of shape (T, d, E, K, h) on a CUDA device.
 
-    Workspaces are allocated once (the largest of the four calls) and reused."""
+    expert: "swiglu" (W1, W3, W2), or the non-gated "silu" / "relu" (W1, W2;
+    pass W3 = None). Workspaces are allocated once (the largest of the four
+    calls) and reused."""
 
-    def __init__(self, T: int, d: int, E: int, K: int, h: int, device="cuda"):
-        self.s = B.shape(T, d, E, K, h)
+    def __init__(self, T: int, d: int, E: int, K: int, h: int, device="cuda",
+                 expert: str = "swiglu"):
+        self.s = B.shape(T, d, E, K, h, expert)
         self.T, self.d, self.E, self.K, self.h = T, d, E, K, h
+        self.expert = expert
+        self.gated = expert == "swiglu"
+        self.hs = 2 * h if self.gated else h  # width of the saved pre-activation
         self.device = torch.device(device)
         sizes = [B.moe_workspace_size(self.s, w) for w in range(4)]
         if any(z == 0 for z in sizes[1:]):
@@ -60,7 +66,7 @@ class MoELayer:
         if y is None:
             y = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
         if H is None:
-            H = torch.empty(self.T * self.K, 2 * self.h, dtype=torch.bfloat16, device=self.device)
+            H = torch.empty(self.T * self.K, self.hs, dtype=torch.bfloat16, device=self.device)
         B.moe_forward(self.s, x, W1, W3, W2, r.ids, r.w, dp.eti, dp.offsets, dp.tim, y, H, self.ws)
         return y, H
 
@@ -78,7 +84,7 @@ class MoELayer:
             dx=torch.empty(T, d, dtype=torch.bfloat16, device=dev),
             dWg=torch.empty(E, d, dtype=torch.float32, device=dev),
             dW1=torch.empty(E, h, d, dtype=torch.bfloat16, device=dev),
-            dW3=torch.empty(E, h, d, dtype=torch.bfloat16, device=dev),
+            dW3=torch.empty(E, h, d, dtype=torch.bfloat16, device=dev) if self.gated else None,
             dW2=torch.empty(E, d, h, dtype=torch.bfloat16, device=dev),
             dS=torch.empty(T, K, dtype=torch.float32, device=dev),
         )
