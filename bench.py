@@ -47,6 +47,21 @@ def flops_per_step(s) -> float:
     return sum(gemm_flop_units(s).values()) * s.T * s.K * s.d * s.h + 6.0 * s.T * s.d * s.E
 
 
+def memory_kernel_bytes(s) -> dict:
+    """Algorithmic bytes per step of the memory-bound kernels: each operand read
+    once and each result written once (the per-kernel byte table of the design
+    notes). Kernel names are the launch names; D1-D3 count together."""
+    T, d, E, K = s.T, s.d, s.E, s.K
+    TK = T * K
+    return {
+        "router": (("router",), T * d * 2 + E * d * 4 + TK * 8 + T * E * 4),
+        "dispatch": (("dispatch_hist", "dispatch_scan", "dispatch_scatter"),
+                     2 * TK * 4 + 2 * TK * 4 + (E + 1) * 4),
+        "combine": (("combine",), TK * d * 2 + TK * 8 + T * d * 2),
+        "dx_combine": (("dx_combine",), TK * d * 2 + TK * 8 + T * d * 2),
+    }
+
+
 def load_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -316,6 +331,16 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peaks['src']} bf16 sustained (kernel timed inside the step)"}
     kernels = {k: {"launches": n, "ms_per_step": t / args.steps} for k, (n, t) in per_kernel.items()}
+    # HBM-bound kernels: algorithmic bytes / event-timed duration vs the measured copy peak
+    memory_bound = {}
+    for mk, (names, nbytes) in memory_kernel_bytes(s).items():
+        ms_k = sum(per_kernel[n][1] for n in names if n in per_kernel) / args.steps
+        if ms_k > 0:
+            gbs = nbytes / (ms_k / 1e3) / 1e9
+            memory_bound[mk] = {"bytes_per_step": nbytes, "ms_per_step": ms_k,
+                                "achieved_gbs": gbs, "frac_of_hbm": gbs / peaks["hbm"],
+                                "launches_per_step": sum(per_kernel[n][0] for n in names
+                                                         if n in per_kernel) / args.steps}
 
     # ---- end to end: host buffers in, results out, through the same C ABI calls
     xh = inp["x"].pin_memory()
@@ -369,7 +394,8 @@ def main():
                     config=workload_config(s, name), tflops=tflops,
                     frac_of_bf16_peak=tflops / peaks["bf16_sus"],
                     peak_note=f"{peaks['src']} bf16 sustained {peaks['bf16_sus']} TFLOP/s",
-                    memory=memory, roofline=roof, kernels=kernels, routing=routing,
+                    memory=memory, roofline=roof, kernels=kernels, memory_bound=memory_bound,
+                    hbm_peak_gbs=peaks["hbm"], routing=routing,
                     cpu_baseline=cpu_base, e2e=e2e, gpu_launches=launches, clocks=clk)
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -95,6 +95,28 @@ def test_layer_small_full_parity(s):
         assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
 
 
+# Router shapes that exercise the cluster split of the reduction over d (2, 4 and
+# 8 CTAs), every padded expert width (8 .. 256), E not a multiple of 8, and a bias.
+ROUTER = [(256, 2048, 8, 2), (1000, 1024, 16, 4), (300, 512, 64, 6), (500, 1024, 128, 8),
+          (200, 2048, 256, 8), (5000, 256, 5, 3), (777, 384, 40, 5)]
+
+
+@pytest.mark.parametrize("T,d,E,K", ROUTER, ids=lambda v: str(v))
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_router_shapes(T, d, E, K, with_bias):
+    from token_dispatch_grouped_gb300.layer import MoELayer
+    s = I.Shape(T, d, E, K, 256)
+    inp = I.make_layer_inputs(s, seed=3, parts=("x", "Wg"))
+    bias = None
+    if with_bias:
+        g = torch.Generator().manual_seed(11)
+        bias = (torch.rand(E, generator=g) - 0.5).float()
+    L = MoELayer(T, d, E, K, 256)
+    r = L.route(inp["x"].cuda(), inp["Wg"].cuda(), None if bias is None else bias.cuda())
+    L.check_error()
+    _check_route(r.logits, r.ids, r.w, inp["x"], inp["Wg"], K, bias)
+
+
 @pytest.mark.parametrize("expert", ["swiglu", "relu"])
 def test_injected_routing_skewed_and_empty_experts(expert):
     s = I.Shape(700, 256, 16, 4, 256, expert)

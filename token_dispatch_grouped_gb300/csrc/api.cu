@@ -266,6 +266,21 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                          strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int* device_status_word() { return status_ptr(); }
 
 int num_sms() {
@@ -352,7 +367,13 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
     layout_fwd(s, ws, &w);
     const int tc = moe_chunk_tokens(s);
     const int nc = nchunks_of(s, tc);
-    MOE_TRY(launch_chunk_segments(s, tc, nc, eti, offsets, w.segs, err, st));
+    const Plan pl = plan_down(s);
+    // Column-chunked passes, and a single token chunk, use the whole-row-space
+    // segments only.
+    const bool per_chunk = !pl.by_cols && nc > 1;
+    MOE_TRY(launch_chunk_segments(s, tc, per_chunk ? nc : 0, eti, offsets,
+                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
+                                  err, st));
     const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
 
     GemmProblem g1{};
@@ -368,9 +389,8 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
     g1.err = err;
     MOE_TRY(launch_gemm(g1, st));
 
-    const Plan pl = plan_down(s);
     for (int c = 0; c < pl.n; ++c) {
-        const Seg* sc = pl.by_cols ? full : w.segs + static_cast<size_t>(c) * s.E;
+        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
         GemmProblem g2{};
         g2.kind = G2_DOWN;
         g2.s = s;
@@ -415,7 +435,13 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
     layout_bwd(s, ws, &w);
     const int tc = moe_chunk_tokens(s);
     const int nc = nchunks_of(s, tc);
-    MOE_TRY(launch_chunk_segments(s, tc, nc, eti, offsets, w.segs, err, st));
+    const Plan pl = plan_dx(s);
+    // Column-chunked passes, and a single token chunk, use the whole-row-space
+    // segments only.
+    const bool per_chunk = !pl.by_cols && nc > 1;
+    MOE_TRY(launch_chunk_segments(s, tc, per_chunk ? nc : 0, eti, offsets,
+                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
+                                  err, st));
     const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
     MOE_TRY(launch_row_weights(s, topk_w, tim, w.wrow, err, st));
 
@@ -459,9 +485,8 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
     g5.err = err;
     MOE_TRY(launch_gemm(g5, st));
 
-    const Plan pl = plan_dx(s);
     for (int c = 0; c < pl.n; ++c) {
-        const Seg* sc = pl.by_cols ? full : w.segs + static_cast<size_t>(c) * s.E;
+        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
         GemmProblem g6{};
         g6.kind = G6_DX;
         g6.s = s;

@@ -40,6 +40,9 @@ struct LaunchScope {
 // box_cols x box_rows and 128-byte swizzle (or none). Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_cols, uint32_t box_rows, bool swizzle128 = true);
+// Same for a row-major fp32 array, without swizzle.
+bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows);
 
 int num_sms();
 

@@ -396,7 +396,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int tile0 = blockIdx.x / CTAS;   // first tile of this CTA (pair)
     const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
 
-    if (has_error(p.err)) return;  // uniform over the grid: both CTAs of a pair return
+    // Skip the work after an earlier error; a CTA of a pair never leaves alone
+    // (its peer would wait at the cluster barrier), so pairs run on.
+    if (!PAIR && has_error(p.err)) return;
 
     // ---- setup: segments, tile prefix, barriers, TMEM
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];

@@ -1,8 +1,10 @@
 // misc.cu — the memory-bound kernels around the expert GEMMs.
 //
-//   chunk_segments  per token chunk c and expert e, the sub-range of e's rows
+//   chunk_search    per token chunk c and expert e, the sub-range of e's rows
 //                   whose tokens fall in the chunk (stable order makes it one
-//                   contiguous range) and where it lands in the chunk buffer.
+//                   contiguous range);
+//   chunk_pack      where each range lands in the chunk buffer, and the
+//                   whole-row-space segments.
 //   row_weights     w_row[token_index_map[t*K+k]] = topk_w[t,k].
 //   combine   (C1)  y_t = sum_k w_{t,k} Y[row(t,k)], fp32, k ascending, one bf16
 //                   rounding. MoEBlaze paper notes 2.3; SonicMoE 3.4.1 (O_t).
@@ -22,46 +24,67 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ int lower_bound_i32(const int32_t* a, int lo, int hi, int key) {
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a[mid] < key) lo = mid + 1;
-        else hi = mid;
+// First index in [lo, hi) with a[i] >= key (hi if none), a sorted ascending.
+// The warp probes 32 evenly spaced positions per round and keeps the gap where
+// the predicate a[i] < key turns false: about log32(hi - lo) dependent loads.
+// Every lane returns the result.
+__device__ __forceinline__ int warp_lower_bound(const int32_t* __restrict__ a, int lo, int hi,
+                                                int key, int lane) {
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        const int pos = min(hi - 1, lo + (lane + 1) * step - 1);
+        const unsigned below = __ballot_sync(0xffffffffu, a[pos] < key);
+        const int cnt = __popc(below);  // the predicate holds on a prefix of the probes
+        const int nlo = lo + cnt * step;
+        hi = min(hi, lo + (cnt + 1) * step);
+        lo = min(nlo, hi);
     }
-    return lo;
+    const bool below = lo + lane < hi && a[lo + lane] < key;
+    return lo + __popc(__ballot_sync(0xffffffffu, below));
 }
 
-// grid = nchunks + 1 (the last "chunk" is the whole row space), block = 256.
-__global__ void chunk_segments_kernel(const int32_t* __restrict__ eti,
-                                      const int32_t* __restrict__ offsets, int E, int T,
-                                      int chunk_tokens, int nchunks, Seg* __restrict__ segs,
-                                      int* err) {
+// Token-chunk ranges: one warp per (chunk c < nchunks, expert e) finds the
+// rows of e whose tokens lie in [c * chunk_tokens, (c + 1) * chunk_tokens).
+__global__ void chunk_search_kernel(const int32_t* __restrict__ eti,
+                                    const int32_t* __restrict__ offsets, int E, int T,
+                                    int chunk_tokens, int nchunks, Seg* __restrict__ segs,
+                                    int* err) {
+    if (has_error(err)) return;
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (item >= nchunks * E) return;  // warp-uniform
+    const int c = item / E, e = item % E;
+    const int o0 = offsets[e], o1 = offsets[e + 1];
+    const int ta = c * chunk_tokens;
+    const int tb = min(T, ta + chunk_tokens);
+    const int lo = warp_lower_bound(eti, o0, o1, ta, lane);
+    const int hi = warp_lower_bound(eti, lo, o1, tb, lane);
+    if (lane == 0) segs[static_cast<size_t>(c) * E + e] = Seg{lo, hi, 0, 0};
+}
+
+// grid = nchunks + 1, block = 256. Block c < nchunks packs the chunk's ranges
+// expert after expert into the chunk buffer (out = rows of the experts before
+// e); the last block writes the whole-row-space segments {o_e, o_e+1, o_e}.
+__global__ void chunk_pack_kernel(const int32_t* __restrict__ offsets, int E, int nchunks,
+                                  Seg* __restrict__ segs, int* err) {
     if (has_error(err)) return;
     __shared__ int cnt[256];
     const int c = blockIdx.x;
     const int e = threadIdx.x;
-    int lo = 0, hi = 0;
+    Seg sg{0, 0, 0, 0};
     if (e < E) {
-        const int o0 = offsets[e], o1 = offsets[e + 1];
-        if (c == nchunks) {
-            lo = o0;
-            hi = o1;
-        } else {
-            const int ta = c * chunk_tokens;
-            const int tb = min(T, ta + chunk_tokens);
-            lo = lower_bound_i32(eti, o0, o1, ta);
-            hi = lower_bound_i32(eti, lo, o1, tb);
-        }
+        if (c == nchunks) sg = Seg{offsets[e], offsets[e + 1], offsets[e], 0};
+        else sg = segs[static_cast<size_t>(c) * E + e];
     }
-    cnt[e] = hi - lo;
+    cnt[e] = sg.hi - sg.lo;
     __syncthreads();
     if (e < E) {
-        int out = lo;
         if (c != nchunks) {
-            out = 0;
+            int out = 0;
             for (int q = 0; q < e; ++q) out += cnt[q];
+            sg.out = out;
         }
-        segs[static_cast<size_t>(c) * E + e] = Seg{lo, hi, out, 0};
+        segs[static_cast<size_t>(c) * E + e] = sg;
     }
 }
 
@@ -266,9 +289,16 @@ __global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
 cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchunks,
                                   const int32_t* eti, const int32_t* offsets, Seg* segs, int* err,
                                   cudaStream_t st) {
-    LaunchScope ls("chunk_segments", st);
-    chunk_segments_kernel<<<nchunks + 1, 256, 0, st>>>(eti, offsets, s.E, s.T, chunk_tokens,
-                                                       nchunks, segs, err);
+    if (nchunks > 0) {
+        LaunchScope ls("chunk_search", st);
+        const int warps = nchunks * s.E;
+        chunk_search_kernel<<<(warps + 7) / 8, 256, 0, st>>>(eti, offsets, s.E, s.T,
+                                                             chunk_tokens, nchunks, segs, err);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    LaunchScope ls("chunk_pack", st);
+    chunk_pack_kernel<<<nchunks + 1, 256, 0, st>>>(offsets, s.E, nchunks, segs, err);
     return cudaGetLastError();
 }
 

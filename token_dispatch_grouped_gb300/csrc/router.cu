@@ -7,190 +7,250 @@
 // Sources: MoEBlaze paper notes 2.1 (TopK(softmax(W_g x))); Dropless MoE, in
 // depth, "A reference implementation" (renormalise over the chosen k).
 //
-// Layout: one CTA of 256 threads owns BT tokens and all EP (padded) experts.
-// Thread (ks, tg, eg) accumulates TT tokens x 8 experts over a 1/KS slice of
-// every KC-wide chunk of the reduction; chunks of x and W_g are staged
-// transposed in shared memory, and the next chunk is already in registers
-// while the current one is used. The KS partial sums are added in a fixed
-// order through shared memory. The EG threads of one token group sit in
-// consecutive lanes of one warp, so the top-K is a butterfly arg-max over
-// those lanes, repeated K times. Few tokens per CTA (16..64) keep the grid
-// large for small T.
+// Layout: a CTA owns BT tokens and all EP (padded) experts. One producer warp
+// streams KC-wide chunks of x (TMA, 128-byte swizzled rows) and W_g (TMA, plain
+// rows) into a ring of shared-memory stages guarded by mbarriers; eight compute
+// warps consume them without CTA-wide barriers. Compute warp w owns expert
+// group eg = w % EG (TE experts) and reduction slice ks = w / EG of each chunk;
+// lane l owns tokens l, l + 32, ... (TT of them), so a quarter-warp's x reads
+// hit 8 rows whose swizzled 16-byte pieces sit in distinct banks, and W_g reads
+// are warp-wide broadcasts. Each thread keeps TT x TE fp32 accumulators (FFMA,
+// k ascending within its slice). When there are few token tiles, a cluster of
+// S CTAs splits the reduction over d; partial sums meet in the first CTA's
+// shared memory and are added in a fixed order (CTA rank, then slice), read
+// through distributed shared memory. The top-K is a butterfly arg-max over the
+// EP/8 lanes that hold a token's logits (8 each), repeated K times. Every
+// mbarrier wait is bounded.
 #include <cfloat>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+using namespace ptx;
+
+constexpr uint64_t kWaitNs = 2000000000ull;
 
 template <int EP>
 struct RouterCfg {
-    static constexpr int EG = EP / 8;
-    static constexpr int KS = EP == 8 ? 16 : EP == 16 ? 8 : EP == 32 ? 4 : EP == 64 ? 2 : 1;
-    static constexpr int TG = kThreads / (EG * KS);
-    static constexpr int TT = EP <= 32 ? 1 : EP == 64 ? 2 : 4;
-    static constexpr int BT = TG * TT;
-    static constexpr int KC = EP == 256 ? 64 : 128;
-    static constexpr int XU = BT * KC / 8;    // 16-byte x units per chunk
-    static constexpr int WU = EP * KC / 4;    // float4 W_g units per chunk
-    static constexpr int XPT = (XU + kThreads - 1) / kThreads;
-    static constexpr int WPT = (WU + kThreads - 1) / kThreads;
-    static constexpr int SMEM_STAGE = (KC * BT + KC * EP) * 4;
-    static constexpr int SMEM_RED = KS > 1 ? KS * BT * EP * 4 : 0;
-    static constexpr int SMEM = SMEM_STAGE > SMEM_RED ? SMEM_STAGE : SMEM_RED;
+    static constexpr int TE = EP <= 64 ? 8 : EP / 8;  // experts per thread
+    static constexpr int TT = EP <= 128 ? 4 : 2;      // tokens per thread
+    static constexpr int EG = EP / TE;             // expert groups
+    static constexpr int KS = EG >= 8 ? 1 : 8 / EG;  // reduction slices per chunk
+    static constexpr int CW = EG * KS;             // compute warps (8 or 16)
+    static constexpr int THREADS = 32 * CW + 32;   // plus the TMA producer warp
+    static constexpr int BT = 32 * TT;             // tokens per CTA
+    static constexpr int KC = 64;                 // reduction chunk: one 128-byte x row
+    static constexpr int X_BYTES = BT * KC * 2;
+    static constexpr int W_BYTES = EP * KC * 4;
+    static constexpr int STAGE = X_BYTES + W_BYTES;
+    static constexpr int BUDGET = EP <= 64 ? 98304 : 147456;
+    static constexpr int STAGES = BUDGET / STAGE > 4 ? 4 : (BUDGET / STAGE < 2 ? 2 : BUDGET / STAGE);
+    static constexpr int PIPE = STAGES * STAGE;
+    static constexpr int EPP = EP + 1;            // floats per logit row (odd: no conflicts)
+    static constexpr int RED = KS * BT * EPP * 4; // partial sums of this CTA
+    static constexpr int ZS = BT * EPP * 4;       // the tile's final logits
+    static constexpr int BODY = PIPE > RED + ZS ? PIPE : RED + ZS;
+    static constexpr int SMEM = 1024 + BODY + 256; // 1 KB alignment slack, barriers
+    static constexpr int G = EP / 8;              // lanes per token in the top-K
+    static_assert((KC / KS) % 8 == 0, "slice of whole 16-byte pieces");
+    static_assert(STAGE % 1024 == 0, "stages keep the 1 KB swizzle alignment");
+    static_assert(16 * STAGES + 8 <= 256, "barrier region");
 };
 
-template <int EP>
-__global__ void __launch_bounds__(kThreads)
-router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 p = __bfloat1622float2(b[j]);
+        f[2 * j] = p.x;
+        f[2 * j + 1] = p.y;
+    }
+}
+
+// Warp-uniform bounded wait: every lane polls, all lanes agree on the result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort, kWaitNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+template <int EP, int S>
+__global__ void __launch_bounds__(RouterCfg<EP>::THREADS, EP <= 64 ? 2 : 1)
+router_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
               const float* __restrict__ bias, float* __restrict__ logits,
               int32_t* __restrict__ ids, float* __restrict__ wout, int T, int d, int E, int K,
               int* err) {
     using C = RouterCfg<EP>;
-    if (has_error(err)) return;
-    extern __shared__ __align__(16) float sm[];
-    float* Xs = sm;                   // [KC][BT]
-    float* Ws = sm + C::KC * C::BT;   // [KC][EP]
+    constexpr int kCompute = 32 * C::CW;
+    constexpr int kThreads = C::THREADS;
+    // A CTA of a cluster must not leave alone (its peers would wait at the
+    // cluster barrier), so only single-CTA launches skip work after an error.
+    if (S == 1 && has_error(err)) return;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1 KB alignment
+    uint8_t* sm = smem_raw + (sbase - raw);
+    const uint32_t bar0 = sbase + C::BODY;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::BODY + 16 * C::STAGES);
 
     const int tid = threadIdx.x;
-    const int eg = tid % C::EG;
-    const int tg = (tid / C::EG) % C::TG;
-    const int ks = tid / (C::EG * C::TG);
-    const int t0 = blockIdx.x * C::BT;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const uint32_t rank = S > 1 ? cluster_ctarank() : 0u;
+    const int t0 = static_cast<int>(blockIdx.x / S) * C::BT;
+    const int dS = d / S;  // this CTA's share of the reduction
+    const int kbeg = static_cast<int>(rank) * dS;
+    const int nchunks = dS / C::KC;
 
-    float acc[C::TT][8];
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kCompute / 32);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kCompute / 32 && lane == 0) {
+        prefetch_tensormap(&mapX);
+        prefetch_tensormap(&mapW);
+    }
+    __syncthreads();
+
+    float acc[C::TT][C::TE];
 #pragma unroll
     for (int i = 0; i < C::TT; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < C::TE; ++j) acc[i][j] = 0.f;
 
-    uint4 xr[C::XPT];
-    float4 wr[C::WPT];
-    auto fetch = [&](int k0) {
-#pragma unroll
-        for (int u = 0; u < C::XPT; ++u) {
-            const int c = tid + u * kThreads;
-            xr[u] = make_uint4(0, 0, 0, 0);
-            if (c < C::XU) {
-                const int r = c / (C::KC / 8);
-                const int t = t0 + r;
-                const int col = k0 + (c % (C::KC / 8)) * 8;  // chunks may run past d: zeros
-                if (t < T && col < d)
-                    xr[u] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + col);
+    if (warp == kCompute / 32) {
+        // ---- producer: one elected lane issues the TMA loads of each stage
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % C::STAGES;
+                const uint32_t ph = (c / C::STAGES) & 1;
+                if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, kWaitNs)) break;
+                mbar_arrive_expect_tx(full_bar(s), C::STAGE);
+                const uint32_t xs = sbase + s * C::STAGE;
+                const int k0 = kbeg + c * C::KC;
+                tma_load_2d(xs, &mapX, full_bar(s), k0, t0);              // rows >= T read as 0
+                tma_load_2d(xs + C::X_BYTES, &mapW, full_bar(s), k0, 0);  // experts >= E read as 0
             }
         }
+        __syncwarp();
+    } else {
+        // ---- compute warps
+        const int eg = warp % C::EG;
+        const int ks = warp / C::EG;
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c % C::STAGES;
+            const uint32_t ph = (c / C::STAGES) & 1;
+            if (!warp_wait(full_bar(s), ph, abort_flag)) break;
+            const uint8_t* xs = sm + s * C::STAGE;
+            const float* ws = reinterpret_cast<const float*>(xs + C::X_BYTES);
+            constexpr int KPS = C::KC / C::KS;
 #pragma unroll
-        for (int u = 0; u < C::WPT; ++u) {
-            const int c = tid + u * kThreads;
-            wr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c < C::WU) {
-                const int e = c / (C::KC / 4);
-                const int col = k0 + (c % (C::KC / 4)) * 4;
-                if (e < E && col < d)
-                    wr[u] = *reinterpret_cast<const float4*>(Wg + static_cast<size_t>(e) * d + col);
+            for (int q = 0; q < KPS; q += 8) {
+                const int kk = ks * KPS + q;
+                const int piece = kk >> 3;  // 16-byte piece of the 128-byte row
+                float xv[C::TT][8];
+#pragma unroll
+                for (int i = 0; i < C::TT; ++i) {
+                    const int r = lane + 32 * i;  // r & 7 == lane & 7
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(
+                                      xs + r * 128 + ((piece ^ (lane & 7)) << 4)),
+                                  xv[i]);
+                }
+#pragma unroll
+                for (int j = 0; j < C::TE; ++j) {
+                    const float* wr = ws + (eg * C::TE + j) * C::KC + kk;
+                    const float4 w0 = *reinterpret_cast<const float4*>(wr);
+                    const float4 w1 = *reinterpret_cast<const float4*>(wr + 4);
+                    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int i = 0; i < C::TT; ++i)
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) acc[i][j] = fmaf(xv[i][m], wv[m], acc[i][j]);
+                }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(s));
         }
-    };
-    auto stage = [&]() {
-#pragma unroll
-        for (int u = 0; u < C::XPT; ++u) {
-            const int c = tid + u * kThreads;
-            if (c < C::XU) {
-                const int r = c / (C::KC / 8);
-                const int cc = (c % (C::KC / 8)) * 8;
-                const __nv_bfloat16* b = reinterpret_cast<const __nv_bfloat16*>(&xr[u]);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) Xs[(cc + j) * C::BT + r] = __bfloat162float(b[j]);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < C::WPT; ++u) {
-            const int c = tid + u * kThreads;
-            if (c < C::WU) {
-                const int e = c / (C::KC / 4);
-                const int cc = (c % (C::KC / 4)) * 4;
-                Ws[(cc + 0) * EP + e] = wr[u].x;
-                Ws[(cc + 1) * EP + e] = wr[u].y;
-                Ws[(cc + 2) * EP + e] = wr[u].z;
-                Ws[(cc + 3) * EP + e] = wr[u].w;
-            }
-        }
-    };
-
-    fetch(0);
-    for (int k0 = 0; k0 < d; k0 += C::KC) {
-        __syncthreads();  // previous chunk fully consumed
-        stage();
-        __syncthreads();
-        if (k0 + C::KC < d) fetch(k0 + C::KC);  // in flight while this chunk is used
-        constexpr int KPT = C::KC / C::KS;
-#pragma unroll 8
-        for (int q = 0; q < KPT; ++q) {
-            const int kk = ks * KPT + q;
-            const float4 w0 = *reinterpret_cast<const float4*>(Ws + kk * EP + eg * 8);
-            const float4 w1 = *reinterpret_cast<const float4*>(Ws + kk * EP + eg * 8 + 4);
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-            for (int i = 0; i < C::TT; ++i) {
-                const float xv = Xs[kk * C::BT + tg * C::TT + i];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv, wv[j], acc[i][j]);
-            }
+    }
+    __syncthreads();  // every stage consumed: the pipeline memory is reused below
+    if (*abort_flag) {
+        if (tid == 0) raise_error(err, MOE_ERR_TIMEOUT);
+        // Let copies already in flight land before the memory is reused.
+        const uint64_t tw = globaltimer_ns();
+        while (globaltimer_ns() - tw < 5000000ull) {
         }
     }
 
-    // Sum the KS partial results in a fixed order (ks = 0, 1, ...).
-    if constexpr (C::KS > 1) {
-        __syncthreads();
-        float* red = sm;  // [KS][BT][EP]
+    // Partial sums of this CTA: red[ks][token][expert].
+    float* red = reinterpret_cast<float*>(sm);
+    float* zs = red + C::KS * C::BT * C::EPP;
+    if (warp < kCompute / 32) {
+        const int eg = warp % C::EG;
+        const int ks = warp / C::EG;
 #pragma unroll
         for (int i = 0; i < C::TT; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                red[(ks * C::BT + tg * C::TT + i) * EP + eg * 8 + j] = acc[i][j];
-        __syncthreads();
-        if (ks == 0) {
+            for (int j = 0; j < C::TE; ++j)
+                red[(ks * C::BT + lane + 32 * i) * C::EPP + eg * C::TE + j] = acc[i][j];
+    }
+    if constexpr (S > 1) cluster_sync();
+    else __syncthreads();
+    if (rank == 0) {
+        // Fixed order: CTA rank, then slice.
+        for (int idx = tid; idx < C::BT * EP; idx += kThreads) {
+            const int r = idx / EP, e = idx % EP;
+            float parts[S * C::KS];
 #pragma unroll
-            for (int i = 0; i < C::TT; ++i)
+            for (int q = 0; q < S; ++q)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float v = 0.f;
-                    for (int q = 0; q < C::KS; ++q)
-                        v += red[(q * C::BT + tg * C::TT + i) * EP + eg * 8 + j];
-                    acc[i][j] = v;
+                for (int s2 = 0; s2 < C::KS; ++s2) {
+                    const int off = (s2 * C::BT + r) * C::EPP + e;
+                    parts[q * C::KS + s2] =
+                        q == 0 ? red[off]
+                               : ld_shared_cluster_f32(mapa_shared(sbase + off * 4, q));
                 }
+            float v = parts[0];
+#pragma unroll
+            for (int q = 1; q < S * C::KS; ++q) v += parts[q];
+            zs[r * C::EPP + e] = v;
         }
     }
-    // Threads of the warps that hold ks == 0 finish; lanes with ks != 0 in such a
-    // warp take part in the shuffles but write nothing.
-    if ((tid / 32) * 32 >= C::EG * C::TG) return;
-    const bool owner = ks == 0;
+    if constexpr (S > 1) cluster_sync();  // peers keep their partials until they are read
+    if (rank != 0) return;
+    __syncthreads();
+    if (warp >= kCompute / 32) return;
 
+    // Top-K: G consecutive lanes hold one token's logits, 8 each.
+    constexpr int G = C::G;
+    constexpr int TPP = kCompute / G;  // tokens per pass
+    const int g = tid % G;
+#pragma unroll 1
+    for (int base = 0; base < C::BT; base += TPP) {
+        const int r = base + tid / G;
+        const int t = t0 + r;
+        const bool live = r < C::BT && t < T;
+        float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e = eg * 8 + j;
-        const float b = (bias != nullptr && e < E) ? bias[e] : 0.f;
-#pragma unroll
-        for (int i = 0; i < C::TT; ++i) acc[i][j] += b;
-    }
-    if (logits != nullptr && owner) {
-#pragma unroll
-        for (int i = 0; i < C::TT; ++i) {
-            const int t = t0 + tg * C::TT + i;
-            if (t >= T) continue;
+        for (int j = 0; j < 8; ++j) {
+            const int e = g * 8 + j;
+            const float b = (bias != nullptr && e < E) ? bias[e] : 0.f;
+            v[j] = (live && e < E) ? zs[r * C::EPP + e] + b : -INFINITY;
+        }
+        if (logits != nullptr && live) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = eg * 8 + j;
-                if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j];
+                const int e = g * 8 + j;
+                if (e < E) logits[static_cast<size_t>(t) * E + e] = v[j];
             }
         }
-    }
-
-#pragma unroll
-    for (int i = 0; i < C::TT; ++i) {
-        const int t = t0 + tg * C::TT + i;
         uint32_t taken = 0;
         float zsel[8];
         int isel[8];
@@ -200,16 +260,15 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
             int bi = 0x7fffffff;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int e = eg * 8 + j;
-                const float v = acc[i][j];
+                const int e = g * 8 + j;
                 const bool ok = e < E && !((taken >> j) & 1u);
-                if (ok && (v > bv || (v == bv && e < bi))) {
-                    bv = v;
+                if (ok && (v[j] > bv || (v[j] == bv && e < bi))) {
+                    bv = v[j];
                     bi = e;
                 }
             }
 #pragma unroll
-            for (int off = 1; off < C::EG; off <<= 1) {
+            for (int off = 1; off < G; off <<= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
                 if (ov > bv || (ov == bv && oi < bi)) {
@@ -217,11 +276,11 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
                     bi = oi;
                 }
             }
-            if (bi / 8 == eg && bi < E) taken |= 1u << (bi % 8);
+            if (bi / 8 == g && bi < E) taken |= 1u << (bi % 8);
             zsel[k] = bv;
             isel[k] = bi;
         }
-        if (owner && eg == 0 && t < T) {
+        if (live && g == 0) {
             float den = 0.f;
             float ex[8];
             for (int k = 0; k < K; ++k) {
@@ -241,22 +300,55 @@ router_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wg,
     }
 }
 
+template <int EP, int S>
+cudaError_t launch_eps(const moe_shape& s, const __nv_bfloat16* x, const float* Wg,
+                       const float* bias, float* logits, int32_t* ids, float* w, int* err,
+                       cudaStream_t st) {
+    using C = RouterCfg<EP>;
+    auto kfn = router_kernel<EP, S>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    CUtensorMap mapX, mapW;
+    if (!make_tmap_bf16(&mapX, x, s.T, s.d, C::KC, C::BT) ||
+        !make_tmap_f32(&mapW, Wg, s.E, s.d, C::KC, EP))
+        return cudaErrorInvalidValue;
+    const int tiles = (s.T + C::BT - 1) / C::BT;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    LaunchScope ls("router", st);
+    return cudaLaunchKernelEx(&cfg, kfn, mapX, mapW, bias, logits, ids, w, s.T, s.d, s.E, s.K,
+                              err);
+}
+
+// Cluster split of the reduction: doubled while the grid has fewer than two
+// CTAs per SM and every CTA keeps at least two chunks of d.
 template <int EP>
 cudaError_t launch_ep(const moe_shape& s, const __nv_bfloat16* x, const float* Wg,
                       const float* bias, float* logits, int32_t* ids, float* w, int* err,
                       cudaStream_t st) {
     using C = RouterCfg<EP>;
-    static_assert(C::EG * C::KS * C::TG == kThreads, "thread layout");
-    const size_t smem = C::SMEM;
-    cudaError_t e = cudaFuncSetAttribute(router_kernel<EP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int grid = (s.T + C::BT - 1) / C::BT;
-    LaunchScope ls("router", st);
-    router_kernel<EP><<<grid, kThreads, smem, st>>>(x, Wg, bias, logits, ids, w, s.T, s.d, s.E,
-                                                    s.K, err);
-    return cudaGetLastError();
+    const int tiles = (s.T + C::BT - 1) / C::BT;
+    int S = 1;
+    while (S < 8 && tiles * S < 2 * num_sms() && s.d % (2 * S * C::KC) == 0 &&
+           s.d / (2 * S) >= 2 * C::KC)
+        S *= 2;
+    switch (S) {
+        case 8: return launch_eps<EP, 8>(s, x, Wg, bias, logits, ids, w, err, st);
+        case 4: return launch_eps<EP, 4>(s, x, Wg, bias, logits, ids, w, err, st);
+        case 2: return launch_eps<EP, 2>(s, x, Wg, bias, logits, ids, w, err, st);
+        default: return launch_eps<EP, 1>(s, x, Wg, bias, logits, ids, w, err, st);
+    }
 }
 
 }  // namespace

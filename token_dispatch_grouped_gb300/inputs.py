@@ -62,6 +62,10 @@ WORKLOADS = {
     # Profiling-size case: the Mixtral-shaped experts (1024 rows each, d=4096,
     # h=14336) with only 2 experts, so an ncu capture holds ~2 GB on the device.
     "mixtral_e2": Shape(1024, 4096, 2, 2, 14336),
+    # Profiling-size case for the memory-bound kernels: Mixtral's routing shape
+    # (d=4096, E=8, K=2) at T=16384, so x (128 MiB) exceeds L2, with narrow
+    # experts (h=1024) to keep the whole step near 1.3 GB on the device.
+    "mixtral_t16k_narrow": Shape(16384, 4096, 8, 2, 1024),
     "moeblaze_conf1": Shape(65536, 512, 4, 1, 2048, "silu"),
     "moeblaze_conf3": Shape(65536, 1024, 16, 4, 4096, "silu"),
     "moeblaze_conf4": Shape(32768, 2048, 16, 4, 8192, "silu"),
