@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixtral]
                     [--impl ours|reference] [--no-cpu-baseline]
+    python bench.py --dispatch-ablation
 
 One step = route + dispatch index + forward + backward of one layer over one
 batch of synthetic, seeded inputs (all through the C ABI). Prints one JSON line
@@ -205,6 +206,101 @@ def workload_config(s, name):
             "l2": "working set > L2 (expert weights alone exceed 129 MB and are streamed every step)"}
 
 
+# ------------------------------------------------------------------ dispatch ablation
+def sort_dispatch(ids: torch.Tensor, E: int):
+    """Sort-based dispatch index on the GPU with library kernels (torch's stable
+    radix sort, a binary search for the offsets, a scatter for the inverse):
+    the baseline the atomic-free build is compared with. Same outputs:
+    expert_token_indices, expert_token_offsets, token_index_map (int32)."""
+    T, K = ids.shape
+    flat = ids.reshape(-1)
+    keys, perm = torch.sort(flat, stable=True)
+    eti = torch.div(perm, K, rounding_mode="floor").to(torch.int32)
+    bounds = torch.arange(E + 1, device=ids.device, dtype=keys.dtype)
+    offsets = torch.searchsorted(keys, bounds).to(torch.int32)
+    tim = torch.empty_like(flat)
+    tim[perm] = torch.arange(flat.numel(), device=ids.device, dtype=torch.int32)
+    return eti, offsets, tim
+
+
+def _graph_us(fn, reps: int) -> tuple[float, float]:
+    """(CUDA-graph replay, eager) microseconds per call of fn, back to back."""
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        fn()
+    b.record(st)
+    torch.cuda.synchronize()
+    eager = a.elapsed_time(b) * 1e3 / reps
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            fn()
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a.record(st)
+    g.replay()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps, eager
+
+
+def run_dispatch_ablation(args):
+    """The atomic-free dispatch build (D1-D3, one C-ABI call) against the
+    sort-based baseline across token counts, expert counts, K and skew. One
+    JSON line per case; both outputs are checked equal first."""
+    from token_dispatch_grouped_gb300 import binding as B
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks = load_peaks()
+    for T in (4096, 32768, 262144):
+        for E, K in ((8, 2), (64, 6), (128, 8)):
+            for skew in (0.0, 1.2):
+                ids = I.random_ids_gumbel(T, E, K, seed=T + E, skew=skew).to(dev)
+                s = B.shape(T, 128, E, K, 128)
+                ws = torch.empty(max(B.moe_workspace_size(s, B.MOE_WS_DISPATCH), 256),
+                                 dtype=torch.uint8, device=dev)
+                TK = T * K
+                eti = torch.empty(TK, dtype=torch.int32, device=dev)
+                off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+                tim = torch.empty(TK, dtype=torch.int32, device=dev)
+
+                def ours():
+                    B.moe_build_dispatch(s, ids, eti, off, tim, ws)
+
+                def base():
+                    return sort_dispatch(ids, E)
+
+                ours()
+                ref = base()
+                torch.cuda.synchronize()
+                same = (torch.equal(eti, ref[0]) and torch.equal(off, ref[1])
+                        and torch.equal(tim, ref[2]))
+                if B.moe_get_error() != B.MOE_OK or not same:
+                    raise SystemExit(f"dispatch ablation: outputs differ at T={T} E={E} K={K}")
+                g_ours, e_ours = _graph_us(ours, 20)
+                g_sort, e_sort = _graph_us(base, 20)
+                nbytes = 2 * TK * 4 + 2 * TK * 4 + (E + 1) * 4  # ids read twice, two maps written
+                line = {"ablation": "dispatch_index", "T": T, "E": E, "K": K, "skew": skew,
+                        "ours_us": g_ours, "sort_us": g_sort, "speedup": g_sort / g_ours,
+                        "ours_eager_us": e_ours, "sort_eager_us": e_sort,
+                        "ours_hbm_frac": nbytes / (g_ours * 1e-6) / 1e9 / peaks["hbm"],
+                        "timing": "CUDA graph of 20 back-to-back calls; eager alongside",
+                        "outputs_equal": True}
+                print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -216,9 +312,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
     ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--dispatch-ablation", action="store_true",
+                    help="time the dispatch build against a sort-based baseline and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.dispatch_ablation:
+        run_dispatch_ablation(args)
+        return
     name = args.workload
     s = I.WORKLOADS[name]
     if args.impl == "reference":
@@ -287,7 +388,6 @@ def main():
     torch.cuda.synchronize(dev)
     L.check_error()
     launches0 = B.moe_launch_count()
-    B.moe_timing_enable(True)
     barrier(world)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -302,9 +402,17 @@ def main():
     barrier(world)
     ms = e0.elapsed_time(e1)
     launches = B.moe_launch_count() - launches0
+    clk = clocks.stop()
+    L.check_error()
+    # Per-kernel breakdown in a separate pass of the same steps: two CUDA events
+    # around every launch (recorded on its stream), so the timed pass above
+    # carries no per-launch instrumentation.
+    B.moe_timing_enable(True)
+    for _ in range(args.steps):
+        step(dv["x"], dv["dO"])
+    torch.cuda.synchronize(dev)
     per_kernel = B.moe_timing_collect()
     B.moe_timing_enable(False)
-    clk = clocks.stop()
     L.check_error()
     ms = max_over_ranks(ms, world)
     ms_step = ms / args.steps

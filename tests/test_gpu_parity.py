@@ -181,6 +181,24 @@ def test_dispatch_adversarial(case):
     _check_dispatch(ids, dp, E)
 
 
+@pytest.mark.parametrize("T,E,K,skew", [(1000, 8, 2, 0.0), (3000, 64, 6, 1.2),
+                                        (513, 128, 8, 0.0), (20000, 16, 4, 2.0)])
+def test_sort_dispatch_baseline_matches_oracle_and_ours(T, E, K, skew):
+    """The sort-based baseline of the dispatch ablation computes the same index."""
+    import bench
+    ids = I.random_ids_gumbel(T, E, K, seed=7, skew=skew)
+    eti, off, tim, _ = O.build_dispatch(ids.numpy(), E)
+    b_eti, b_off, b_tim = bench.sort_dispatch(ids.cuda(), E)
+    assert np.array_equal(cpu(b_eti), eti)
+    assert np.array_equal(cpu(b_off), off)
+    assert np.array_equal(cpu(b_tim), tim)
+    L = _layer(I.Shape(T, 128, E, K, 128))
+    dp = L.dispatch(ids.cuda())
+    L.check_error()
+    assert torch.equal(dp.eti, b_eti) and torch.equal(dp.offsets, b_off)
+    assert torch.equal(dp.tim, b_tim)
+
+
 def test_bad_expert_ids_raise_device_error():
     from token_dispatch_grouped_gb300 import binding as B
     s = I.Shape(64, 128, 8, 2, 128)

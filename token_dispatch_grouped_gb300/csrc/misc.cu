@@ -116,14 +116,20 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 
 constexpr int kCombThreads = 256;   // 8 warps; one warp per token at a time
 constexpr int kCombWarps = kCombThreads / 32;
+// A lane loads the K rows' pieces of U = max(1, 8 / K) 8-column pieces at once:
+// about 8 16-byte loads (4 KB per warp) in flight before any arithmetic.
+template <int K>
+constexpr int comb_u() { return K >= 8 ? 1 : 8 / K; }
 
 // Weighted combine of one chunk. Each warp takes a token (grid-stride), reads
 // its K (expert, position, weight) triples once, then every lane sums 8-column
-// pieces of the K expert-output rows in slot order and stores bf16. The chunk
-// buffer's rows hold columns [c0, c0 + nc) of the expert outputs, and
-// row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo).
+// pieces of the K expert-output rows in slot order and stores bf16; a lane
+// loads the pieces of all K rows for U column pieces before any arithmetic.
+// The chunk buffer's rows hold columns [c0, c0 + nc) of the expert outputs,
+// and row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo).
+template <int K>
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
+combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ ids,
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ Yc,
                __nv_bfloat16* __restrict__ y, int* err) {
@@ -139,17 +145,45 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* __re
             off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
             wl = topk_w[i];
         }
-        for (int c = lane * 8; c < nc; c += 32 * 8) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < K; ++k) {
-                const size_t ok = __shfl_sync(0xffffffffu, off, k);
-                const float w = __shfl_sync(0xffffffffu, wl, k);
-                float f[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4*>(Yc + ok + c), f);
+        constexpr int U = comb_u<K>();
+        size_t ok[K];
+        float w[K];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = fmaf(w, f[j], acc[j]);
+        for (int k = 0; k < K; ++k) {
+            ok[k] = __shfl_sync(0xffffffffu, off, k);
+            w[k] = __shfl_sync(0xffffffffu, wl, k);
+        }
+        for (int cb = lane * 8; cb < nc; cb += 32 * 8 * U) {
+            uint4 v[K][U];
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + u * 256;
+                    v[k][u] = c < nc ? *reinterpret_cast<const uint4*>(Yc + ok[k] + c)
+                                     : make_uint4(0, 0, 0, 0);
+                }
+            float acc[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float f[8];
+                    bf16x8_to_f32(v[k][u], f);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[u][j] = fmaf(w[k], f[j], acc[u][j]);
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + u * 256;
+                if (c < nc)
+                    *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) =
+                        f32_to_bf16x8(acc[u]);
             }
-            *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) = f32_to_bf16x8(acc);
         }
     }
 }
@@ -185,8 +219,9 @@ __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* 
 
 // Token-gradient sum of one chunk plus the router term:
 // dx_t = sum_k (dX~[row(t,k)] + dz_{t,k} W_g[e_{t,k}]), fp32, k ascending.
+template <int K>
 __global__ void __launch_bounds__(kCombThreads)
-dx_combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* __restrict__ ids,
+dx_combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ ids,
                   const float* __restrict__ dz, const int32_t* __restrict__ tim,
                   const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ dXc,
                   const float* __restrict__ Wg, __nv_bfloat16* __restrict__ dx, int* err) {
@@ -204,23 +239,54 @@ dx_combine_kernel(int t0, int t1, int c0, int nc, int d, int K, const int32_t* _
             off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
             zl = dz[i];
         }
-        for (int c = lane * 8; c < nc; c += 32 * 8) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < K; ++k) {
-                const size_t ok = __shfl_sync(0xffffffffu, off, k);
-                const int e = __shfl_sync(0xffffffffu, el, k);
-                const float z = __shfl_sync(0xffffffffu, zl, k);
-                float f[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4*>(dXc + ok + c), f);
-                const float* wg = Wg + static_cast<size_t>(e) * d + c0 + c;
-                const float4 g0 = *reinterpret_cast<const float4*>(wg);
-                const float4 g1 = *reinterpret_cast<const float4*>(wg + 4);
-                const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        constexpr int U = comb_u<K>();
+        size_t ok[K];
+        const float* wg[K];
+        float z[K];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] += f[j] + z * gz[j];
+        for (int k = 0; k < K; ++k) {
+            ok[k] = __shfl_sync(0xffffffffu, off, k);
+            wg[k] = Wg + static_cast<size_t>(__shfl_sync(0xffffffffu, el, k)) * d + c0;
+            z[k] = __shfl_sync(0xffffffffu, zl, k);
+        }
+        for (int cb = lane * 8; cb < nc; cb += 32 * 8 * U) {
+            uint4 v[K][U];
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + u * 256;
+                    v[k][u] = c < nc ? *reinterpret_cast<const uint4*>(dXc + ok[k] + c)
+                                     : make_uint4(0, 0, 0, 0);
+                }
+            float acc[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + u * 256;
+                    float f[8];
+                    bf16x8_to_f32(v[k][u], f);
+                    // W_g rows are small and stay in L2.
+                    const float4 g0 = c < nc ? *reinterpret_cast<const float4*>(wg[k] + c)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 g1 = c < nc ? *reinterpret_cast<const float4*>(wg[k] + c + 4)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[u][j] += f[j] + z[k] * gz[j];
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + u * 256;
+                if (c < nc)
+                    *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) =
+                        f32_to_bf16x8(acc[u]);
             }
-            *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) =
-                f32_to_bf16x8(acc);
         }
     }
 }
@@ -321,8 +387,18 @@ cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, c
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("combine", st);
-    combine_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, s.K, ids,
-                                                                topk_w, tim, seg, Yc, y, err);
+    const int grid = comb_grid(t1 - t0);
+    switch (s.K) {
+#define MOE_COMBINE_CASE(KK)                                                                  \
+    case KK:                                                                                  \
+        combine_kernel<KK><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, topk_w,   \
+                                                          tim, seg, Yc, y, err);              \
+        break;
+        MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
+        MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
+#undef MOE_COMBINE_CASE
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
@@ -341,8 +417,19 @@ cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc
                               __nv_bfloat16* dx, int* err, cudaStream_t st) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls("dx_combine", st);
-    dx_combine_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, s.K, ids,
-                                                                   dz, tim, seg, dXc, Wg, dx, err);
+    const int grid = comb_grid(t1 - t0);
+    switch (s.K) {
+#define MOE_DX_COMBINE_CASE(KK)                                                               \
+    case KK:                                                                                  \
+        dx_combine_kernel<KK><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, dz,    \
+                                                             tim, seg, dXc, Wg, dx, err);     \
+        break;
+        MOE_DX_COMBINE_CASE(1) MOE_DX_COMBINE_CASE(2) MOE_DX_COMBINE_CASE(3)
+        MOE_DX_COMBINE_CASE(4) MOE_DX_COMBINE_CASE(5) MOE_DX_COMBINE_CASE(6)
+        MOE_DX_COMBINE_CASE(7) MOE_DX_COMBINE_CASE(8)
+#undef MOE_DX_COMBINE_CASE
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -145,6 +145,19 @@ def random_ids(T: int, E: int, K: int, seed: int, skew: float = 0.0) -> torch.Te
     return ids.to(torch.int32).contiguous()
 
 
+def random_ids_gumbel(T: int, E: int, K: int, seed: int, skew: float = 0.0) -> torch.Tensor:
+    """Random valid top-K expert ids [T,K] int32 for large T: K distinct experts
+    per token drawn without replacement with probability proportional to
+    (rank+1)^-skew (uniform for skew = 0), by the Gumbel-top-K construction
+    (the K largest of log p_e + Gumbel noise)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    logp = -skew * torch.log(torch.arange(1, E + 1, dtype=torch.float32))
+    u = torch.rand(T, E, generator=g).clamp_(min=1e-12)
+    keys = logp - torch.log(-torch.log(u))
+    return keys.topk(K, dim=1).indices.to(torch.int32).contiguous()
+
+
 def random_weights(T: int, K: int, seed: int) -> torch.Tensor:
     """Positive routing weights [T,K] fp32, uniform on [0.05, 1.05)."""
     g = torch.Generator(device="cpu")
