@@ -182,7 +182,8 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     const int tc = moe_chunk_tokens(s);
     const int nc = nchunks_of(s, tc);
     const size_t TK = static_cast<size_t>(s.T) * s.K;
-    const int nparts = s.h / gemm_bn(G3_DH, s);
+    const int bn3 = gemm_bn(G3_DH, s);
+    const int nparts = (s.h + bn3 - 1) / bn3;
     Carve c;
     c.base = static_cast<char*>(ws);
     BwdWs w;
@@ -459,7 +460,8 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
     g3.dS_part = w.dS_part;
     g3.err = err;
     MOE_TRY(launch_gemm(g3, st));
-    const int nparts = s.h / gemm_bn(G3_DH, s);
+    const int bn3 = gemm_bn(G3_DH, s);
+    const int nparts = (s.h + bn3 - 1) / bn3;  // G3's N tiles, one dS partial each
     MOE_TRY(launch_router_dz(s, nparts, w.dS_part, topk_w, tim, dS, w.dz, w.dz_row, err, st));
 
     GemmProblem g4{};

@@ -112,6 +112,7 @@ struct Params {
     int Kdim;      // VM: reduction length
     int M;         // VK: rows of the output per expert
     int n_tiles;   // tiles along N
+    int n_half;    // G5: N tiles per half (dW1 | dW3); the last tile of a half may be partial
     int n_off;     // G2/G6: first output column of this launch (column chunk)
     int ldo;       // G2/G6: row stride of the output chunk buffer (elements)
     const Seg* segs;
@@ -458,13 +459,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
             const int row0 = t.lo + t.m_blk * BMC + rank * BM;   // VM: this CTA's A rows
-            const int ncol = t.n_blk * BN + rank * BNL;          // this CTA's B columns
+            // First B column of the tile inside its half (G5: dW1 | dW3), and
+            // this CTA's first B column in the B tensor.
+            const int nin = (KIND == G5_DW13 ? t.n_blk % p.n_half : t.n_blk) * BN;
+            const int ncol = (KIND == G5_DW13 ? (t.n_blk / p.n_half) * p.h : 0) + nin + rank * BNL;
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                     stop = true;
                     break;
                 }
-                if (leader && lane == 0) mbar_arrive_expect_tx(full_bar(stage), CTAS * TMA_BYTES);
+                if (leader && lane == 0) {
+                    uint32_t bytes = CTAS * TMA_BYTES;
+                    if constexpr (KIND == G3_DH || KIND == G3_DH_ACT || KIND == G4_DW2 ||
+                                  KIND == G5_DW13) {
+                        // h need not be a multiple of BN: 64-column B boxes that
+                        // start at or past h are not loaded (their output columns
+                        // are never stored).
+                        bytes = 0;
+                        for (int r = 0; r < CTAS; ++r)
+                            for (int l = 0; l < BNL / 64; ++l)
+                                if (nin + r * BNL + l * 64 < p.h) bytes += 8192;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                }
                 __syncwarp();
                 const uint32_t a_dst = sA + stage * C::A_BYTES;
                 const uint32_t b_dst = sB + stage * C::B_BYTES;
@@ -503,11 +520,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 } else if constexpr (KIND == G2_DOWN) {
                     if (lane == 0) load(b_dst, &mapB0, k0, t.e * p.d + p.n_off + ncol);
                 } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
-                    if (lane < BNL / 64)
+                    if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.e * p.d + k0);
                 } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13) {
                     // B rows of this expert (A' for dW2, dH for dW1/dW3), MN-major.
-                    if (lane < BNL / 64)
+                    if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.lo + k0);
                 } else {  // G6: K = 2h, first h from W1, then W3 (non-gated: K = h, W1).
                     if (lane < BNL / 64) {
@@ -664,6 +681,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 const int row0w = rbase + q * 32;
                 const int nvalid = t.hi - row0w;
                 const int n0 = t.n_blk * BN;
+                const int ncols = min(BN, p.h - n0);  // the last N tile may be partial
                 const size_t r0 = static_cast<size_t>(row0w > 0 ? row0w : 0);
                 const float w = valid ? p.wrow[r] : 0.f;
                 float dsum = 0.f;
@@ -680,11 +698,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     uint4 pa[4];
                     if (nvalid > 0) rows_fetch(pa, lane, Hw, p.h, nvalid);
 #pragma unroll 1
-                    for (int j = 0; j < BN; j += 32) {
+                    for (int j = 0; j < ncols; j += 32) {
                         uint4 ua[4];
                         if (nvalid > 0) {
                             box_get_row_raw(box_in, lane, pa, ua);
-                            if (j + 32 < BN) rows_fetch(pa, lane, Hw + j + 32, p.h, nvalid);
+                            if (j + 32 < ncols) rows_fetch(pa, lane, Hw + j + 32, p.h, nvalid);
                         }
                         tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
                         if (nvalid > 0) {
@@ -710,12 +728,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         rows_fetch(pb, lane, Hw + p.h, 2 * p.h, nvalid);
                     }
 #pragma unroll 1
-                    for (int j = 0; j < BN; j += 32) {
+                    for (int j = 0; j < ncols; j += 32) {
                         uint4 ua[4], ub[4];
                         if (nvalid > 0) {
                             box_get_row_raw(box_da, lane, pa, ua);
                             box_get_row_raw(box_db, lane, pb, ub);
-                            if (j + 32 < BN) {
+                            if (j + 32 < ncols) {
                                 rows_fetch(pa, lane, Hw + j + 32, 2 * p.h, nvalid);
                                 rows_fetch(pb, lane, Hw + p.h + j + 32, 2 * p.h, nvalid);
                             }
@@ -765,8 +783,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 // a shared-memory box and one TMA store (whole lines, asynchronous).
                 const bool empty = t.hi <= t.lo;
                 const int grow = t.e * p.d + mbase + q * 32;  // row in [E*d, h]
+                const int ncols = min(BN, p.h - t.n_blk * BN);  // the last N tile may be partial
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32, ++nstore) {
+                for (int j = 0; j < ncols; j += 32, ++nstore) {
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -789,12 +808,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 // a shared-memory box [n][m] and stored with one TMA store into
                 // dW1 or dW3 viewed as [E*h, d].
                 const bool empty = t.hi <= t.lo;
-                const int n0 = t.n_blk * BN;  // index into [0, 2h); never straddles h
-                const bool first_half = n0 < p.h;
-                const int nrow = t.e * p.h + (first_half ? n0 : n0 - p.h);
+                const bool first_half = t.n_blk < p.n_half;
+                const int n0 = (t.n_blk % p.n_half) * BN;  // first column inside the half
+                const int ncols = min(BN, p.h - n0);        // the last tile of a half may be partial
+                const int nrow = t.e * p.h + n0;
                 const int mcol = mbase + q * 32;
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32, ++nstore) {
+                for (int j = 0; j < ncols; j += 32, ++nstore) {
                     if (empty) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -1081,7 +1101,7 @@ int gemm_bn(GemmKind kind, const moe_shape& s) {
         case G6_DX: return s.d % 256 == 0 ? 256 : 128;
         case G3_DH:
         case G4_DW2:
-        case G5_DW13: return s.h % 256 == 0 ? 256 : 128;  // N tiles never straddle W1 | W3
+        case G5_DW13: return s.h >= 256 ? 256 : 128;  // the last N tile (of a half) may be partial
     }
     return 128;
 }
@@ -1144,7 +1164,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, 64);
             mp.a = mp.b1 = mp.o = mp.b0;
             prm.Kdim = s.d;
-            prm.n_tiles = s.h / BN;
+            prm.n_tiles = (s.h + BN - 1) / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
             break;
         case G4_DW2:  // A = dy gathered (MN-major, M = d); B = A' rows [TK, h]; TMA-stored dW2
@@ -1153,7 +1173,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             ok &= make_tmap_bf16(&mp.o, g.out0, E * d, h, 32, 32, false);
             mp.a = mp.b1 = mp.b0;
             prm.M = s.d;
-            prm.n_tiles = s.h / BN;
+            prm.n_tiles = (s.h + BN - 1) / BN;
             max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
         case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, hs]; TMA-stored
@@ -1164,7 +1184,8 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             else mp.b1 = mp.o;
             mp.a = mp.b0;
             prm.M = s.d;
-            prm.n_tiles = static_cast<int>(hs / BN);
+            prm.n_half = (s.h + BN - 1) / BN;
+            prm.n_tiles = (gated ? 2 : 1) * prm.n_half;
             max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
         case G6_DX:  // A = dH rows [TK, hs]; B = W1 | W3 [E*h, d] (or W1) read MN-major
