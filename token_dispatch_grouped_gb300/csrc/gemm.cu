@@ -94,7 +94,7 @@ struct Cfg {
     static constexpr int SMEM_EPI = 4 * EPI_BOXES * 2048;  // per epilogue warp: 32x32 bf16 boxes
     static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC + SMEM_EPI;
     static_assert(1024 + 16 * kMaxE + 4 * (kMaxE + 1) <= SMEM_MISC, "misc region");
-    static_assert(8 * (3 * STAGES + 4) + 16 <= 1024, "barrier region");
+    static_assert(8 * (3 * STAGES + 4) + 48 <= 1024, "barrier region");
 };
 
 constexpr int kGatherThreads = 128;
@@ -155,8 +155,9 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
 }
 
 // Warp-uniform bounded wait: every lane polls, all lanes agree on the result.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort, kWaitNs);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          bool cluster_scope = false) {
+    const bool ok = mbar_wait(bar, parity, abort, kWaitNs, cluster_scope);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -384,6 +385,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * C::STAGES + 2 + a); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (3 * C::STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 8 * (3 * C::STAGES + 4) + 8);
+    // 16-byte slot (16-byte aligned) for the relay's completion signal.
+    const uint32_t relay_slot = (smem_u32(misc) + 8 * (3 * C::STAGES + 4) + 16 + 15) & ~15u;
     Seg* s_segs = reinterpret_cast<Seg*>(misc + 1024);
     int* s_prefix = reinterpret_cast<int*>(misc + 1024 + 16 * kMaxE);
     uint8_t* epi = misc + C::SMEM_MISC;  // epilogue staging (TMA-store source)
@@ -415,7 +418,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int s = 0; s < C::STAGES; ++s) {
             // full: the producer's expect-tx arrival, this CTA's gather threads,
             // and in a pair the relay of the second CTA's gathers.
-            mbar_init(full_bar(s), 1 + (TR::A_G ? kGatherThreads : 0) + (TR::A_G && PAIR ? 1 : 0));
+            mbar_init(full_bar(s), 1 + (TR::A_G ? kGatherThreads : 0));
             mbar_init(empty_bar(s), 1);
             mbar_init(gfull_bar(s), kGatherThreads);
         }
@@ -480,6 +483,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                             for (int l = 0; l < BNL / 64; ++l)
                                 if (nin + r * BNL + l * 64 < p.h) bytes += 8192;
                     }
+                    // In a gathering pair, the relay's 16-byte signal copy.
+                    if constexpr (TR::A_G && PAIR) bytes += 16;
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                 }
                 __syncwarp();
@@ -551,12 +556,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) break;
+                // In a pair, the second CTA's epilogue and relay arrive from the
+                // other SM: acquire at cluster scope.
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, PAIR)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * NMMA;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!warp_wait(full_bar(stage), phase, abort_flag)) {
+                    if (!warp_wait(full_bar(stage), phase, abort_flag, PAIR)) {
                         ok = false;
                         break;
                     }
@@ -982,11 +989,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if constexpr (TR::A_G && PAIR) {
             // =========================== relay (warp 10 of the second CTA)
             // Waits for this CTA's gathered stage, makes it visible to the async
-            // proxy and arrives on the first CTA's full barrier.
+            // proxy, then signals the first CTA's full barrier through the bulk-
+            // copy engine: a 16-byte shared-to-shared copy whose bytes complete
+            // on that barrier. The relay thread never waits on a cluster fence,
+            // so the signals of consecutive stages overlap.
             if (!leader) {
                 int stage = 0;
                 uint32_t phase = 0;
                 bool stop = false;
+                const uint32_t dst = mapa_shared(relay_slot, 0);
                 for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
                     const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
                     const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
@@ -996,7 +1007,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                             break;
                         }
                         fence_proxy_async_smem();
-                        if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(stage), 0));
+                        if (lane == 0)
+                            bulk_copy_s2c(dst, relay_slot, 16, mapa_shared(full_bar(stage), 0));
                         __syncwarp();
                         if (++stage == C::STAGES) {
                             stage = 0;
@@ -1074,20 +1086,20 @@ cudaError_t launch_ctas(int ctas, int BN, const Maps& mp, const Params& prm, int
                      : launch_bn<KIND, 1>(BN, mp, prm, max_tiles, st, name);
 }
 
-// CTA pairs halve each SM's share of the B tile (more stages in flight) but
-// double the tile height. Measured on GB300 (Mixtral-shaped layer): the pair
-// speeds up the TMA-fed GEMMs (G2, G6) by 8-14% once experts hold a few
-// hundred rows, while the gathered kinds run 2-3x slower through the relay of
-// the second CTA's cp.async completions, so those stay on single CTAs.
-// MOE_GEMM_CTAS=1|2 forces one mode wherever it is legal (VK needs d % 256 == 0).
+// CTA pairs halve each SM's share of the B tile (more stages in flight, half
+// the operand bytes per SM per MMA) but double the tile height. Measured on
+// GB300 (Mixtral-shaped and fine-grained layers): pairs speed up the
+// row-tiled GEMMs (G1, G2, G3, G6) by 2-14% once experts hold a few hundred
+// rows; the weight-gradient GEMMs (G4, G5) run 15-30% slower as pairs and stay
+// on single CTAs. MOE_GEMM_CTAS=1|2 forces one mode wherever it is legal (VK
+// needs d % 256 == 0).
 int choose_ctas(GemmKind kind, const moe_shape& s) {
     static const char* force = std::getenv("MOE_GEMM_CTAS");
     const bool vk = kind == G4_DW2 || kind == G5_DW13;
     const bool ok2 = vk ? (s.d % 256 == 0) : true;
     if (force != nullptr && (force[0] == '1' || force[0] == '2'))
         return (force[0] == '2' && ok2) ? 2 : 1;
-    const bool gathered = kind == G1_UP || kind == G3_DH || kind == G4_DW2 || kind == G5_DW13;
-    if (!ok2 || gathered) return 1;
+    if (vk) return 1;
     const long long rows_per_expert = static_cast<long long>(s.T) * s.K / s.E;
     return rows_per_expert >= 384 ? 2 : 1;
 }

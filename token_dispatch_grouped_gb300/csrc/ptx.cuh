@@ -49,18 +49,64 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// nanoseconds while the phase is incomplete (it resumes when the phase
+// completes), so a waiting warp does not take issue slots from the others.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// As mbar_try_wait_sleep with acquire at cluster scope: for barriers that
+// receive arrivals from another CTA of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_sleep_cluster(uint32_t bar, uint32_t parity,
+                                                            uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up after
 // `limit_ns` or as soon as *abort becomes non-zero; returns false then (and
-// sets *abort on a time-out).
-// The global timer and the abort flag are read only every 64 polls: a timer
-// read is slow, and checking it on every poll delays the waiter's reaction.
+// sets *abort on a time-out). Polls suspend the thread for at most 20 us each,
+// and the timer and the abort flag are read every 16 polls.
+// With cluster_scope the acquire is at cluster scope (arrivals from a peer CTA).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                          uint64_t limit_ns, bool cluster_scope = false) {
+    if (!cluster_scope && mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0) {
+        if (cluster_scope ? mbar_try_wait_sleep_cluster(bar, parity, 20000u)
+                          : mbar_try_wait_sleep(bar, parity, 20000u))
+            return true;
+        if ((i & 15u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
@@ -92,6 +138,15 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
     return v;
+}
+// Arrive on a peer CTA's mbarrier without ordering earlier memory accesses
+// (pair with fence_acq_rel_cluster before it).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
@@ -149,6 +204,18 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                      reinterpret_cast<uint64_t>(map)),
                  "r"(src), "r"(c0), "r"(c1)
                  : "memory");
+}
+// Shared-memory copy from this CTA to another CTA of the cluster through the
+// bulk-copy (async) engine; the bytes are counted on the destination CTA's
+// mbarrier `cluster_bar` (same CTA as `cluster_dst`). 16-byte aligned, size a
+// multiple of 16.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t cluster_dst, uint32_t src, uint32_t bytes,
+                                              uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(cluster_dst),
+        "r"(src), "r"(bytes), "r"(cluster_bar)
+        : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
