@@ -498,13 +498,15 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
         g6.b_src0 = W1;
         g6.b_src1 = W3;
         g6.out0 = w.dXc;
+        g6.wrow = w.dz_row;  // router term dz_r W_g[e] added in the epilogue
+        g6.aux0 = Wg;
         g6.n_off = pl.by_cols ? c * pl.dc : 0;
         g6.n_cols = pl.by_cols ? pl.dc : s.d;
         g6.err = err;
         MOE_TRY(launch_gemm(g6, st));
         const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
-        MOE_TRY(launch_dx_combine(s, t0, t1, g6.n_off, g6.n_cols, topk_ids, w.dz, tim, sc,
-                                  w.dXc, Wg, static_cast<__nv_bfloat16*>(dx), err, st));
+        MOE_TRY(launch_combine(s, t0, t1, g6.n_off, g6.n_cols, topk_ids, nullptr, tim, sc, w.dXc,
+                               static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
     }
     MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), eti, offsets, w.dz_row,
                               w.dwg_part, dWg, err, st));

@@ -69,16 +69,15 @@ cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchu
                                   cudaStream_t st);
 cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const int32_t* tim,
                                float* wrow, int* err, cudaStream_t st);
+// topk_w == nullptr sums with weight 1 (the token-gradient sum); `name` labels
+// the launch for the kernel timer.
 cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
-                           const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st);
+                           const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st,
+                           const char* name = "combine");
 cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
                              float* dz_row, int* err, cudaStream_t st);
-cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc,
-                              const int32_t* ids, const float* dz, const int32_t* tim,
-                              const Seg* seg, const __nv_bfloat16* dXc, const float* Wg,
-                              __nv_bfloat16* dx, int* err, cudaStream_t st);
 int dwg_parts();
 cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
                               const int32_t* offsets, const float* dz_row, float* part,

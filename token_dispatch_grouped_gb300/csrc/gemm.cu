@@ -44,7 +44,8 @@
 //       A, M = d), dH rows (MN-major B); the epilogue stores the transpose.
 //       (MoEBlaze Algorithm 1, FusedBwdW). Non-gated: [d, h] = dW1_e^T.
 //   G6  dX~ [T_e, d] = da W1_e + db W3_e   one accumulator over K = 2h
-//       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer).
+//       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer);
+//       the epilogue adds the router term dz_r W_g[e] of each row.
 //       Non-gated: K = h, da W1_e.
 // The saved pre-activation H and its gradient dH are [TK, hs] with hs = 2h
 // (a | b) for SwiGLU and hs = h (a) for non-gated experts.
@@ -674,10 +675,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 __nv_bfloat16* out =
                     static_cast<__nv_bfloat16*>(p.out0) +
                     static_cast<size_t>(t.out + (row0w - t.lo)) * p.ldo + t.n_blk * BN;
+                // G6 adds the router term dz_r W_g[e] of its row: every row of the
+                // tile belongs to expert e, so W_g[e] is one broadcast vector.
+                float dzr = 0.f;
+                const float* wg = nullptr;
+                if constexpr (KIND == G6_DX) {
+                    const int r = rbase + row_in_tile;
+                    dzr = r < t.hi ? p.wrow[r] : 0.f;
+                    wg = static_cast<const float*>(p.aux0) + static_cast<size_t>(t.e) * p.d +
+                         p.n_off + t.n_blk * BN;
+                }
 #pragma unroll 1
                 for (int j = 0; j < BN; j += 32) {
                     tmem_ld32f(tacc + j, v);
                     if (nvalid > 0) {
+                        if constexpr (KIND == G6_DX) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 g = *reinterpret_cast<const float4*>(wg + j + i);
+                                v[i] = fmaf(dzr, g.x, v[i]);
+                                v[i + 1] = fmaf(dzr, g.y, v[i + 1]);
+                                v[i + 2] = fmaf(dzr, g.z, v[i + 2]);
+                                v[i + 3] = fmaf(dzr, g.w, v[i + 3]);
+                            }
+                        }
                         box_put_row(stg, lane, v);
                         box_store_rows(stg, lane, out + j, p.ldo, nvalid);
                     }

@@ -11,9 +11,11 @@
 //   router_dz (R2a) dS_{t,k} = sum over N-tiles of the partial <dA'_r, A_r>;
 //                   dz_k = w_k (dS_k - sum_j w_j dS_j): the Jacobian of the
 //                   softmax over the chosen logits applied to dS.
-//   dx_combine(C2)  dx_t = sum_k (dX~[row(t,k)] + dz_{t,k} W_g[e_{t,k}]), fp32,
-//                   k ascending. MoEBlaze paper notes 3.2 (token gradient
-//                   accumulation over the K routed rows).
+//   combine also serves C2 (weights 1): dx_t = sum_k dX~'[row(t,k)], fp32, k
+//                   ascending, where dX~' already holds the router term
+//                   dz_{t,k} W_g[e_{t,k}] (added in the dX GEMM's epilogue).
+//                   MoEBlaze paper notes 3.2 (token gradient accumulation over
+//                   the K routed rows).
 //   router_dwg(R2b) dW_g = dz^T x as per-expert sums over the expert's rows
 //                   (partials over 32 row parts, then a fixed-order sum).
 // All sums run in a fixed order, so results are bit-reproducible.
@@ -143,7 +145,7 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
             const size_t i = static_cast<size_t>(t) * K + lane;
             const Seg sg = seg[ids[i]];
             off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
-            wl = topk_w[i];
+            wl = topk_w != nullptr ? topk_w[i] : 1.f;
         }
         constexpr int U = comb_u<K>();
         size_t ok[K];
@@ -214,80 +216,6 @@ __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* 
         dS[i] = s[k];
         dz[i] = z;
         dz_row[rows[k]] = z;
-    }
-}
-
-// Token-gradient sum of one chunk plus the router term:
-// dx_t = sum_k (dX~[row(t,k)] + dz_{t,k} W_g[e_{t,k}]), fp32, k ascending.
-template <int K>
-__global__ void __launch_bounds__(kCombThreads)
-dx_combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ ids,
-                  const float* __restrict__ dz, const int32_t* __restrict__ tim,
-                  const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ dXc,
-                  const float* __restrict__ Wg, __nv_bfloat16* __restrict__ dx, int* err) {
-    if (has_error(err)) return;
-    const int lane = threadIdx.x & 31;
-    for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
-         t += gridDim.x * kCombWarps) {
-        size_t off = 0;
-        int el = 0;
-        float zl = 0.f;
-        if (lane < K) {
-            const size_t i = static_cast<size_t>(t) * K + lane;
-            el = ids[i];
-            const Seg sg = seg[el];
-            off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
-            zl = dz[i];
-        }
-        constexpr int U = comb_u<K>();
-        size_t ok[K];
-        const float* wg[K];
-        float z[K];
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-            ok[k] = __shfl_sync(0xffffffffu, off, k);
-            wg[k] = Wg + static_cast<size_t>(__shfl_sync(0xffffffffu, el, k)) * d + c0;
-            z[k] = __shfl_sync(0xffffffffu, zl, k);
-        }
-        for (int cb = lane * 8; cb < nc; cb += 32 * 8 * U) {
-            uint4 v[K][U];
-#pragma unroll
-            for (int k = 0; k < K; ++k)
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = cb + u * 256;
-                    v[k][u] = c < nc ? *reinterpret_cast<const uint4*>(dXc + ok[k] + c)
-                                     : make_uint4(0, 0, 0, 0);
-                }
-            float acc[U][8];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
-#pragma unroll
-            for (int k = 0; k < K; ++k)
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int c = cb + u * 256;
-                    float f[8];
-                    bf16x8_to_f32(v[k][u], f);
-                    // W_g rows are small and stay in L2.
-                    const float4 g0 = c < nc ? *reinterpret_cast<const float4*>(wg[k] + c)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 g1 = c < nc ? *reinterpret_cast<const float4*>(wg[k] + c + 4)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float gz[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[u][j] += f[j] + z[k] * gz[j];
-                }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = cb + u * 256;
-                if (c < nc)
-                    *reinterpret_cast<uint4*>(dx + static_cast<size_t>(t) * d + c0 + c) =
-                        f32_to_bf16x8(acc[u]);
-            }
-        }
     }
 }
 
@@ -384,9 +312,10 @@ int comb_grid(int tokens) {
 
 cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
-                           const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st) {
+                           const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st,
+                           const char* name) {
     if (t1 <= t0) return cudaSuccess;
-    LaunchScope ls("combine", st);
+    LaunchScope ls(name, st);
     const int grid = comb_grid(t1 - t0);
     switch (s.K) {
 #define MOE_COMBINE_CASE(KK)                                                                  \
@@ -408,28 +337,6 @@ cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_par
     LaunchScope ls("router_dz", st);
     router_dz_kernel<<<(s.T + 127) / 128, 128, 0, st>>>(s.T, s.K, s.T * s.K, nparts, dS_part,
                                                         topk_w, tim, dS, dz, dz_row, err);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_dx_combine(const moe_shape& s, int t0, int t1, int c0, int nc,
-                              const int32_t* ids, const float* dz, const int32_t* tim,
-                              const Seg* seg, const __nv_bfloat16* dXc, const float* Wg,
-                              __nv_bfloat16* dx, int* err, cudaStream_t st) {
-    if (t1 <= t0) return cudaSuccess;
-    LaunchScope ls("dx_combine", st);
-    const int grid = comb_grid(t1 - t0);
-    switch (s.K) {
-#define MOE_DX_COMBINE_CASE(KK)                                                               \
-    case KK:                                                                                  \
-        dx_combine_kernel<KK><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, dz,    \
-                                                             tim, seg, dXc, Wg, dx, err);     \
-        break;
-        MOE_DX_COMBINE_CASE(1) MOE_DX_COMBINE_CASE(2) MOE_DX_COMBINE_CASE(3)
-        MOE_DX_COMBINE_CASE(4) MOE_DX_COMBINE_CASE(5) MOE_DX_COMBINE_CASE(6)
-        MOE_DX_COMBINE_CASE(7) MOE_DX_COMBINE_CASE(8)
-#undef MOE_DX_COMBINE_CASE
-        default: return cudaErrorInvalidValue;
-    }
     return cudaGetLastError();
 }
 
