@@ -935,8 +935,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 // MN-major A: 64 k-rows (tokens) x 128 m-columns in two 64-column
                 // chunks of 8 KB; this thread copies 16-byte chunk col16 of column
                 // chunk ch for token rows rb + 8 j, j = 0..7. Work items (tile,
-                // k-block) are walked with a one-item lookahead for the row indices;
-                // tiles of experts without rows have no k-blocks and are skipped.
+                // k-block) change their row indices every k-block, so the indices
+                // are loaded kLook items ahead (a ring of register slots, about a
+                // microsecond of lead); tiles of experts without rows have no
+                // k-blocks and are skipped.
+                constexpr int kLook = 4;
                 const int ch = (g >> 3) & 1;
                 const int rb = g >> 4;
                 const uint32_t soff =
@@ -959,6 +962,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                     return false;
                 };
+                auto advance = [&](Pos& ps) -> bool {  // ps := the item after ps
+                    if (ps.kb + 1 < ps.nkb) {
+                        ++ps.kb;
+                        return true;
+                    }
+                    return first_from(ps.tile + tstep, ps);
+                };
                 auto load_idx = [&](const Pos& ps, int (&dst)[8]) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -966,42 +976,54 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         dst[j] = r < ps.t.hi ? p.eti[r] : -1;
                     }
                 };
-                Pos cur{};
-                bool have = first_from(tile0, cur);
-                int idx[8], nxt[8];
-                if (have) load_idx(cur, idx);
-                while (have && !stop) {
-                    Pos nx = cur;
-                    bool have_next;
-                    if (cur.kb + 1 < cur.nkb) {
-                        nx.kb = cur.kb + 1;
-                        have_next = true;
-                    } else {
-                        have_next = first_from(cur.tile + tstep, nx);
-                    }
-                    if (have_next) load_idx(nx, nxt);
-                    if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
-                        stop = true;
-                        break;
-                    }
-                    const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
-                    const size_t coff =
-                        static_cast<size_t>(cur.t.m_blk * BMC + rank * BM + ch * 64) * 2 +
-                        col16 * 16;
+                Pos slot[kLook];
+                int idx[kLook][8];
+                bool have[kLook];
+                Pos tail{};
+                bool more = first_from(tile0, tail);  // tail: the next item to prefetch
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
-                        cp_async16(a_dst + j * 8 * 128, src, idx[j] >= 0 ? 16u : 0u);
+                for (int u = 0; u < kLook; ++u) {
+                    have[u] = more;
+                    if (more) {
+                        slot[u] = tail;
+                        load_idx(tail, idx[u]);
+                        more = advance(tail);
                     }
-                    cp_async_arrive_noinc(done_bar(stage));
-                    if (++stage == C::STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                }
+                bool done = !have[0];
+                while (!done && !stop) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) idx[j] = nxt[j];
-                    cur = nx;
-                    have = have_next;
+                    for (int u = 0; u < kLook; ++u) {
+                        if (!have[u]) {  // items are assigned in order: the rest are empty
+                            done = true;
+                            break;
+                        }
+                        if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                            stop = true;
+                            break;
+                        }
+                        const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
+                        const size_t coff =
+                            static_cast<size_t>(slot[u].t.m_blk * BMC + rank * BM + ch * 64) * 2 +
+                            col16 * 16;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int ix = idx[u][j];
+                            const char* src = src0 + (ix >= 0 ? ix * rowbytes + coff : 0);
+                            cp_async16(a_dst + j * 8 * 128, src, ix >= 0 ? 16u : 0u);
+                        }
+                        cp_async_arrive_noinc(done_bar(stage));
+                        if (++stage == C::STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        have[u] = more;  // refill this slot kLook items ahead
+                        if (more) {
+                            slot[u] = tail;
+                            load_idx(tail, idx[u]);
+                            more = advance(tail);
+                        }
+                    }
                 }
             }
             cp_async_wait_all();
