@@ -1131,18 +1131,18 @@ cudaError_t launch_ctas(int ctas, int BN, const Maps& mp, const Params& prm, int
 
 // CTA pairs halve each SM's share of the B tile (more stages in flight, half
 // the operand bytes per SM per MMA) but double the tile height. Measured on
-// GB300 (Mixtral-shaped and fine-grained layers): pairs speed up the
+// GB300 (Mixtral-shaped, fine-grained and skewed layers): pairs speed up the
 // row-tiled GEMMs (G1, G2, G3, G6) by 2-14% once experts hold a few hundred
-// rows; the weight-gradient GEMMs (G4, G5) run 15-30% slower as pairs and stay
-// on single CTAs. MOE_GEMM_CTAS=1|2 forces one mode wherever it is legal (VK
-// needs d % 256 == 0).
+// rows, and the weight-gradient GEMMs (G4, G5) by 3-5% (their tile height is
+// d, so they pair whenever d % 256 == 0). MOE_GEMM_CTAS=1|2 forces one mode
+// wherever it is legal.
 int choose_ctas(GemmKind kind, const moe_shape& s) {
     static const char* force = std::getenv("MOE_GEMM_CTAS");
     const bool vk = kind == G4_DW2 || kind == G5_DW13;
     const bool ok2 = vk ? (s.d % 256 == 0) : true;
     if (force != nullptr && (force[0] == '1' || force[0] == '2'))
         return (force[0] == '2' && ok2) ? 2 : 1;
-    if (vk) return 1;
+    if (vk) return ok2 ? 2 : 1;
     const long long rows_per_expert = static_cast<long long>(s.T) * s.K / s.E;
     return rows_per_expert >= 384 ? 2 : 1;
 }
