@@ -312,6 +312,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0 = auto)")
     ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--combine", default="chunked", choices=["chunked", "slotwise"],
+                    help="forward combine: chunked expert-output passes (moe_forward) or "
+                         "fused into the down projection slot by slot (moe_forward_slotwise)")
     ap.add_argument("--dispatch-ablation", action="store_true",
                     help="time the dispatch build against a sort-based baseline and exit")
     args = ap.parse_args()
@@ -352,11 +355,13 @@ def main():
     bias = dv["bias"]
     st = torch.cuda.current_stream(dev)
 
+    fwd = B.moe_forward_slotwise if args.combine == "slotwise" else B.moe_forward
+
     def step(x, dy):
         B.moe_route(L.s, x, dv["Wg"], bias, r.logits, r.ids, r.w, L.ws)
         B.moe_build_dispatch(L.s, r.ids, dp.eti, dp.offsets, dp.tim, L.ws)
-        B.moe_forward(L.s, x, dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti, dp.offsets,
-                      dp.tim, y, H, L.ws)
+        fwd(L.s, x, dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti, dp.offsets, dp.tim, y, H,
+            L.ws)
         B.moe_backward(L.s, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti,
                        dp.offsets, dp.tim, H, grads["dx"], grads["dWg"], grads["dW1"],
                        grads["dW3"], grads["dW2"], grads["dS"], L.ws)
@@ -369,7 +374,8 @@ def main():
     L.check_error()
     torch.cuda.synchronize(dev)
     routed_bytes = s.T * s.K * s.d * 2
-    ws_f = B.moe_workspace_size(L.s, B.MOE_WS_FORWARD)
+    ws_f = B.moe_workspace_size(L.s, B.MOE_WS_FORWARD_SLOTWISE if args.combine == "slotwise"
+                                else B.MOE_WS_FORWARD)
     ws_b = B.moe_workspace_size(L.s, B.MOE_WS_BACKWARD)
     saved = H.numel() * 2 + 3 * TK * 4 + (s.E + 1) * 4 + 2 * TK * 4
     memory = {"routed_buffer_bytes_not_allocated": routed_bytes,
@@ -499,7 +505,7 @@ def main():
         line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
                     warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
-                    config=workload_config(s, name), tflops=tflops,
+                    config=dict(workload_config(s, name), combine=args.combine), tflops=tflops,
                     frac_of_bf16_peak=tflops / peaks["bf16_sus"],
                     peak_note=f"{peaks['src']} bf16 sustained {peaks['bf16_sus']} TFLOP/s",
                     memory=memory, roofline=roof, kernels=kernels, memory_bound=memory_bound,

@@ -92,7 +92,8 @@ enum moe_workspace_kind {
     MOE_WS_ROUTE = 0,
     MOE_WS_DISPATCH = 1,
     MOE_WS_FORWARD = 2,
-    MOE_WS_BACKWARD = 3
+    MOE_WS_BACKWARD = 3,
+    MOE_WS_FORWARD_SLOTWISE = 4
 };
 
 /* Bytes of device workspace that the call `which` needs for shape s (0 if the
@@ -170,6 +171,23 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
                 const int32_t* expert_token_indices, const int32_t* expert_token_offsets,
                 const int32_t* token_index_map,
                 void* y, void* H_saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward with the weighted combine fused into the down projection (same
+ * arguments and outputs as moe_forward; workspace MOE_WS_FORWARD_SLOTWISE).
+ * The down projection runs once per routing slot k = 0..K-1 over the rows
+ * (t, k) of that slot, grouped by expert; its epilogue adds w_{t,k} Y_{t,k}
+ * into an fp32 accumulator row of token t (each token appears once per slot,
+ * so no atomics and a fixed order), and the last slot writes bf16 y. No
+ * expert-output buffer exists; the accumulator holds T*d fp32 values (K >= 2)
+ * and is read and written once per slot, K*T*d*8 bytes in total, against the
+ * 4*T*K*d bytes of the chunked combine. y is not rounded to bf16 between the
+ * expert output and the sum (moe_forward rounds each Y row once).
+ * [SonicMoE 3.4.1, O_t = sum_k s_{t,k} Y_{t,k}; MoEBlaze paper notes 5.2] */
+int moe_forward_slotwise(moe_shape s, const void* x, const void* W1, const void* W3,
+                         const void* W2, const int32_t* topk_ids, const float* topk_w,
+                         const int32_t* expert_token_indices,
+                         const int32_t* expert_token_offsets, const int32_t* token_index_map,
+                         void* y, void* H_saved, void* ws, size_t ws_bytes, void* stream);
 
 /* Backward with upstream gradient dy [T,d] bf16. Outputs: dx [T,d] bf16
  * (expert and router paths), dWg [E,d] fp32, dW1, dW3 [E,h,d] bf16 (dW3 is

@@ -44,6 +44,10 @@ def test_host_functions():
     assert fwd >= TK * 14336 * 2 + 1024 * 2 * 4096 * 2
     assert fwd < TK * 14336 * 2 + 4096 * 2 * 4096 * 2 // 2
     assert B.moe_workspace_size(s, B.MOE_WS_ROUTE) == 0
+    # slot-wise forward: no chunk buffer, an fp32 [T, d] accumulator instead
+    slot = B.moe_workspace_size(s, B.MOE_WS_FORWARD_SLOTWISE)
+    assert slot >= TK * 14336 * 2 + 4096 * 4096 * 4
+    assert slot < TK * 14336 * 2 + 4096 * 4096 * 4 + 8 * 2**20
     for bad in (B.shape(0, 128, 8, 2, 128), B.shape(8, 100, 8, 2, 128), B.shape(8, 128, 4, 5, 128),
                 B.shape(8, 128, 300, 2, 128), B.shape(8, 128, 16, 9, 128)):
         assert B.moe_workspace_size(bad, B.MOE_WS_FORWARD) == 0

@@ -95,6 +95,33 @@ def test_layer_small_full_parity(s):
         assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
 
 
+# Slot-wise forward (combine fused into the down projection): ragged tiles, K = 1
+# (no accumulator), K = E = 8, CTA-pair shapes and a non-gated expert.
+SLOTWISE = [I.Shape(300, 256, 6, 3, 512), I.Shape(1500, 128, 16, 1, 256),
+            I.Shape(129, 384, 8, 8, 128), I.Shape(2100, 512, 4, 2, 512),
+            I.Shape(1100, 512, 8, 2, 768, "relu")]
+
+
+@pytest.mark.parametrize("s", SLOTWISE, ids=_sid)
+def test_forward_slotwise_parity(s):
+    inp = I.make_layer_inputs(s, seed=5)
+    dv = to_dev(inp)
+    L = _layer(s)
+    r = L.route(dv["x"], dv["Wg"])
+    dp = L.dispatch(r.ids)
+    y = torch.full((s.T, s.d), float("nan"), dtype=torch.bfloat16, device="cuda")  # poison
+    y, H = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp, y=y, combine="slotwise")
+    y_c, H_c = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp, combine="chunked")
+    y_again, _ = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp, combine="slotwise")
+    L.check_error()
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], cpu(r.ids), cpu(r.w), s.expert)
+    assert not np.isnan(cpu(y)).any()
+    assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
+    assert torch.equal(H, H_c)                     # the up projection is shared
+    assert rel_fro(cpu(y), cpu(y_c)) <= TOL_BF16   # same sum, one rounding fewer
+    assert torch.equal(y, y_again)                 # fixed order: bit-reproducible
+
+
 # Router shapes that exercise the cluster split of the reduction over d (2, 4 and
 # 8 CTAs), every padded expert width (8 .. 256), E not a multiple of 8, and a bias.
 ROUTER = [(256, 2048, 8, 2), (1000, 1024, 16, 4), (300, 512, 64, 6), (500, 1024, 128, 8),
@@ -278,6 +305,12 @@ def test_full_workload_sampled(name):
     ys, dSs, dxs = O.tokens_forward_backward(toks, inp["x"], inp["dO"], inp["Wg"], inp["W1"],
                                              inp["W3"], inp["W2"], ids, w, s.expert)
     assert rel_fro(cpu(y)[toks], ys) <= TOL_BF16
+    if name in ("mixtral", "skew"):  # slot-wise forward at full size (K = 2 and K = 8)
+        L = _layer(s)
+        dv = to_dev(inp)
+        y_s, _ = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp, combine="slotwise")
+        L.check_error()
+        assert rel_fro(cpu(y_s)[toks], ys) <= TOL_BF16
     assert rel_fro(cpu(g["dS"])[toks], dSs) <= TOL_BF16
     assert rel_fro(cpu(g["dx"])[toks], dxs) <= TOL_BF16
     # weight gradients on sampled (expert, hidden unit) pairs

@@ -28,6 +28,7 @@ MOE_ERR_STATIC_SCRATCH_LIMIT = 9
 MOE_NOALLOC_DISPATCH_MAX_ENTRIES = 1 << 20
 
 MOE_WS_ROUTE, MOE_WS_DISPATCH, MOE_WS_FORWARD, MOE_WS_BACKWARD = 0, 1, 2, 3
+MOE_WS_FORWARD_SLOTWISE = 4
 
 MOE_EXPERT_SWIGLU, MOE_EXPERT_SILU, MOE_EXPERT_RELU = 0, 1, 2
 EXPERT_CODES = {"swiglu": MOE_EXPERT_SWIGLU, "silu": MOE_EXPERT_SILU, "relu": MOE_EXPERT_RELU}
@@ -66,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "moe_build_dispatch": (I, [MoeShape, P, P, P, P, P, S, P]),
         "moe_build_dispatch_noalloc": (I, [MoeShape, P, P, P, P, P]),
         "moe_forward": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
+        "moe_forward_slotwise": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_backward": (I, [MoeShape] + [P] * 19 + [S, P]),
         "moe_get_error": (I, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
@@ -156,6 +158,19 @@ def moe_forward(s, x, W1, W3, W2, topk_ids, topk_w, eti, offsets, tim, y, H_save
                          0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     if check:
         _check(rc, "moe_forward")
+    return rc
+
+
+def moe_forward_slotwise(s, x, W1, W3, W2, topk_ids, topk_w, eti, offsets, tim, y, H_saved, ws,
+                         stream=None, check=True):
+    """moe_forward with the combine fused into the down projection, slot by slot."""
+    rc = LIB.moe_forward_slotwise(s, _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(topk_ids),
+                                  _ptr(topk_w), _ptr(eti), _ptr(offsets), _ptr(tim), _ptr(y),
+                                  _ptr(H_saved), _ptr(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(),
+                                  _stream(stream))
+    if check:
+        _check(rc, "moe_forward_slotwise")
     return rc
 
 

@@ -200,6 +200,33 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     return align_up(c.off, 256);
 }
 
+struct SlotWs {
+    Seg* segs;        // [E] whole-row-space segments (G1), then [K][E] per slot
+    __nv_bfloat16* Aact;
+    int32_t* eti_k;   // [K][T]
+    int32_t* off_k;   // [K][E+1]
+    int32_t* tim_k;   // [K][T] (written by the slot dispatch, unused)
+    int32_t* hist;    // [K][ceil(T/256)][E]
+    float* acc;       // [T, d] fp32 accumulator of y (K >= 2)
+};
+
+size_t layout_fwd_slot(const moe_shape& s, void* ws, SlotWs* o) {
+    const size_t TK = static_cast<size_t>(s.T) * s.K;
+    const size_t nblk = (s.T + dispatch_block_tokens() - 1) / dispatch_block_tokens();
+    Carve c;
+    c.base = static_cast<char*>(ws);
+    SlotWs w;
+    w.segs = c.take<Seg>(static_cast<size_t>(s.K + 1) * s.E);
+    w.Aact = c.take<__nv_bfloat16>(TK * s.h);
+    w.eti_k = c.take<int32_t>(TK);
+    w.off_k = c.take<int32_t>(static_cast<size_t>(s.K) * (s.E + 1));
+    w.tim_k = c.take<int32_t>(TK);
+    w.hist = c.take<int32_t>(static_cast<size_t>(s.K) * nblk * s.E);
+    w.acc = s.K > 1 ? c.take<float>(static_cast<size_t>(s.T) * s.d) : nullptr;
+    if (o) *o = w;
+    return align_up(c.off, 256);
+}
+
 size_t layout_dispatch(const moe_shape& s, void* ws, int32_t** hist) {
     const int nblk = (s.T + dispatch_block_tokens() - 1) / dispatch_block_tokens();
     Carve c;
@@ -313,6 +340,7 @@ size_t moe_workspace_size(moe_shape s, int which) {
         case MOE_WS_DISPATCH: return layout_dispatch(s, nullptr, nullptr);
         case MOE_WS_FORWARD: return layout_fwd(s, nullptr, nullptr);
         case MOE_WS_BACKWARD: return layout_bwd(s, nullptr, nullptr);
+        case MOE_WS_FORWARD_SLOTWISE: return layout_fwd_slot(s, nullptr, nullptr);
     }
     return 0;
 }
@@ -407,6 +435,65 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
         const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
         MOE_TRY(launch_combine(s, t0, t1, g2.n_off, g2.n_cols, topk_ids, topk_w, tim, sc, w.Yc,
                                static_cast<__nv_bfloat16*>(y), err, st));
+    }
+    return MOE_OK;
+}
+
+int moe_forward_slotwise(moe_shape s, const void* x, const void* W1, const void* W3,
+                         const void* W2, const int32_t* topk_ids, const float* topk_w,
+                         const int32_t* eti, const int32_t* offsets, const int32_t* tim, void* y,
+                         void* H_saved, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (!x || !W1 || (gated(s) && !W3) || !W2 || !topk_ids || !topk_w || !eti || !offsets ||
+        !tim || !y || !H_saved || !ws)
+        return MOE_ERR_INVALID_ARG;
+    for (const void* p : std::initializer_list<const void*>{x, W1, W2, y, H_saved, ws})
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (gated(s) && !aligned16(W3)) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < layout_fwd_slot(s, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int* err = status_ptr();
+    if (!err) return MOE_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SlotWs w;
+    layout_fwd_slot(s, ws, &w);
+    const int tc = moe_chunk_tokens(s);
+    MOE_TRY(launch_chunk_segments(s, tc, 0, eti, offsets, w.segs, err, st));
+
+    GemmProblem g1{};
+    g1.kind = G1_UP;
+    g1.s = s;
+    g1.segs = w.segs;
+    g1.eti = eti;
+    g1.a_src = x;
+    g1.b_src0 = W1;
+    g1.b_src1 = W3;
+    g1.out0 = H_saved;
+    g1.out1 = w.Aact;
+    g1.err = err;
+    MOE_TRY(launch_gemm(g1, st));
+
+    // Slot k's rows grouped by expert, ascending token: the dispatch of ids[:, k].
+    MOE_TRY(launch_slot_dispatch(s, topk_ids, w.eti_k, w.off_k, w.tim_k, w.hist, err, st));
+    for (int k = 0; k < s.K; ++k) {
+        Seg* sk = w.segs + static_cast<size_t>(k + 1) * s.E;
+        const int32_t* eti_k = w.eti_k + static_cast<size_t>(k) * s.T;
+        MOE_TRY(launch_chunk_segments(s, tc, 0, eti_k, w.off_k + static_cast<size_t>(k) * (s.E + 1),
+                                      sk, err, st));
+        GemmProblem g2{};
+        g2.kind = G2_SLOT;
+        g2.s = s;
+        g2.segs = sk;
+        g2.eti = eti_k;
+        g2.a_src = w.Aact;
+        g2.b_src0 = W2;
+        g2.out0 = w.acc;
+        g2.out1 = y;
+        g2.wrow = topk_w;
+        g2.tim = tim;
+        g2.slot = k;
+        g2.err = err;
+        MOE_TRY(launch_gemm(g2, st));
     }
     return MOE_OK;
 }

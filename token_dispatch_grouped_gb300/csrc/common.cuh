@@ -62,6 +62,12 @@ int dispatch_block_tokens();
 cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
                             int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
                             cudaStream_t st);
+// Per-slot lists for the slot-wise fused combine: for every slot k, the
+// dispatch of the column ids[:, k] (eti_k [K][T], offsets_k [K][E+1],
+// tim_k [K][T]); hist holds K * ceil(T/256) * E entries.
+cudaError_t launch_slot_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti_k,
+                                 int32_t* offsets_k, int32_t* tim_k, int32_t* hist, int* err,
+                                 cudaStream_t st);
 
 // misc.cu
 cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchunks,
@@ -87,7 +93,10 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
 enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5,
                 // Non-gated (SiLU/ReLU) variants of G1 and G3; chosen by launch_gemm
                 // from moe_shape.expert, callers pass G1_UP / G3_DH.
-                G1_UP_ACT = 6, G3_DH_ACT = 7 };
+                G1_UP_ACT = 6, G3_DH_ACT = 7,
+                // Down projection of one routing slot with the combine fused
+                // into its epilogue (slot-wise forward).
+                G2_SLOT = 8 };
 
 struct GemmProblem {
     GemmKind kind;
@@ -106,6 +115,11 @@ struct GemmProblem {
     float* dS_part;           // [h/BN][TK] (G3)
     int n_off = 0;            // G2/G6: first output column computed by this launch
     int n_cols = 0;           // G2/G6: output columns of this launch (= row stride of out0)
+    // G2_SLOT: eti = this slot's token list, a_src = A_act, b_src0 = W2, out0 = the fp32
+    // accumulator [T, d], out1 = y [T, d] bf16, wrow = topk_w [T, K], tim = the routing's
+    // token_index_map (A_act row of (t, k) = tim[t*K + k]).
+    const int32_t* tim = nullptr;
+    int slot = 0;
     int* err;
 };
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t st);

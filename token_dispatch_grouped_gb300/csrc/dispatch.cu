@@ -33,10 +33,15 @@ constexpr int kWarps = kBlockTokens / 32;
 constexpr int kMaxE = 256;
 constexpr int kScanThreads = 1024;
 
+// The kernels read ids[t * ld + k] for k < K: the whole routing (ld = K) or,
+// with gridDim.y = K' and K = 1, one column per blockIdx.y (the slot-wise
+// lists of the fused combine); blockIdx.y also selects that slot's output
+// arrays.
+//
 // Builds masks[w][e] (bit l set when lane l of warp w chose expert e) for the
 // block `blk`. Flags ids out of range or repeated within a token.
-__device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int T, int E, int K,
-                                            int blk, uint32_t (*masks)[kMaxE], int* err,
+__device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int ld, int T, int E,
+                                            int K, int blk, uint32_t (*masks)[kMaxE], int* err,
                                             int (&my_e)[8]) {
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -46,7 +51,7 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int
     const bool valid = t < T;
     bool bad = false;
     for (int k = 0; k < K; ++k) {
-        int e = valid ? ids[static_cast<size_t>(t) * K + k] : -1;
+        int e = valid ? ids[static_cast<size_t>(t) * ld + k] : -1;
         if (valid) {
             bool dup = false;
             for (int j = 0; j < k; ++j) dup |= (my_e[j] == e);
@@ -66,12 +71,14 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int
 }
 
 __global__ void __launch_bounds__(kBlockTokens)
-dispatch_hist_kernel(const int32_t* __restrict__ ids, int T, int E, int K, int32_t* __restrict__ hist,
-                     int* err) {
+dispatch_hist_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, int K,
+                     int32_t* __restrict__ hist, int* err) {
     if (has_error(err)) return;
     __shared__ uint32_t masks[kWarps][kMaxE];
     int my_e[8];
-    build_masks(ids, T, E, K, blockIdx.x, masks, err, my_e);
+    ids += blockIdx.y;
+    hist += static_cast<size_t>(blockIdx.y) * gridDim.x * E;
+    build_masks(ids, ld, T, E, K, blockIdx.x, masks, err, my_e);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int c = 0;
 #pragma unroll
@@ -86,6 +93,8 @@ __global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int32_t* __restrict__ offsets,
                      int* err) {
     if (has_error(err)) return;
+    hist += static_cast<size_t>(blockIdx.x) * nblk * E;  // one CTA per slot view
+    offsets += static_cast<size_t>(blockIdx.x) * (E + 1);
     __shared__ int32_t part_sum[kScanThreads];
     __shared__ int32_t exp_tot[kMaxE];
     const int P = kScanThreads / E;  // parts per expert (E <= 256 -> P >= 4)
@@ -130,14 +139,20 @@ dispatch_scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int32_t* __res
 }
 
 __global__ void __launch_bounds__(kBlockTokens)
-dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
+dispatch_scatter_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, int K,
                         const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                         int32_t* __restrict__ eti, int32_t* __restrict__ tim, int* err) {
     if (has_error(err)) return;
     __shared__ uint32_t masks[kWarps][kMaxE];
     __shared__ int32_t wbase[kWarps][kMaxE];
     int my_e[8];
-    build_masks(ids, T, E, K, blockIdx.x, masks, err, my_e);
+    const size_t view = blockIdx.y;
+    ids += view;
+    base += view * gridDim.x * E;
+    offsets += view * (E + 1);
+    eti += view * T * K;
+    tim += view * T * K;
+    build_masks(ids, ld, T, E, K, blockIdx.x, masks, err, my_e);
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int32_t run = offsets[e] + base[static_cast<size_t>(blockIdx.x) * E + e];
 #pragma unroll
@@ -165,28 +180,45 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int K,
 
 int dispatch_block_tokens() { return kBlockTokens; }
 
-cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
-                            int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
-                            cudaStream_t st) {
-    const int nblk = (s.T + kBlockTokens - 1) / kBlockTokens;
+namespace {
+cudaError_t launch_views(int T, int E, int K, int ld, int views, const int32_t* ids,
+                         int32_t* eti, int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
+                         cudaStream_t st, const char* n1, const char* n2, const char* n3) {
+    const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
     {
-        LaunchScope ls("dispatch_hist", st);
-        dispatch_hist_kernel<<<nblk, kBlockTokens, 0, st>>>(ids, s.T, s.E, s.K, hist, err);
+        LaunchScope ls(n1, st);
+        dispatch_hist_kernel<<<dim3(nblk, views), kBlockTokens, 0, st>>>(ids, ld, T, E, K, hist,
+                                                                         err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     {
-        LaunchScope ls("dispatch_scan", st);
-        dispatch_scan_kernel<<<1, kScanThreads, 0, st>>>(hist, nblk, s.E, offsets, err);
+        LaunchScope ls(n2, st);
+        dispatch_scan_kernel<<<views, kScanThreads, 0, st>>>(hist, nblk, E, offsets, err);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     {
-        LaunchScope ls("dispatch_scatter", st);
-        dispatch_scatter_kernel<<<nblk, kBlockTokens, 0, st>>>(ids, s.T, s.E, s.K, hist, offsets,
-                                                               eti, tim, err);
+        LaunchScope ls(n3, st);
+        dispatch_scatter_kernel<<<dim3(nblk, views), kBlockTokens, 0, st>>>(
+            ids, ld, T, E, K, hist, offsets, eti, tim, err);
     }
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
+                            int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
+                            cudaStream_t st) {
+    return launch_views(s.T, s.E, s.K, s.K, 1, ids, eti, offsets, tim, hist, err, st,
+                        "dispatch_hist", "dispatch_scan", "dispatch_scatter");
+}
+
+cudaError_t launch_slot_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti_k,
+                                 int32_t* offsets_k, int32_t* tim_k, int32_t* hist, int* err,
+                                 cudaStream_t st) {
+    return launch_views(s.T, s.E, 1, s.K, s.K, ids, eti_k, offsets_k, tim_k, hist, err, st,
+                        "slot_hist", "slot_scan", "slot_scatter");
 }
 
 }  // namespace moe

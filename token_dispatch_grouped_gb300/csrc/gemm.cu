@@ -47,6 +47,11 @@
 //       (MoEBlaze 5.2: both branches aggregated in place, no per-branch buffer);
 //       the epilogue adds the router term dz_r W_g[e] of each row.
 //       Non-gated: K = h, da W1_e.
+//   G2_SLOT  (slot-wise forward) [T_e^k, h] x [h, d] for the rows (t, k) of one
+//       routing slot k, A rows gathered through tim[t*K + k]; the epilogue adds
+//       w_{t,k} Y into an fp32 accumulator row of token t (each token once per
+//       slot, so no two CTAs touch one row), and the last slot writes bf16 y.
+//       (SonicMoE 3.4.1: O_t = sum_k s_{t,k} Y_{t,k}, in slot order)
 // The saved pre-activation H and its gradient dH are [TK, hs] with hs = 2h
 // (a | b) for SwiGLU and hs = h (a) for non-gated experts.
 // Rows past an expert's end are zero-filled on the gathered operand, so
@@ -80,6 +85,7 @@ template <> struct Tr<G4_DW2>  { static constexpr bool VK = true;  static conste
 template <> struct Tr<G5_DW13> { static constexpr bool VK = true;  static constexpr int A_MN = 1, B_MN = 1, A_G = 1; };
 template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static constexpr int A_MN = 0, B_MN = 1, A_G = 0; };
 template <> struct Tr<G1_UP_ACT> : Tr<G1_UP> {};
+template <> struct Tr<G2_SLOT> : Tr<G1_UP> {};  // gathered K-major A, K-major B
 template <> struct Tr<G3_DH_ACT> : Tr<G3_DH> {};
 
 template <int BN, int CTAS, int EPI_BOXES = 2>
@@ -114,6 +120,9 @@ struct Params {
     int M;         // VK: rows of the output per expert
     int n_tiles;   // tiles along N
     int n_half;    // G5: N tiles per half (dW1 | dW3); the last tile of a half may be partial
+    int slot;      // G2_SLOT: routing slot k of this launch (of K = nslot)
+    int nslot;
+    const int32_t* tim;  // G2_SLOT: token_index_map
     int n_off;     // G2/G6: first output column of this launch (column chunk)
     int ldo;       // G2/G6: row stride of the output chunk buffer (elements)
     const Seg* segs;
@@ -523,7 +532,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                             }
                         }
                     }
-                } else if constexpr (KIND == G2_DOWN) {
+                } else if constexpr (KIND == G2_DOWN || KIND == G2_SLOT) {
                     if (lane == 0) load(b_dst, &mapB0, k0, t.e * p.d + p.n_off + ncol);
                 } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
                     if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
@@ -701,6 +710,48 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         }
                         box_put_row(stg, lane, v);
                         box_store_rows(stg, lane, out + j, p.ldo, nvalid);
+                    }
+                }
+            } else if constexpr (KIND == G2_SLOT) {
+                // Row r of this slot's list is token tok; y_tok accumulates
+                // w_{tok,k} Y in fp32 in slot order, the last slot stores bf16.
+                const int r = rbase + row_in_tile;
+                const bool valid = r < t.hi;
+                const int tok = valid ? p.eti[r] : 0;
+                const float w = valid ? p.wrow[static_cast<size_t>(tok) * p.nslot + p.slot] : 0.f;
+                const bool first = p.slot == 0, last = p.slot == p.nslot - 1;
+                float* arow = static_cast<float*>(p.out0) + static_cast<size_t>(tok) * p.d +
+                              t.n_blk * BN;
+                __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out1) +
+                                      static_cast<size_t>(tok) * p.d + t.n_blk * BN;
+#pragma unroll 1
+                for (int j = 0; j < BN; j += 32) {
+                    tmem_ld32f(tacc + j, v);
+                    if (valid) {
+                        float a[32];
+                        if (first) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) a[i] = 0.f;
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 q4 = *reinterpret_cast<const float4*>(arow + j + i);
+                                a[i] = q4.x;
+                                a[i + 1] = q4.y;
+                                a[i + 2] = q4.z;
+                                a[i + 3] = q4.w;
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = fmaf(w, v[i], a[i]);
+                        if (last) {
+                            store32_bf16(yrow + j, a);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(arow + j + i) =
+                                    make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+                        }
                     }
                 }
             } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
@@ -881,7 +932,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             // gfull barrier, which the relay warp forwards.
             const int g = threadIdx.x - 192;  // 0..127
             const int col16 = g & 7;
-            const size_t rowbytes = static_cast<size_t>(p.d) * 2;
+            // Gathered rows: x or dy [T, d]; for G2_SLOT the SwiGLU output [TK, h].
+            const size_t rowbytes = static_cast<size_t>(KIND == G2_SLOT ? p.h : p.d) * 2;
             const char* src0 = reinterpret_cast<const char*>(p.gsrc);
             auto done_bar = [&](int s) { return leader ? full_bar(s) : gfull_bar(s); };
             int stage = 0;
@@ -897,7 +949,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int r = tt.lo + tt.m_blk * BMC + rank * BM + rb + 16 * j;
-                        dst[j] = r < tt.hi ? p.eti[r] : -1;
+                        if constexpr (KIND == G2_SLOT)
+                            dst[j] = r < tt.hi ? p.tim[static_cast<size_t>(p.eti[r]) * p.nslot + p.slot]
+                                               : -1;
+                        else
+                            dst[j] = r < tt.hi ? p.eti[r] : -1;
                     }
                 };
                 int idx[8], nidx[8];
@@ -1143,7 +1199,9 @@ int choose_ctas(GemmKind kind, const moe_shape& s) {
     if (force != nullptr && (force[0] == '1' || force[0] == '2'))
         return (force[0] == '2' && ok2) ? 2 : 1;
     if (vk) return ok2 ? 2 : 1;
-    const long long rows_per_expert = static_cast<long long>(s.T) * s.K / s.E;
+    // A slot-wise down projection covers one slot: T rows over the experts.
+    const long long rows_per_expert =
+        static_cast<long long>(s.T) * (kind == G2_SLOT ? 1 : s.K) / s.E;
     return rows_per_expert >= 384 ? 2 : 1;
 }
 
@@ -1153,6 +1211,7 @@ int gemm_bn(GemmKind kind, const moe_shape& s) {
     switch (kind) {
         case G1_UP: return 256;  // 128 gate + 128 up columns
         case G2_DOWN:
+        case G2_SLOT:
         case G6_DX: return s.d % 256 == 0 ? 256 : 128;
         case G3_DH:
         case G4_DW2:
@@ -1180,6 +1239,9 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     prm.h = s.h;
     prm.E = s.E;
     prm.act = s.expert;
+    prm.slot = g.slot;
+    prm.nslot = s.K;
+    prm.tim = g.tim;
     prm.segs = g.segs;
     prm.eti = g.eti;
     prm.out0 = g.out0;
@@ -1213,6 +1275,14 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             prm.ldo = g.n_cols;
             prm.n_tiles = g.n_cols / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
+            break;
+        case G2_SLOT:  // A = SwiGLU output rows gathered by slot; B = W2 [E*d, h], K-major
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, bnl);
+            mp.a = mp.b1 = mp.o = mp.b0;
+            prm.Kdim = s.h;
+            prm.n_tiles = s.d / BN;
+            max_tiles = (s.T / bmc + s.E) * prm.n_tiles;
             break;
         case G3_DH:  // A = dy gathered; B = W2 [E*d, h] read MN-major
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
@@ -1262,6 +1332,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             return gated ? launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu")
                          : launch_ctas<G1_UP_ACT>(ctas, BN, mp, prm, max_tiles, st, "g1_up_act");
         case G2_DOWN: return launch_ctas<G2_DOWN>(ctas, BN, mp, prm, max_tiles, st, "g2_down");
+        case G2_SLOT: return launch_ctas<G2_SLOT>(ctas, BN, mp, prm, max_tiles, st, "g2_slot");
         case G3_DH:
             return gated ? launch_ctas<G3_DH>(ctas, BN, mp, prm, max_tiles, st, "g3_dh")
                          : launch_ctas<G3_DH_ACT>(ctas, BN, mp, prm, max_tiles, st, "g3_dh_act");

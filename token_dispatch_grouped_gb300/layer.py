@@ -39,7 +39,7 @@ class MoELayer:
         self.gated = expert == "swiglu"
         self.hs = 2 * h if self.gated else h  # width of the saved pre-activation
         self.device = torch.device(device)
-        sizes = [B.moe_workspace_size(self.s, w) for w in range(4)]
+        sizes = [B.moe_workspace_size(self.s, w) for w in range(5)]
         if any(z == 0 for z in sizes[1:]):
             raise B.MoeError(B.MOE_ERR_UNSUPPORTED_SHAPE, "MoELayer")
         self.ws_bytes = max(sizes)
@@ -62,12 +62,15 @@ class MoELayer:
         B.moe_build_dispatch(self.s, ids, eti, off, tim, self.ws)
         return Dispatch(eti, off, tim)
 
-    def forward(self, x, W1, W3, W2, r: Routing, dp: Dispatch, y=None, H=None):
+    def forward(self, x, W1, W3, W2, r: Routing, dp: Dispatch, y=None, H=None,
+                combine: str = "chunked"):
+        """combine: "chunked" (moe_forward) or "slotwise" (moe_forward_slotwise)."""
         if y is None:
             y = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
         if H is None:
             H = torch.empty(self.T * self.K, self.hs, dtype=torch.bfloat16, device=self.device)
-        B.moe_forward(self.s, x, W1, W3, W2, r.ids, r.w, dp.eti, dp.offsets, dp.tim, y, H, self.ws)
+        fwd = B.moe_forward_slotwise if combine == "slotwise" else B.moe_forward
+        fwd(self.s, x, W1, W3, W2, r.ids, r.w, dp.eti, dp.offsets, dp.tim, y, H, self.ws)
         return y, H
 
     def backward(self, dy, x, Wg, W1, W3, W2, r: Routing, dp: Dispatch, H, grads=None):
