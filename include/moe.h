@@ -202,6 +202,71 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg,
                  void* dx, float* dWg, void* dW1, void* dW3, void* dW2, float* dS,
                  void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Token rounding and routings given as rows ----------------------------
+ *
+ * Token rounding (TR) replaces each expert's token-choice count f_e by the
+ * nearest multiple of m_tile (a tie rounds down; at most T), so that no
+ * grouped-GEMM tile is padded. Rounding down drops the expert's lowest-scoring
+ * token-choice tokens; rounding up adds the best other tokens. The score of
+ * (t, e) is the router probability (softmax of z_t over all experts); ties rank
+ * the lower token first. [SonicMoE 3.4.4, Algorithm 4, NR-f subroutine]
+ * A token can end with fewer or more than K experts; its gate weights are the
+ * softmax of z_t over its final experts (renormalised over the chosen experts
+ * as for top-K), and a token without experts gets y = 0 and no gradient.
+ *
+ * The result is a routing given as rows, consumed by moe_forward_rows and
+ * moe_backward_rows:
+ *   expert_token_indices [rows_cap] (first offsets[E] used; each expert's
+ *     tokens ascending), expert_token_offsets [E+1],
+ *   w_row [rows_cap] fp32: gate weight of each row,
+ *   tok_off [T+1]: token t's entries are tok_off[t] .. tok_off[t+1] of
+ *   tok_exp [rows_cap] (its experts, ascending) and tok_rows [rows_cap] (the
+ *     row of each of those experts).
+ * rows_cap = moe_rows_capacity(s, m_tile) bounds the rows (T*K plus fewer than
+ * m_tile added tokens per expert, and at most T*E). */
+
+/* Row capacity for token rounding with tile m_tile (0 if unsupported). */
+size_t moe_rows_capacity(moe_shape s, int m_tile);
+
+/* Workspace bytes of moe_token_rounding (0 if unsupported). */
+size_t moe_token_rounding_workspace_size(moe_shape s, int m_tile);
+
+/* Token rounding of a token-choice routing. Inputs: logits [T,E] fp32 (from
+ * moe_route), topk_ids [T,K], and expert_token_indices / offsets of their
+ * dispatch (moe_build_dispatch). Outputs as described above. m_tile in
+ * [1, 4096]. Every output is a deterministic function of the inputs. */
+int moe_token_rounding(moe_shape s, int m_tile, const float* logits, const int32_t* topk_ids,
+                       const int32_t* tc_expert_token_indices,
+                       const int32_t* tc_expert_token_offsets,
+                       int32_t* expert_token_indices, int32_t* expert_token_offsets,
+                       float* w_row, int32_t* tok_off, int32_t* tok_exp, int32_t* tok_rows,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of moe_forward_rows (which = MOE_WS_FORWARD) and
+ * moe_backward_rows (MOE_WS_BACKWARD) for row capacity rows_cap. */
+size_t moe_workspace_size_rows(moe_shape s, int32_t rows_cap, int which);
+
+/* Forward on a routing given as rows (same computation as moe_forward; the
+ * K slots of a token become its tok_off range). H_saved is [rows_cap, hs].
+ * Down-projection passes split columns (d % 512 == 0) or run once over all
+ * rows. */
+int moe_forward_rows(moe_shape s, int32_t rows_cap, const void* x, const void* W1,
+                     const void* W3, const void* W2, const int32_t* expert_token_indices,
+                     const int32_t* expert_token_offsets, const float* w_row,
+                     const int32_t* tok_off, const int32_t* tok_exp, const int32_t* tok_rows,
+                     void* y, void* H_saved, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward on a routing given as rows. dS_row [rows_cap] fp32 = <dy_t, Y_r> per
+ * row; the router gradient is that of w_row = softmax of z_t over the token's
+ * rows: dz_r = w_r (dS_r - sum over the token's rows of w dS). */
+int moe_backward_rows(moe_shape s, int32_t rows_cap, const void* dy, const void* x,
+                      const float* Wg, const void* W1, const void* W3, const void* W2,
+                      const int32_t* expert_token_indices, const int32_t* expert_token_offsets,
+                      const float* w_row, const int32_t* tok_off, const int32_t* tok_exp,
+                      const int32_t* tok_rows, const void* H_saved, void* dx, float* dWg,
+                      void* dW1, void* dW3, void* dW2, float* dS_row, void* ws, size_t ws_bytes,
+                      void* stream);
+
 /* Waits for `stream`, then returns and clears the device status word of the
  * current device (MOE_OK if no device-side error happened since the last
  * call). The only call that blocks the host. */

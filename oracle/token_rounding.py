@@ -33,15 +33,19 @@ import numpy as np
 from oracle.moe_oracle import _as64, act, act_grad, silu, silu_grad, softmax
 
 
-def token_rounding(z, K: int, m_tile: int = 128):
+def token_rounding(z, K: int, m_tile: int = 128, ids=None):
     """Token rounding of the logits z [T, E]. Returns a dict:
     final [T,E] bool (the rounded assignment), w [T,E] (gate weights, zero off
     the final set), tc [T,E] bool (the token-choice assignment), f [E]
-    (token-choice counts), n [E] (kept counts), up [E] bool (padded)."""
+    (token-choice counts), n [E] (kept counts), up [E] bool (padded), p [T,E]
+    (the scores). `ids` [T,K] gives the token-choice assignment instead of
+    taking the top-K of z (to compare on another implementation's routing)."""
     z = _as64(z)
     T, E = z.shape
     p = softmax(z)
-    ids = np.argsort(-p, axis=1, kind="stable")[:, :K]   # token choice, ties to lower id
+    if ids is None:
+        ids = np.argsort(-p, axis=1, kind="stable")[:, :K]   # token choice, ties to lower id
+    ids = np.asarray(ids, dtype=np.int64)
     tc = np.zeros((T, E), dtype=bool)
     tc[np.arange(T)[:, None], ids] = True
     f = tc.sum(axis=0).astype(np.int64)
@@ -60,7 +64,7 @@ def token_rounding(z, K: int, m_tile: int = 128):
         sel = final[t]
         if sel.any():
             w[t, sel] = softmax(z[t, sel])
-    return dict(final=final, w=w, tc=tc, f=f, n=n, up=up)
+    return dict(final=final, w=w, tc=tc, f=f, n=n, up=up, p=p)
 
 
 def rows_of(final):

@@ -69,6 +69,12 @@ def _load() -> ctypes.CDLL:
         "moe_forward": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_forward_slotwise": (I, [MoeShape, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
         "moe_backward": (I, [MoeShape] + [P] * 19 + [S, P]),
+        "moe_rows_capacity": (S, [MoeShape, I]),
+        "moe_token_rounding_workspace_size": (S, [MoeShape, I]),
+        "moe_token_rounding": (I, [MoeShape, I] + [P] * 11 + [S, P]),
+        "moe_workspace_size_rows": (S, [MoeShape, ctypes.c_int32, I]),
+        "moe_forward_rows": (I, [MoeShape, ctypes.c_int32] + [P] * 13 + [S, P]),
+        "moe_backward_rows": (I, [MoeShape, ctypes.c_int32] + [P] * 20 + [S, P]),
         "moe_get_error": (I, [P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_last_cuda_error": (ctypes.c_char_p, []),
@@ -171,6 +177,57 @@ def moe_forward_slotwise(s, x, W1, W3, W2, topk_ids, topk_w, eti, offsets, tim, 
                                   _stream(stream))
     if check:
         _check(rc, "moe_forward_slotwise")
+    return rc
+
+
+def moe_rows_capacity(s: MoeShape, m_tile: int) -> int:
+    return int(LIB.moe_rows_capacity(s, m_tile))
+
+
+def moe_token_rounding_workspace_size(s: MoeShape, m_tile: int) -> int:
+    return int(LIB.moe_token_rounding_workspace_size(s, m_tile))
+
+
+def moe_workspace_size_rows(s: MoeShape, rows_cap: int, which: int) -> int:
+    return int(LIB.moe_workspace_size_rows(s, rows_cap, which))
+
+
+def _nbytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def moe_token_rounding(s, m_tile, logits, topk_ids, tc_eti, tc_offsets, eti, offsets, w_row,
+                       tok_off, tok_exp, tok_rows, ws, stream=None, check=True):
+    rc = LIB.moe_token_rounding(s, m_tile, _ptr(logits), _ptr(topk_ids), _ptr(tc_eti),
+                                _ptr(tc_offsets), _ptr(eti), _ptr(offsets), _ptr(w_row),
+                                _ptr(tok_off), _ptr(tok_exp), _ptr(tok_rows), _ptr(ws),
+                                _nbytes(ws), _stream(stream))
+    if check:
+        _check(rc, "moe_token_rounding")
+    return rc
+
+
+def moe_forward_rows(s, rows_cap, x, W1, W3, W2, eti, offsets, w_row, tok_off, tok_exp, tok_rows,
+                     y, H_saved, ws, stream=None, check=True):
+    rc = LIB.moe_forward_rows(s, rows_cap, _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(eti),
+                              _ptr(offsets), _ptr(w_row), _ptr(tok_off), _ptr(tok_exp),
+                              _ptr(tok_rows), _ptr(y), _ptr(H_saved), _ptr(ws), _nbytes(ws),
+                              _stream(stream))
+    if check:
+        _check(rc, "moe_forward_rows")
+    return rc
+
+
+def moe_backward_rows(s, rows_cap, dy, x, Wg, W1, W3, W2, eti, offsets, w_row, tok_off, tok_exp,
+                      tok_rows, H_saved, dx, dWg, dW1, dW3, dW2, dS_row, ws, stream=None,
+                      check=True):
+    rc = LIB.moe_backward_rows(s, rows_cap, _ptr(dy), _ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3),
+                               _ptr(W2), _ptr(eti), _ptr(offsets), _ptr(w_row), _ptr(tok_off),
+                               _ptr(tok_exp), _ptr(tok_rows), _ptr(H_saved), _ptr(dx),
+                               _ptr(dWg), _ptr(dW1), _ptr(dW3), _ptr(dW2), _ptr(dS_row),
+                               _ptr(ws), _nbytes(ws), _stream(stream))
+    if check:
+        _check(rc, "moe_backward_rows")
     return rc
 
 

@@ -98,6 +98,8 @@ int check_shape(const moe_shape& s) {
 
 bool gated(const moe_shape& s) { return s.expert == MOE_EXPERT_SWIGLU; }
 
+size_t tk_of(const moe_shape& s) { return static_cast<size_t>(s.T) * s.K; }
+
 // Width of the saved pre-activation H and of its gradient dH.
 size_t hs_of(const moe_shape& s) { return gated(s) ? 2 * static_cast<size_t>(s.h) : s.h; }
 
@@ -115,9 +117,20 @@ struct Plan {
     int dc;        // columns per column chunk
 };
 
-Plan make_plan(const moe_shape& s, double weight_bytes, double act_bytes) {
+// Row mode (a routing given as rows, e.g. after token rounding): a token chunk
+// may hold any number of rows, so passes split columns only (d % 512 == 0) or
+// there is a single pass over all rows.
+Plan make_plan(const moe_shape& s, double weight_bytes, double act_bytes, bool row_mode) {
     Plan p{1, false, s.T, s.d};
     if (s.T < 1024) return p;
+    if (row_mode) {
+        if (s.d % (4 * 128) == 0) {
+            p.n = 4;
+            p.by_cols = true;
+            p.dc = s.d / 4;
+        }
+        return p;
+    }
     p.n = 4;
     p.tc = moe_chunk_tokens(s);
     p.n = nchunks_of(s, p.tc);
@@ -131,20 +144,19 @@ Plan make_plan(const moe_shape& s, double weight_bytes, double act_bytes) {
     return p;
 }
 
-Plan plan_down(const moe_shape& s) {
-    const double TK = static_cast<double>(s.T) * s.K;
-    return make_plan(s, 2.0 * s.E * s.d * s.h, 2.0 * TK * s.h);
+// rows: row capacity of the routing (T*K for a top-K routing).
+Plan plan_down(const moe_shape& s, size_t rows, bool row_mode) {
+    return make_plan(s, 2.0 * s.E * s.d * s.h, 2.0 * static_cast<double>(rows) * s.h, row_mode);
 }
 
-Plan plan_dx(const moe_shape& s) {
-    const double TK = static_cast<double>(s.T) * s.K;
+Plan plan_dx(const moe_shape& s, size_t rows, bool row_mode) {
     const double hs = static_cast<double>(hs_of(s));
-    return make_plan(s, 2.0 * s.E * s.d * hs, 2.0 * TK * hs);
+    return make_plan(s, 2.0 * s.E * s.d * hs, 2.0 * static_cast<double>(rows) * hs, row_mode);
 }
 
-size_t chunk_buffer_elems(const moe_shape& s, const Plan& p) {
-    const size_t TK = static_cast<size_t>(s.T) * s.K;
-    return p.by_cols ? TK * p.dc : static_cast<size_t>(p.tc) * s.K * s.d;
+size_t chunk_buffer_elems(const moe_shape& s, const Plan& p, size_t rows, bool row_mode) {
+    if (p.by_cols) return rows * p.dc;
+    return row_mode ? rows * s.d : static_cast<size_t>(p.tc) * s.K * s.d;
 }
 
 struct FwdWs {
@@ -164,21 +176,21 @@ struct BwdWs {
     float* dwg_part;
 };
 
-size_t layout_fwd(const moe_shape& s, void* ws, FwdWs* o) {
+size_t layout_fwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, FwdWs* o) {
     const int tc = moe_chunk_tokens(s);
     const int nc = nchunks_of(s, tc);
-    const size_t TK = static_cast<size_t>(s.T) * s.K;
     Carve c;
     c.base = static_cast<char*>(ws);
     FwdWs w;
     w.segs = c.take<Seg>(static_cast<size_t>(nc + 1) * s.E);
-    w.Aact = c.take<__nv_bfloat16>(TK * s.h);
-    w.Yc = c.take<__nv_bfloat16>(chunk_buffer_elems(s, plan_down(s)));
+    w.Aact = c.take<__nv_bfloat16>(rows * s.h);
+    w.Yc = c.take<__nv_bfloat16>(
+        chunk_buffer_elems(s, plan_down(s, rows, row_mode), rows, row_mode));
     if (o) *o = w;
     return align_up(c.off, 256);
 }
 
-size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
+size_t layout_bwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, BwdWs* o) {
     const int tc = moe_chunk_tokens(s);
     const int nc = nchunks_of(s, tc);
     const size_t TK = static_cast<size_t>(s.T) * s.K;
@@ -188,13 +200,14 @@ size_t layout_bwd(const moe_shape& s, void* ws, BwdWs* o) {
     c.base = static_cast<char*>(ws);
     BwdWs w;
     w.segs = c.take<Seg>(static_cast<size_t>(nc + 1) * s.E);
-    w.wrow = c.take<float>(TK);
-    w.dS_part = c.take<float>(TK * nparts);
+    w.wrow = c.take<float>(rows);
+    w.dS_part = c.take<float>(rows * nparts);
     w.dz = c.take<float>(TK);
-    w.dz_row = c.take<float>(TK);
-    w.Ap = c.take<__nv_bfloat16>(TK * s.h);
-    w.dH = c.take<__nv_bfloat16>(TK * hs_of(s));
-    w.dXc = c.take<__nv_bfloat16>(chunk_buffer_elems(s, plan_dx(s)));
+    w.dz_row = c.take<float>(rows);
+    w.Ap = c.take<__nv_bfloat16>(rows * s.h);
+    w.dH = c.take<__nv_bfloat16>(rows * hs_of(s));
+    w.dXc = c.take<__nv_bfloat16>(
+        chunk_buffer_elems(s, plan_dx(s, rows, row_mode), rows, row_mode));
     w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
     if (o) *o = w;
     return align_up(c.off, 256);
@@ -223,6 +236,42 @@ size_t layout_fwd_slot(const moe_shape& s, void* ws, SlotWs* o) {
     w.tim_k = c.take<int32_t>(TK);
     w.hist = c.take<int32_t>(static_cast<size_t>(s.K) * nblk * s.E);
     w.acc = s.K > 1 ? c.take<float>(static_cast<size_t>(s.T) * s.d) : nullptr;
+    if (o) *o = w;
+    return align_up(c.off, 256);
+}
+
+// The routing a forward or backward runs on: top-K slots (ids, topk_w, tim;
+// rows = T*K) or rows with a per-token row list (tok_off, tok_exp, tok_rows,
+// w_row; rows = the row capacity).
+struct RouteView {
+    size_t rows;
+    const int32_t* eti;
+    const int32_t* offsets;
+    const int32_t* ids = nullptr;
+    const float* topk_w = nullptr;
+    const int32_t* tim = nullptr;
+    const int32_t* tok_off = nullptr;
+    const int32_t* tok_exp = nullptr;
+    const int32_t* tok_rows = nullptr;
+    const float* w_row = nullptr;
+    bool row_mode() const { return tok_off != nullptr; }
+};
+
+size_t rows_capacity(const moe_shape& s, int m_tile) {
+    const size_t a = tk_of(s) + static_cast<size_t>(s.E) * (m_tile - 1);
+    const size_t b = static_cast<size_t>(s.T) * s.E;
+    return std::min(a, b);
+}
+
+size_t layout_rounding(const moe_shape& s, int m_tile, void* ws, TrScratch* o) {
+    Carve c;
+    c.base = static_cast<char*>(ws);
+    TrScratch w;
+    w.lse = c.take<float>(s.T);
+    w.par = c.take<int4>(s.E);
+    w.thr = c.take<unsigned long long>(s.E);
+    w.n_t = c.take<int32_t>(s.T);
+    w.w_tok = c.take<float>(rows_capacity(s, m_tile));
     if (o) *o = w;
     return align_up(c.off, 256);
 }
@@ -324,6 +373,197 @@ int num_sms() {
 
 }  // namespace moe
 
+// ---------------------------------------------------------------- call sequences
+namespace moe {
+namespace {
+
+int forward_impl(const moe_shape& s, const RouteView& rv, const void* x, const void* W1,
+                 const void* W3, const void* W2, void* y, void* H_saved, void* ws,
+                 size_t ws_bytes, void* stream) {
+    const bool rm = rv.row_mode();
+    if (!x || !W1 || (gated(s) && !W3) || !W2 || !rv.eti || !rv.offsets || !y || !H_saved || !ws)
+        return MOE_ERR_INVALID_ARG;
+    for (const void* p : std::initializer_list<const void*>{x, W1, W2, y, H_saved, ws})
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (gated(s) && !aligned16(W3)) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < layout_fwd(s, rv.rows, rm, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int* err = status_ptr();
+    if (!err) return MOE_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    FwdWs w;
+    layout_fwd(s, rv.rows, rm, ws, &w);
+    const int nc = nchunks_of(s, moe_chunk_tokens(s));
+    const Plan pl = plan_down(s, rv.rows, rm);
+    // Column-chunked passes, and a single pass, use the whole-row-space
+    // segments only.
+    const bool per_chunk = !pl.by_cols && pl.n > 1;
+    MOE_TRY(launch_chunk_segments(s, pl.tc, per_chunk ? pl.n : 0, rv.eti, rv.offsets,
+                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
+                                  err, st));
+    const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
+
+    GemmProblem g1{};
+    g1.kind = G1_UP;
+    g1.s = s;
+    g1.rows = static_cast<int>(rv.rows);
+    g1.segs = full;
+    g1.eti = rv.eti;
+    g1.a_src = x;
+    g1.b_src0 = W1;
+    g1.b_src1 = W3;
+    g1.out0 = H_saved;
+    g1.out1 = w.Aact;
+    g1.err = err;
+    MOE_TRY(launch_gemm(g1, st));
+
+    for (int c = 0; c < pl.n; ++c) {
+        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
+        GemmProblem g2{};
+        g2.kind = G2_DOWN;
+        g2.s = s;
+        g2.rows = static_cast<int>(rv.rows);
+        g2.segs = sc;
+        g2.eti = rv.eti;
+        g2.a_src = w.Aact;
+        g2.b_src0 = W2;
+        g2.out0 = w.Yc;
+        g2.n_off = pl.by_cols ? c * pl.dc : 0;
+        g2.n_cols = pl.by_cols ? pl.dc : s.d;
+        g2.err = err;
+        MOE_TRY(launch_gemm(g2, st));
+        const int t0 = pl.by_cols ? 0 : c * pl.tc;
+        const int t1 = pl.by_cols ? s.T : std::min(s.T, t0 + pl.tc);
+        if (rm)
+            MOE_TRY(launch_combine_rows(s, t0, t1, g2.n_off, g2.n_cols, rv.tok_off, rv.tok_exp,
+                                        rv.tok_rows, rv.w_row, sc, w.Yc,
+                                        static_cast<__nv_bfloat16*>(y), err, st, "combine"));
+        else
+            MOE_TRY(launch_combine(s, t0, t1, g2.n_off, g2.n_cols, rv.ids, rv.topk_w, rv.tim, sc,
+                                   w.Yc, static_cast<__nv_bfloat16*>(y), err, st));
+    }
+    return MOE_OK;
+}
+
+int backward_impl(const moe_shape& s, const RouteView& rv, const void* dy, const void* x,
+                  const float* Wg, const void* W1, const void* W3, const void* W2,
+                  const void* H_saved, void* dx, float* dWg, void* dW1, void* dW3, void* dW2,
+                  float* dS, void* ws, size_t ws_bytes, void* stream) {
+    const bool rm = rv.row_mode();
+    const bool gw = gated(s);  // W3 and dW3 exist
+    if (!dy || !x || !Wg || !W1 || (gw && !W3) || !W2 || !rv.eti || !rv.offsets || !H_saved ||
+        !dx || !dWg || !dW1 || (gw && !dW3) || !dW2 || !dS || !ws)
+        return MOE_ERR_INVALID_ARG;
+    for (const void* p : std::initializer_list<const void*>{
+             dy, x, static_cast<const void*>(Wg), W1, W2, H_saved, static_cast<const void*>(dx),
+             static_cast<const void*>(dWg), static_cast<const void*>(dW1),
+             static_cast<const void*>(dW2), static_cast<const void*>(ws)})
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (gw && (!aligned16(W3) || !aligned16(dW3))) return MOE_ERR_MISALIGNED;
+    if (ws_bytes < layout_bwd(s, rv.rows, rm, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int* err = status_ptr();
+    if (!err) return MOE_ERR_NO_DEVICE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    BwdWs w;
+    layout_bwd(s, rv.rows, rm, ws, &w);
+    const int nc = nchunks_of(s, moe_chunk_tokens(s));
+    const Plan pl = plan_dx(s, rv.rows, rm);
+    const bool per_chunk = !pl.by_cols && pl.n > 1;
+    MOE_TRY(launch_chunk_segments(s, pl.tc, per_chunk ? pl.n : 0, rv.eti, rv.offsets,
+                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
+                                  err, st));
+    const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
+    const float* wrow = rv.w_row;
+    if (!rm) {
+        MOE_TRY(launch_row_weights(s, rv.topk_w, rv.tim, w.wrow, err, st));
+        wrow = w.wrow;
+    }
+    const int rows = static_cast<int>(rv.rows);
+
+    GemmProblem g3{};
+    g3.kind = G3_DH;
+    g3.s = s;
+    g3.rows = rows;
+    g3.segs = full;
+    g3.eti = rv.eti;
+    g3.a_src = dy;
+    g3.b_src0 = W2;
+    g3.out0 = w.dH;
+    g3.out1 = w.Ap;
+    g3.aux0 = H_saved;
+    g3.wrow = wrow;
+    g3.dS_part = w.dS_part;
+    g3.err = err;
+    MOE_TRY(launch_gemm(g3, st));
+    const int bn3 = gemm_bn(G3_DH, s);
+    const int nparts = (s.h + bn3 - 1) / bn3;  // G3's N tiles, one dS partial each
+    if (rm)
+        MOE_TRY(launch_router_dz_rows(s, rows, nparts, w.dS_part, rv.tok_off, rv.tok_rows,
+                                      rv.w_row, dS, w.dz_row, err, st));
+    else
+        MOE_TRY(launch_router_dz(s, nparts, w.dS_part, rv.topk_w, rv.tim, dS, w.dz, w.dz_row, err,
+                                 st));
+
+    GemmProblem g4{};
+    g4.kind = G4_DW2;
+    g4.s = s;
+    g4.rows = rows;
+    g4.segs = full;
+    g4.eti = rv.eti;
+    g4.a_src = dy;
+    g4.b_src0 = w.Ap;
+    g4.out0 = dW2;
+    g4.err = err;
+    MOE_TRY(launch_gemm(g4, st));
+
+    GemmProblem g5{};
+    g5.kind = G5_DW13;
+    g5.s = s;
+    g5.rows = rows;
+    g5.segs = full;
+    g5.eti = rv.eti;
+    g5.a_src = x;
+    g5.b_src0 = w.dH;
+    g5.out0 = dW1;
+    g5.out1 = dW3;
+    g5.err = err;
+    MOE_TRY(launch_gemm(g5, st));
+
+    for (int c = 0; c < pl.n; ++c) {
+        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
+        GemmProblem g6{};
+        g6.kind = G6_DX;
+        g6.s = s;
+        g6.rows = rows;
+        g6.segs = sc;
+        g6.eti = rv.eti;
+        g6.a_src = w.dH;
+        g6.b_src0 = W1;
+        g6.b_src1 = W3;
+        g6.out0 = w.dXc;
+        g6.wrow = w.dz_row;  // router term dz_r W_g[e] added in the epilogue
+        g6.aux0 = Wg;
+        g6.n_off = pl.by_cols ? c * pl.dc : 0;
+        g6.n_cols = pl.by_cols ? pl.dc : s.d;
+        g6.err = err;
+        MOE_TRY(launch_gemm(g6, st));
+        const int t0 = pl.by_cols ? 0 : c * pl.tc;
+        const int t1 = pl.by_cols ? s.T : std::min(s.T, t0 + pl.tc);
+        if (rm)
+            MOE_TRY(launch_combine_rows(s, t0, t1, g6.n_off, g6.n_cols, rv.tok_off, rv.tok_exp,
+                                        rv.tok_rows, nullptr, sc, w.dXc,
+                                        static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
+        else
+            MOE_TRY(launch_combine(s, t0, t1, g6.n_off, g6.n_cols, rv.ids, nullptr, rv.tim, sc,
+                                   w.dXc, static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
+    }
+    MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), rv.eti, rv.offsets,
+                              w.dz_row, w.dwg_part, dWg, err, st));
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -338,8 +578,8 @@ size_t moe_workspace_size(moe_shape s, int which) {
     switch (which) {
         case MOE_WS_ROUTE: return 0;
         case MOE_WS_DISPATCH: return layout_dispatch(s, nullptr, nullptr);
-        case MOE_WS_FORWARD: return layout_fwd(s, nullptr, nullptr);
-        case MOE_WS_BACKWARD: return layout_bwd(s, nullptr, nullptr);
+        case MOE_WS_FORWARD: return layout_fwd(s, tk_of(s), false, nullptr, nullptr);
+        case MOE_WS_BACKWARD: return layout_bwd(s, tk_of(s), false, nullptr, nullptr);
         case MOE_WS_FORWARD_SLOTWISE: return layout_fwd_slot(s, nullptr, nullptr);
     }
     return 0;
@@ -382,61 +622,36 @@ int moe_forward(moe_shape s, const void* x, const void* W1, const void* W3, cons
                 size_t ws_bytes, void* stream) {
     int rc = check_shape(s);
     if (rc) return rc;
-    if (!x || !W1 || (gated(s) && !W3) || !W2 || !topk_ids || !topk_w || !eti || !offsets ||
-        !tim || !y || !H_saved || !ws)
+    if (!topk_ids || !topk_w || !tim) return MOE_ERR_INVALID_ARG;
+    RouteView rv;
+    rv.rows = tk_of(s);
+    rv.eti = eti;
+    rv.offsets = offsets;
+    rv.ids = topk_ids;
+    rv.topk_w = topk_w;
+    rv.tim = tim;
+    return forward_impl(s, rv, x, W1, W3, W2, y, H_saved, ws, ws_bytes, stream);
+}
+
+int moe_forward_rows(moe_shape s, int32_t rows_cap, const void* x, const void* W1,
+                     const void* W3, const void* W2, const int32_t* eti, const int32_t* offsets,
+                     const float* w_row, const int32_t* tok_off, const int32_t* tok_exp,
+                     const int32_t* tok_rows, void* y, void* H_saved, void* ws, size_t ws_bytes,
+                     void* stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (rows_cap < 1 || static_cast<size_t>(rows_cap) > static_cast<size_t>(s.T) * s.E)
         return MOE_ERR_INVALID_ARG;
-    for (const void* p : std::initializer_list<const void*>{x, W1, W2, y, H_saved, ws})
-        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
-    if (gated(s) && !aligned16(W3)) return MOE_ERR_MISALIGNED;
-    if (ws_bytes < layout_fwd(s, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    int* err = status_ptr();
-    if (!err) return MOE_ERR_NO_DEVICE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    FwdWs w;
-    layout_fwd(s, ws, &w);
-    const int tc = moe_chunk_tokens(s);
-    const int nc = nchunks_of(s, tc);
-    const Plan pl = plan_down(s);
-    // Column-chunked passes, and a single token chunk, use the whole-row-space
-    // segments only.
-    const bool per_chunk = !pl.by_cols && nc > 1;
-    MOE_TRY(launch_chunk_segments(s, tc, per_chunk ? nc : 0, eti, offsets,
-                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
-                                  err, st));
-    const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
-
-    GemmProblem g1{};
-    g1.kind = G1_UP;
-    g1.s = s;
-    g1.segs = full;
-    g1.eti = eti;
-    g1.a_src = x;
-    g1.b_src0 = W1;
-    g1.b_src1 = W3;
-    g1.out0 = H_saved;
-    g1.out1 = w.Aact;
-    g1.err = err;
-    MOE_TRY(launch_gemm(g1, st));
-
-    for (int c = 0; c < pl.n; ++c) {
-        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
-        GemmProblem g2{};
-        g2.kind = G2_DOWN;
-        g2.s = s;
-        g2.segs = sc;
-        g2.eti = eti;
-        g2.a_src = w.Aact;
-        g2.b_src0 = W2;
-        g2.out0 = w.Yc;
-        g2.n_off = pl.by_cols ? c * pl.dc : 0;
-        g2.n_cols = pl.by_cols ? pl.dc : s.d;
-        g2.err = err;
-        MOE_TRY(launch_gemm(g2, st));
-        const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
-        MOE_TRY(launch_combine(s, t0, t1, g2.n_off, g2.n_cols, topk_ids, topk_w, tim, sc, w.Yc,
-                               static_cast<__nv_bfloat16*>(y), err, st));
-    }
-    return MOE_OK;
+    if (!w_row || !tok_off || !tok_exp || !tok_rows) return MOE_ERR_INVALID_ARG;
+    RouteView rv;
+    rv.rows = static_cast<size_t>(rows_cap);
+    rv.eti = eti;
+    rv.offsets = offsets;
+    rv.tok_off = tok_off;
+    rv.tok_exp = tok_exp;
+    rv.tok_rows = tok_rows;
+    rv.w_row = w_row;
+    return forward_impl(s, rv, x, W1, W3, W2, y, H_saved, ws, ws_bytes, stream);
 }
 
 int moe_forward_slotwise(moe_shape s, const void* x, const void* W1, const void* W3,
@@ -505,98 +720,78 @@ int moe_backward(moe_shape s, const void* dy, const void* x, const float* Wg, co
                  float* dS, void* ws, size_t ws_bytes, void* stream) {
     int rc = check_shape(s);
     if (rc) return rc;
-    const bool gw = gated(s);  // W3 and dW3 exist
-    if (!dy || !x || !Wg || !W1 || (gw && !W3) || !W2 || !topk_ids || !topk_w || !eti ||
-        !offsets || !tim || !H_saved || !dx || !dWg || !dW1 || (gw && !dW3) || !dW2 || !dS || !ws)
+    if (!topk_ids || !topk_w || !tim) return MOE_ERR_INVALID_ARG;
+    RouteView rv;
+    rv.rows = tk_of(s);
+    rv.eti = eti;
+    rv.offsets = offsets;
+    rv.ids = topk_ids;
+    rv.topk_w = topk_w;
+    rv.tim = tim;
+    return backward_impl(s, rv, dy, x, Wg, W1, W3, W2, H_saved, dx, dWg, dW1, dW3, dW2, dS, ws,
+                         ws_bytes, stream);
+}
+
+int moe_backward_rows(moe_shape s, int32_t rows_cap, const void* dy, const void* x,
+                      const float* Wg, const void* W1, const void* W3, const void* W2,
+                      const int32_t* eti, const int32_t* offsets, const float* w_row,
+                      const int32_t* tok_off, const int32_t* tok_exp, const int32_t* tok_rows,
+                      const void* H_saved, void* dx, float* dWg, void* dW1, void* dW3, void* dW2,
+                      float* dS_row, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (rows_cap < 1 || static_cast<size_t>(rows_cap) > static_cast<size_t>(s.T) * s.E)
         return MOE_ERR_INVALID_ARG;
-    for (const void* p : std::initializer_list<const void*>{
-             dy, x, static_cast<const void*>(Wg), W1, W2, H_saved, static_cast<const void*>(dx),
-             static_cast<const void*>(dWg), static_cast<const void*>(dW1),
-             static_cast<const void*>(dW2), static_cast<const void*>(ws)})
-        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
-    if (gw && (!aligned16(W3) || !aligned16(dW3))) return MOE_ERR_MISALIGNED;
-    if (ws_bytes < layout_bwd(s, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (!w_row || !tok_off || !tok_exp || !tok_rows) return MOE_ERR_INVALID_ARG;
+    RouteView rv;
+    rv.rows = static_cast<size_t>(rows_cap);
+    rv.eti = eti;
+    rv.offsets = offsets;
+    rv.tok_off = tok_off;
+    rv.tok_exp = tok_exp;
+    rv.tok_rows = tok_rows;
+    rv.w_row = w_row;
+    return backward_impl(s, rv, dy, x, Wg, W1, W3, W2, H_saved, dx, dWg, dW1, dW3, dW2, dS_row,
+                         ws, ws_bytes, stream);
+}
+
+size_t moe_rows_capacity(moe_shape s, int m_tile) {
+    if (check_shape(s) != MOE_OK || m_tile < 1) return 0;
+    return rows_capacity(s, m_tile);
+}
+
+size_t moe_workspace_size_rows(moe_shape s, int32_t rows_cap, int which) {
+    if (check_shape(s) != MOE_OK || rows_cap < 1) return 0;
+    switch (which) {
+        case MOE_WS_FORWARD: return layout_fwd(s, static_cast<size_t>(rows_cap), true, nullptr, nullptr);
+        case MOE_WS_BACKWARD: return layout_bwd(s, static_cast<size_t>(rows_cap), true, nullptr, nullptr);
+    }
+    return 0;
+}
+
+size_t moe_token_rounding_workspace_size(moe_shape s, int m_tile) {
+    if (check_shape(s) != MOE_OK || m_tile < 1) return 0;
+    return layout_rounding(s, m_tile, nullptr, nullptr);
+}
+
+int moe_token_rounding(moe_shape s, int m_tile, const float* logits, const int32_t* topk_ids,
+                       const int32_t* tc_eti, const int32_t* tc_offsets, int32_t* eti,
+                       int32_t* offsets, float* w_row, int32_t* tok_off, int32_t* tok_exp,
+                       int32_t* tok_rows, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(s);
+    if (rc) return rc;
+    if (m_tile < 1 || m_tile > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!logits || !topk_ids || !tc_eti || !tc_offsets || !eti || !offsets || !w_row ||
+        !tok_off || !tok_exp || !tok_rows || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < layout_rounding(s, m_tile, nullptr, nullptr)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     int* err = status_ptr();
     if (!err) return MOE_ERR_NO_DEVICE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    BwdWs w;
-    layout_bwd(s, ws, &w);
-    const int tc = moe_chunk_tokens(s);
-    const int nc = nchunks_of(s, tc);
-    const Plan pl = plan_dx(s);
-    // Column-chunked passes, and a single token chunk, use the whole-row-space
-    // segments only.
-    const bool per_chunk = !pl.by_cols && nc > 1;
-    MOE_TRY(launch_chunk_segments(s, tc, per_chunk ? nc : 0, eti, offsets,
-                                  per_chunk ? w.segs : w.segs + static_cast<size_t>(nc) * s.E,
-                                  err, st));
-    const Seg* full = w.segs + static_cast<size_t>(nc) * s.E;
-    MOE_TRY(launch_row_weights(s, topk_w, tim, w.wrow, err, st));
-
-    GemmProblem g3{};
-    g3.kind = G3_DH;
-    g3.s = s;
-    g3.segs = full;
-    g3.eti = eti;
-    g3.a_src = dy;
-    g3.b_src0 = W2;
-    g3.out0 = w.dH;
-    g3.out1 = w.Ap;
-    g3.aux0 = H_saved;
-    g3.wrow = w.wrow;
-    g3.dS_part = w.dS_part;
-    g3.err = err;
-    MOE_TRY(launch_gemm(g3, st));
-    const int bn3 = gemm_bn(G3_DH, s);
-    const int nparts = (s.h + bn3 - 1) / bn3;  // G3's N tiles, one dS partial each
-    MOE_TRY(launch_router_dz(s, nparts, w.dS_part, topk_w, tim, dS, w.dz, w.dz_row, err, st));
-
-    GemmProblem g4{};
-    g4.kind = G4_DW2;
-    g4.s = s;
-    g4.segs = full;
-    g4.eti = eti;
-    g4.a_src = dy;
-    g4.b_src0 = w.Ap;
-    g4.out0 = dW2;
-    g4.err = err;
-    MOE_TRY(launch_gemm(g4, st));
-
-    GemmProblem g5{};
-    g5.kind = G5_DW13;
-    g5.s = s;
-    g5.segs = full;
-    g5.eti = eti;
-    g5.a_src = x;
-    g5.b_src0 = w.dH;
-    g5.out0 = dW1;
-    g5.out1 = dW3;
-    g5.err = err;
-    MOE_TRY(launch_gemm(g5, st));
-
-    for (int c = 0; c < pl.n; ++c) {
-        const Seg* sc = per_chunk ? w.segs + static_cast<size_t>(c) * s.E : full;
-        GemmProblem g6{};
-        g6.kind = G6_DX;
-        g6.s = s;
-        g6.segs = sc;
-        g6.eti = eti;
-        g6.a_src = w.dH;
-        g6.b_src0 = W1;
-        g6.b_src1 = W3;
-        g6.out0 = w.dXc;
-        g6.wrow = w.dz_row;  // router term dz_r W_g[e] added in the epilogue
-        g6.aux0 = Wg;
-        g6.n_off = pl.by_cols ? c * pl.dc : 0;
-        g6.n_cols = pl.by_cols ? pl.dc : s.d;
-        g6.err = err;
-        MOE_TRY(launch_gemm(g6, st));
-        const int t0 = pl.by_cols ? 0 : c * tc, t1 = pl.by_cols ? s.T : std::min(s.T, t0 + tc);
-        MOE_TRY(launch_combine(s, t0, t1, g6.n_off, g6.n_cols, topk_ids, nullptr, tim, sc, w.dXc,
-                               static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
-    }
-    MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), eti, offsets, w.dz_row,
-                              w.dwg_part, dWg, err, st));
+    TrScratch sc;
+    layout_rounding(s, m_tile, ws, &sc);
+    MOE_TRY(launch_token_rounding(s, m_tile, logits, topk_ids, tc_eti, tc_offsets, sc, eti,
+                                  offsets, w_row, tok_off, tok_exp, tok_rows, err,
+                                  static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 

@@ -69,6 +69,35 @@ cudaError_t launch_slot_dispatch(const moe_shape& s, const int32_t* ids, int32_t
                                  int32_t* offsets_k, int32_t* tim_k, int32_t* hist, int* err,
                                  cudaStream_t st);
 
+// Token rounding (rounding.cu). Scratch: lse [T], par [E], thr [E], n_t [T],
+// w_tok [rows_max].
+struct TrScratch {
+    float* lse;
+    int4* par;
+    unsigned long long* thr;
+    int32_t* n_t;
+    float* w_tok;
+};
+cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z,
+                                  const int32_t* ids, const int32_t* tc_eti,
+                                  const int32_t* tc_offsets, TrScratch sc, int32_t* eti_tr,
+                                  int32_t* offsets_tr, float* w_row, int32_t* tok_off,
+                                  int32_t* tok_exp, int32_t* tok_rows, int* err, cudaStream_t st);
+
+// Routing given as rows (misc.cu): token t's rows are tok_rows[tok_off[t] ..
+// tok_off[t+1]) of experts tok_exp[...]; row r has weight w_row[r] (nullptr: 1).
+cudaError_t launch_combine_rows(const moe_shape& s, int t0, int t1, int c0, int nc,
+                                const int32_t* tok_off, const int32_t* tok_exp,
+                                const int32_t* tok_rows, const float* w_row, const Seg* seg,
+                                const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err,
+                                cudaStream_t st, const char* name);
+// dS_row[r] = sum of the partials of row r; dz_row[r] = w_r (dS_r - sum over the
+// token's rows of w dS).
+cudaError_t launch_router_dz_rows(const moe_shape& s, int rows_cap, int nparts,
+                                  const float* dS_part, const int32_t* tok_off,
+                                  const int32_t* tok_rows, const float* w_row, float* dS_row,
+                                  float* dz_row, int* err, cudaStream_t st);
+
 // misc.cu
 cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchunks,
                                   const int32_t* eti, const int32_t* offsets, Seg* segs, int* err,
@@ -120,6 +149,7 @@ struct GemmProblem {
     // token_index_map (A_act row of (t, k) = tim[t*K + k]).
     const int32_t* tim = nullptr;
     int slot = 0;
+    int rows = 0;             // row capacity of the routed-row arrays (0: T*K)
     int* err;
 };
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t st);

@@ -1226,7 +1226,9 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     const int BN = (g.kind == G2_DOWN || g.kind == G6_DX) ? (g.n_cols % 256 == 0 ? 256 : 128)
                                                           : gemm_bn(g.kind, s);
     const int ctas = choose_ctas(g.kind, s);
-    const uint64_t TK = static_cast<uint64_t>(s.T) * s.K, d = s.d, h = s.h, E = s.E;
+    // Row capacity of the routed-row arrays (H, A, dH, A', the chunk buffer).
+    const uint64_t TK = g.rows > 0 ? static_cast<uint64_t>(g.rows) : static_cast<uint64_t>(s.T) * s.K;
+    const uint64_t d = s.d, h = s.h, E = s.E;
     const bool gated = s.expert == MOE_EXPERT_SWIGLU;
     const uint64_t hs = gated ? 2 * h : h;  // width of H and dH
     const uint32_t bnl = static_cast<uint32_t>(BN / ctas);  // B rows staged per CTA
@@ -1234,7 +1236,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     bool ok = true;
     Params prm{};
     prm.T = s.T;
-    prm.TK = s.T * s.K;
+    prm.TK = static_cast<int>(TK);
     prm.d = s.d;
     prm.h = s.h;
     prm.E = s.E;

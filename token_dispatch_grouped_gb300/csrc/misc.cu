@@ -219,6 +219,93 @@ __global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* 
     }
 }
 
+// Combine over a row-format routing: warp per token, the token's rows in CSR
+// order (ascending expert), summed in that order in fp32, one bf16 rounding;
+// the weight of routed row r is w_row[r] (nullptr: 1).
+// Chunk-buffer row of routed row r of expert e: seg[e].out + (r - seg[e].lo).
+__global__ void __launch_bounds__(kCombThreads)
+combine_rows_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ tok_off,
+                    const int32_t* __restrict__ tok_exp, const int32_t* __restrict__ tok_rows,
+                    const float* __restrict__ w_row, const Seg* __restrict__ seg,
+                    const __nv_bfloat16* __restrict__ Yc, __nv_bfloat16* __restrict__ y, int* err) {
+    if (has_error(err)) return;
+    const int lane = threadIdx.x & 31;
+    constexpr int U = 4;
+    for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
+         t += gridDim.x * kCombWarps) {
+        const int b0 = tok_off[t], b1 = tok_off[t + 1];
+        for (int cb = lane * 8; cb < nc; cb += 32 * 8 * U) {
+            float acc[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[u][j] = 0.f;
+            for (int g0 = b0; g0 < b1; g0 += 32) {  // groups of 32 rows of this token
+                size_t off = 0;
+                float wl = 0.f;
+                if (g0 + lane < b1) {
+                    const int i = g0 + lane;
+                    const Seg sg = seg[tok_exp[i]];
+                    const int r = tok_rows[i];
+                    off = static_cast<size_t>(sg.out + (r - sg.lo)) * nc;
+                    wl = w_row != nullptr ? w_row[r] : 1.f;
+                }
+                const int n = min(32, b1 - g0);
+                for (int q = 0; q < n; ++q) {
+                    const size_t ok = __shfl_sync(0xffffffffu, off, q);
+                    const float w = __shfl_sync(0xffffffffu, wl, q);
+                    uint4 v[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int c = cb + u * 256;
+                        v[u] = c < nc ? *reinterpret_cast<const uint4*>(Yc + ok + c)
+                                      : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        float f[8];
+                        bf16x8_to_f32(v[u], f);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[u][j] = fmaf(w, f[j], acc[u][j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + u * 256;
+                if (c < nc)
+                    *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) =
+                        f32_to_bf16x8(acc[u]);
+            }
+        }
+    }
+}
+
+// Router gradient over a row-format routing: thread per token.
+__global__ void router_dz_rows_kernel(int T, int rows_cap, int nparts,
+                                      const float* __restrict__ dS_part,
+                                      const int32_t* __restrict__ tok_off,
+                                      const int32_t* __restrict__ tok_rows,
+                                      const float* __restrict__ w_row, float* __restrict__ dS_row,
+                                      float* __restrict__ dz_row, int* err) {
+    if (has_error(err)) return;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const int b0 = tok_off[t], b1 = tok_off[t + 1];
+    float sbar = 0.f;
+    for (int i = b0; i < b1; ++i) {
+        const int r = tok_rows[i];
+        float acc = 0.f;
+        for (int p = 0; p < nparts; ++p) acc += dS_part[static_cast<size_t>(p) * rows_cap + r];
+        dS_row[r] = acc;
+        sbar = fmaf(w_row[r], acc, sbar);
+    }
+    for (int i = b0; i < b1; ++i) {
+        const int r = tok_rows[i];
+        dz_row[r] = w_row[r] * (dS_row[r] - sbar);
+    }
+}
+
 constexpr int kDwgParts = 32;      // row parts per expert
 constexpr int kDwgCols = 2048;     // columns per CTA (256 threads x 8)
 
@@ -337,6 +424,29 @@ cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_par
     LaunchScope ls("router_dz", st);
     router_dz_kernel<<<(s.T + 127) / 128, 128, 0, st>>>(s.T, s.K, s.T * s.K, nparts, dS_part,
                                                         topk_w, tim, dS, dz, dz_row, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_rows(const moe_shape& s, int t0, int t1, int c0, int nc,
+                                const int32_t* tok_off, const int32_t* tok_exp,
+                                const int32_t* tok_rows, const float* w_row, const Seg* seg,
+                                const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err,
+                                cudaStream_t st, const char* name) {
+    if (t1 <= t0) return cudaSuccess;
+    LaunchScope ls(name, st);
+    combine_rows_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(
+        t0, t1, c0, nc, s.d, tok_off, tok_exp, tok_rows, w_row, seg, Yc, y, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_dz_rows(const moe_shape& s, int rows_cap, int nparts,
+                                  const float* dS_part, const int32_t* tok_off,
+                                  const int32_t* tok_rows, const float* w_row, float* dS_row,
+                                  float* dz_row, int* err, cudaStream_t st) {
+    LaunchScope ls("router_dz", st);
+    router_dz_rows_kernel<<<(s.T + 255) / 256, 256, 0, st>>>(s.T, rows_cap, nparts, dS_part,
+                                                             tok_off, tok_rows, w_row, dS_row,
+                                                             dz_row, err);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,18 @@ class Dispatch:
     tim: torch.Tensor
 
 
+@dataclass
+class RowRouting:
+    """A routing given as rows (after token rounding)."""
+    rows_cap: int
+    eti: torch.Tensor
+    offsets: torch.Tensor
+    w_row: torch.Tensor
+    tok_off: torch.Tensor
+    tok_exp: torch.Tensor
+    tok_rows: torch.Tensor
+
+
 class MoELayer:
     """One dropless MoE layer of shape (T, d, E, K, h) on a CUDA device.
 
@@ -91,6 +103,50 @@ class MoELayer:
             dW2=torch.empty(E, d, h, dtype=torch.bfloat16, device=dev),
             dS=torch.empty(T, K, dtype=torch.float32, device=dev),
         )
+
+    # ---------------------------------------------------------- token rounding
+    def round_tokens(self, logits, r: Routing, dp: Dispatch, m_tile: int = 128) -> RowRouting:
+        """Token rounding (NR-f) of the token-choice routing r (needs its logits)."""
+        dev, T, E = self.device, self.T, self.E
+        cap = B.moe_rows_capacity(self.s, m_tile)
+        ws = torch.empty(max(B.moe_token_rounding_workspace_size(self.s, m_tile), 256),
+                         dtype=torch.uint8, device=dev)
+        rr = RowRouting(cap, torch.empty(cap, dtype=torch.int32, device=dev),
+                        torch.empty(E + 1, dtype=torch.int32, device=dev),
+                        torch.empty(cap, dtype=torch.float32, device=dev),
+                        torch.empty(T + 1, dtype=torch.int32, device=dev),
+                        torch.empty(cap, dtype=torch.int32, device=dev),
+                        torch.empty(cap, dtype=torch.int32, device=dev))
+        B.moe_token_rounding(self.s, m_tile, logits, r.ids, dp.eti, dp.offsets, rr.eti,
+                             rr.offsets, rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, ws)
+        return rr
+
+    def _rows_ws(self, rr: RowRouting) -> torch.Tensor:
+        need = max(B.moe_workspace_size_rows(self.s, rr.rows_cap, B.MOE_WS_FORWARD),
+                   B.moe_workspace_size_rows(self.s, rr.rows_cap, B.MOE_WS_BACKWARD), 256)
+        if getattr(self, "_rws", None) is None or self._rws.numel() < need:
+            self._rws = torch.empty(need, dtype=torch.uint8, device=self.device)
+        return self._rws
+
+    def forward_rows(self, x, W1, W3, W2, rr: RowRouting, y=None, H=None):
+        if y is None:
+            y = torch.empty(self.T, self.d, dtype=torch.bfloat16, device=self.device)
+        if H is None:
+            H = torch.empty(rr.rows_cap, self.hs, dtype=torch.bfloat16, device=self.device)
+        B.moe_forward_rows(self.s, rr.rows_cap, x, W1, W3, W2, rr.eti, rr.offsets, rr.w_row,
+                           rr.tok_off, rr.tok_exp, rr.tok_rows, y, H, self._rows_ws(rr))
+        return y, H
+
+    def backward_rows(self, dy, x, Wg, W1, W3, W2, rr: RowRouting, H, grads=None):
+        if grads is None:
+            grads = self.alloc_grads()
+        dS_row = torch.empty(rr.rows_cap, dtype=torch.float32, device=self.device)
+        B.moe_backward_rows(self.s, rr.rows_cap, dy, x, Wg, W1, W3, W2, rr.eti, rr.offsets,
+                            rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, H, grads["dx"],
+                            grads["dWg"], grads["dW1"], grads["dW3"], grads["dW2"], dS_row,
+                            self._rows_ws(rr))
+        grads["dS_row"] = dS_row
+        return grads
 
     def step(self, x, Wg, W1, W3, W2, dy, bias=None):
         """route -> dispatch -> forward -> backward; returns all outputs."""
