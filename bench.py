@@ -44,8 +44,10 @@ def gemm_flop_units(s) -> dict:
     return GEMM_FLOP_UNITS if s.gated else GEMM_FLOP_UNITS_NON_GATED
 
 
-def flops_per_step(s) -> float:
-    return sum(gemm_flop_units(s).values()) * s.T * s.K * s.d * s.h + 6.0 * s.T * s.d * s.E
+def flops_per_step(s, rows=None) -> float:
+    """Algorithmic FLOPs of one step; rows = routed rows (T*K for top-K routing)."""
+    rows = s.T * s.K if rows is None else rows
+    return sum(gemm_flop_units(s).values()) * rows * s.d * s.h + 6.0 * s.T * s.d * s.E
 
 
 def memory_kernel_bytes(s) -> dict:
@@ -315,6 +317,10 @@ def main():
     ap.add_argument("--combine", default="chunked", choices=["chunked", "slotwise"],
                     help="forward combine: chunked expert-output passes (moe_forward) or "
                          "fused into the down projection slot by slot (moe_forward_slotwise)")
+    ap.add_argument("--routing", default="tc", choices=["tc", "tr"],
+                    help="tc: top-K token choice; tr: token rounding of it (NR-f, --m-tile) "
+                         "and the layer on the rounded rows")
+    ap.add_argument("--m-tile", type=int, default=128)
     ap.add_argument("--dispatch-ablation", action="store_true",
                     help="time the dispatch build against a sort-based baseline and exit")
     args = ap.parse_args()
@@ -365,6 +371,37 @@ def main():
         B.moe_backward(L.s, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti,
                        dp.offsets, dp.tim, H, grads["dx"], grads["dWg"], grads["dW1"],
                        grads["dW3"], grads["dW2"], grads["dS"], L.ws)
+
+    rows_of_step = None
+    if args.routing == "tr":
+        # Token rounding of the top-K routing, then the layer on the rounded rows.
+        from token_dispatch_grouped_gb300.layer import RowRouting
+        m = args.m_tile
+        cap = B.moe_rows_capacity(L.s, m)
+        i32 = dict(dtype=torch.int32, device=dev)
+        rr = RowRouting(cap, torch.empty(cap, **i32), torch.empty(s.E + 1, **i32),
+                        torch.empty(cap, dtype=torch.float32, device=dev),
+                        torch.empty(s.T + 1, **i32), torch.empty(cap, **i32),
+                        torch.empty(cap, **i32))
+        tr_ws = torch.empty(max(B.moe_token_rounding_workspace_size(L.s, m), 256),
+                            dtype=torch.uint8, device=dev)
+        rows_ws = torch.empty(max(B.moe_workspace_size_rows(L.s, cap, B.MOE_WS_FORWARD),
+                                  B.moe_workspace_size_rows(L.s, cap, B.MOE_WS_BACKWARD)),
+                              dtype=torch.uint8, device=dev)
+        H = torch.empty(cap, L.hs, dtype=torch.bfloat16, device=dev)
+        dS_row = torch.empty(cap, dtype=torch.float32, device=dev)
+
+        def step(x, dy):  # noqa: F811
+            B.moe_route(L.s, x, dv["Wg"], bias, r.logits, r.ids, r.w, L.ws)
+            B.moe_build_dispatch(L.s, r.ids, dp.eti, dp.offsets, dp.tim, L.ws)
+            B.moe_token_rounding(L.s, m, r.logits, r.ids, dp.eti, dp.offsets, rr.eti, rr.offsets,
+                                 rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, tr_ws)
+            B.moe_forward_rows(L.s, cap, x, dv["W1"], dv["W3"], dv["W2"], rr.eti, rr.offsets,
+                               rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, y, H, rows_ws)
+            B.moe_backward_rows(L.s, cap, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], rr.eti,
+                                rr.offsets, rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, H,
+                                grads["dx"], grads["dWg"], grads["dW1"], grads["dW3"],
+                                grads["dW2"], dS_row, rows_ws)
 
     # ---- memory: activation bytes of one fwd+bwd beyond inputs/weights/grads/outputs
     torch.cuda.synchronize(dev)
@@ -423,7 +460,9 @@ def main():
     ms = max_over_ranks(ms, world)
     ms_step = ms / args.steps
     value = world * s.T * args.steps / (ms / 1e3)
-    tflops = flops_per_step(s) / (ms_step / 1e3) / 1e12
+    if args.routing == "tr":
+        rows_of_step = int(rr.offsets[-1].item())
+    tflops = flops_per_step(s, rows_of_step) / (ms_step / 1e3) / 1e12
 
     # ---- roofline of the dominant kernel (event-timed over the timed region)
     top = max(per_kernel.items(), key=lambda kv: kv[1][1])
@@ -431,7 +470,8 @@ def main():
     roof = None
     units = gemm_flop_units(s)
     if kname in units:
-        per_launch_flop = units[kname] * TK * s.d * s.h * args.steps / klaunches
+        per_launch_flop = (units[kname] * (rows_of_step or TK) * s.d * s.h * args.steps
+                           / klaunches)
         achieved = per_launch_flop / (kms / klaunches / 1e3) / 1e12
         peak = peaks["bf16_sus"]
         traffic = None
@@ -505,7 +545,11 @@ def main():
         line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps,
                     warmup=args.warmup, ms_per_step=ms_step, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="bf16", data="synthetic",
-                    config=dict(workload_config(s, name), combine=args.combine), tflops=tflops,
+                    config=dict(workload_config(s, name), combine=args.combine,
+                                routing=args.routing,
+                                **({"m_tile": args.m_tile, "rows": rows_of_step}
+                                   if args.routing == "tr" else {})),
+                    tflops=tflops,
                     frac_of_bf16_peak=tflops / peaks["bf16_sus"],
                     peak_note=f"{peaks['src']} bf16 sustained {peaks['bf16_sus']} TFLOP/s",
                     memory=memory, roofline=roof, kernels=kernels, memory_bound=memory_bound,

@@ -21,6 +21,8 @@
 //   R5  the same per-token pass writes tok_exp and the weights in CSR order.
 //   R6  one CTA per expert: compaction of its final tokens in ascending order
 //       into expert_token_indices, with each row's weight and its CSR slot.
+// The expert-side kernels (R2, R6) test token choice in a bitmap [E][T/32]
+// built from the token-choice dispatch.
 // Histogram bins in R2 are counted with shared-memory atomics (exact integer
 // counts); every output is order-independent and bit-reproducible.
 #include <cfloat>
@@ -46,6 +48,45 @@ __device__ __forceinline__ bool is_tc(const int32_t* ids, int t, int K, int e) {
     bool r = false;
     for (int k = 0; k < K; ++k) r |= ids[static_cast<size_t>(t) * K + k] == e;
     return r;
+}
+
+// Token-choice bitmap: bit t of row e (words of 32 tokens) is set when token t
+// chose expert e.
+__device__ __forceinline__ bool tc_bit(const uint32_t* __restrict__ bm, int words, int t, int e) {
+    return (bm[static_cast<size_t>(e) * words + (t >> 5)] >> (t & 31)) & 1u;
+}
+
+// Builds the bitmap from the token-choice dispatch: CTA per expert; the
+// expert's tokens are sorted, so the tokens of one word are adjacent; a
+// warp's lanes that share a word combine their bits by shuffles and the lowest
+// of them ORs them into the word (a word can span two warps' ranges; an
+// integer OR gives the same word in any order).
+__global__ void tr_bitmap_kernel(const int32_t* __restrict__ tc_eti,
+                                 const int32_t* __restrict__ tc_offsets, int words,
+                                 uint32_t* __restrict__ bm, int* err) {
+    if (has_error(err)) return;
+    const int e = blockIdx.x;
+    uint32_t* row = bm + static_cast<size_t>(e) * words;
+    for (int w = threadIdx.x; w < words; w += blockDim.x) row[w] = 0u;
+    __syncthreads();
+    const int o0 = tc_offsets[e], o1 = tc_offsets[e + 1];
+    const int lane = threadIdx.x & 31;
+    for (int base = o0 + (threadIdx.x & ~31); base < o1; base += blockDim.x) {
+        const int i = base + lane;
+        const bool ok = i < o1;
+        const int t = ok ? tc_eti[i] : -1;
+        const int word = ok ? (t >> 5) : -1;
+        const uint32_t bit = ok ? (1u << (t & 31)) : 0u;
+        const unsigned same = __match_any_sync(0xffffffffu, word);
+        // Every lane takes part in all 32 shuffles (a loop over its own group
+        // would leave the other lanes out of a full-mask shuffle).
+        uint32_t acc = 0u;
+        for (int src = 0; src < 32; ++src) {
+            const uint32_t b = __shfl_sync(0xffffffffu, bit, src);
+            if ((same >> src) & 1u) acc |= b;
+        }
+        if (ok && lane == __ffs(same) - 1) atomicOr(&row[word], acc);
+    }
 }
 
 // R0: warp per token.
@@ -100,7 +141,7 @@ __global__ void tr_decide_kernel(const int32_t* __restrict__ tc_offsets, int T, 
 // are dropped). thr = 0 when nothing changes.
 __global__ void __launch_bounds__(kSelThreads)
 tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
-                 const int32_t* __restrict__ ids, const int32_t* __restrict__ tc_eti,
+                 const uint32_t* __restrict__ bm, int words, const int32_t* __restrict__ tc_eti,
                  const int32_t* __restrict__ tc_offsets, const int4* __restrict__ par, int T,
                  int E, int K, unsigned long long* __restrict__ thr, int* err) {
     if (has_error(err)) return;
@@ -131,7 +172,7 @@ tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
             int t;
             if (up) {
                 t = i;
-                if (is_tc(ids, t, K, e)) continue;
+                if (tc_bit(bm, words, t, e)) continue;
             } else {
                 t = tc_eti[o0 + i];
             }
@@ -159,13 +200,11 @@ tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
     if (threadIdx.x == 0) thr[e] = s_prefix;
 }
 
-// Final membership of (t, e).
-__device__ __forceinline__ bool tr_member(const float* __restrict__ z, float lse_t,
-                                          const int32_t* __restrict__ ids, int t, int E, int K,
-                                          int e, const int4* __restrict__ par,
+// Final membership of (t, e), given whether token t chose e.
+__device__ __forceinline__ bool tr_member(const float* __restrict__ z, float lse_t, bool tc,
+                                          int t, int E, int e, const int4* __restrict__ par,
                                           const unsigned long long* __restrict__ thr) {
     const int4 pe = par[e];
-    const bool tc = is_tc(ids, t, K, e);
     if (pe.y == 0) return tc;
     const uint64_t key = tr_key(z[static_cast<size_t>(t) * E + e] - lse_t, t);
     if (pe.z) return tc || key >= thr[e];
@@ -190,7 +229,7 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     float zmax = -INFINITY;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, ids, t, E, K, e, par, thr);
+        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
         const unsigned b = __ballot_sync(0xffffffffu, mem);
         if (mem) zmax = fmaxf(zmax, zt[e]);
         count += __popc(b);
@@ -205,7 +244,7 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     float den = 0.f;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, ids, t, E, K, e, par, thr);
+        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
         float v = mem ? expf(zt[e] - zmax) : 0.f;
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         den += v;
@@ -214,7 +253,7 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     int base = tok_off[t];
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, ids, t, E, K, e, par, thr);
+        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
         const unsigned b = __ballot_sync(0xffffffffu, mem);
         if (mem) {
             const int slot = base + __popc(b & ((1u << lane) - 1u));
@@ -258,7 +297,7 @@ tr_scan_kernel(const int32_t* __restrict__ n_t, int T, int32_t* __restrict__ tok
 // the membership flags.
 __global__ void __launch_bounds__(kSelThreads)
 tr_compact_kernel(const float* __restrict__ z, const float* __restrict__ lse,
-                  const int32_t* __restrict__ ids, const int4* __restrict__ par,
+                  const uint32_t* __restrict__ bm, int words, const int4* __restrict__ par,
                   const unsigned long long* __restrict__ thr, int T, int E, int K,
                   const int32_t* __restrict__ offsets_tr, const int32_t* __restrict__ tok_off,
                   const int32_t* __restrict__ tok_exp, const float* __restrict__ w_tok,
@@ -273,19 +312,18 @@ tr_compact_kernel(const float* __restrict__ z, const float* __restrict__ lse,
     __syncthreads();
     for (int t0 = 0; t0 < T; t0 += blockDim.x) {
         const int t = t0 + threadIdx.x;
-        const bool mem = t < T && tr_member(z, t < T ? lse[t] : 0.f, ids, t, E, K, e, par, thr);
+        const bool mem = t < T && tr_member(z, lse[t], tc_bit(bm, words, t, e), t, E, e, par, thr);
         const unsigned b = __ballot_sync(0xffffffffu, mem);
         if (lane == 0) warp_cnt[warp] = __popc(b);
         __syncthreads();
         int before = s_run;
         for (int w = 0; w < warp; ++w) before += warp_cnt[w];
         const int lim = offsets_tr[e + 1];
-        if (mem) {
-            const int pos = before + __popc(b & ((1u << lane) - 1u));
-            if (pos >= lim) {  // more members than the decided count: inconsistent state
-                raise_error(err, MOE_ERR_CUDA);
-                continue;
-            }
+        const int pos = before + __popc(b & ((1u << lane) - 1u));
+        // More members than the decided count would be an inconsistent state:
+        // flag it and write nothing (every thread still reaches the barriers).
+        if (mem && pos >= lim) raise_error(err, MOE_ERR_CUDA);
+        if (mem && pos < lim) {
             eti_tr[pos] = t;
             // e is in t's list: the same membership test wrote it.
             const int end = tok_off[t + 1];
@@ -329,10 +367,16 @@ cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z
                                             err);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int words = (s.T + 31) / 32;
+    {
+        LaunchScope ls("tr_bitmap", st);
+        tr_bitmap_kernel<<<s.E, 256, 0, st>>>(tc_eti, tc_offsets, words, sc.bm, err);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         LaunchScope ls("tr_select", st);
-        tr_select_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, ids, tc_eti, tc_offsets, sc.par,
-                                                     s.T, s.E, s.K, sc.thr, err);
+        tr_select_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, sc.bm, words, tc_eti, tc_offsets,
+                                                     sc.par, s.T, s.E, s.K, sc.thr, err);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
@@ -356,9 +400,9 @@ cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         LaunchScope ls("tr_compact", st);
-        tr_compact_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, ids, sc.par, sc.thr, s.T, s.E,
-                                                      s.K, offsets_tr, tok_off, tok_exp, sc.w_tok,
-                                                      eti_tr, w_row, tok_rows, err);
+        tr_compact_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, sc.bm, words, sc.par, sc.thr,
+                                                      s.T, s.E, s.K, offsets_tr, tok_off, tok_exp,
+                                                      sc.w_tok, eti_tr, w_row, tok_rows, err);
     }
     return cudaGetLastError();
 }
