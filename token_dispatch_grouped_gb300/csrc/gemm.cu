@@ -1,9 +1,10 @@
 // gemm.cu — grouped expert GEMMs on tcgen05 tensor cores (sm_103a).
 //
-// One persistent, warp-specialised kernel template serves the six expert
-// GEMMs of the layer. It runs either one CTA per tile (CTAS = 1, M = 128) or a
-// CTA pair per tile (CTAS = 2, cluster of two CTAs, tcgen05 cta_group::2,
-// M = 256 split 128/128, the B tile split by N so each SM stages half of it).
+// One persistent, warp-specialised kernel template serves the expert GEMMs
+// of the layer (six kinds, plus the non-gated and slot-wise variants). It
+// runs either one CTA per tile (CTAS = 1, M = 128) or a CTA pair per tile
+// (CTAS = 2, cluster of two CTAs, tcgen05 cta_group::2, M = 256 split 128/128,
+// the B tile split by N so each SM stages half of it).
 // Warp roles in every CTA:
 //   warp 0      producer: TMA tile loads of the operands that are stored
 //               contiguously (weights, SwiGLU output, dH, A') into a ring of
@@ -18,8 +19,9 @@
 //               past an expert's end are zero-filled. No routed copy of the
 //               activations exists anywhere.
 //   warp 10     (gathering kinds, second CTA of a pair) relays the completion
-//               of that CTA's gathers to the pair's MMA issuer: cp.async can
-//               only signal a barrier of its own CTA.
+//               of that CTA's gathers to the pair's MMA issuer (cp.async can
+//               only signal a barrier of its own CTA) as the byte count of a
+//               16-byte bulk copy into the first CTA.
 // The accumulator is double-buffered in TMEM, so the epilogue of one tile
 // overlaps the main loop of the next. Tiles are walked in a static
 // round-robin over a device-side tile list derived from the per-expert row
@@ -206,34 +208,6 @@ __device__ __forceinline__ void store32_bf16(void* dst, const float (&v)[32]) {
     }
 }
 
-__device__ __forceinline__ void load32_bf16(const void* src, float (&v)[32]) {
-    const uint4* p = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint4 u = p[q];
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(b[j]);
-            v[8 * q + 2 * j] = f.x;
-            v[8 * q + 2 * j + 1] = f.y;
-        }
-    }
-}
-
-__device__ __forceinline__ void load32_bf16(const uint4 (&u)[4], float (&v)[32]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(b[j]);
-            v[8 * q + 2 * j] = f.x;
-            v[8 * q + 2 * j + 1] = f.y;
-        }
-    }
-}
-
 __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     tmem_ld32(taddr, r);
@@ -315,22 +289,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
         f[2 * j] = x.x;
         f[2 * j + 1] = x.y;
     }
-}
-
-// Fetched pieces -> box -> the lane's own row as 32 fp32.
-__device__ __forceinline__ void box_get_row(uint8_t* box, int lane, const uint4 (&pc4)[4],
-                                            float (&v)[32]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pc = lane + 32 * i;
-        *reinterpret_cast<uint4*>(box + box_off(pc >> 2, pc & 3)) = pc4[i];
-    }
-    __syncwarp();
-    uint4 u[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const uint4*>(box + box_off(lane, c));
-    __syncwarp();
-    load32_bf16(u, v);
 }
 
 // Non-gated backward for one lane's 32 columns: a (packed bf16 in ua) and
