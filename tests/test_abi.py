@@ -106,3 +106,26 @@ def test_gated_expert_needs_w3_before_any_device_work():
     assert B.LIB.moe_backward(*bw) == B.MOE_ERR_INVALID_ARG
     bw = [s, *fake[:15], None, *fake[16:19], 1 << 20, None]    # dW3 missing
     assert B.LIB.moe_backward(*bw) == B.MOE_ERR_INVALID_ARG
+
+
+def test_row_routing_entry_points_host_checks():
+    from token_dispatch_grouped_gb300 import binding as B
+    T, d, E, K, h = 4096, 1024, 16, 4, 2048
+    s = B.shape(T, d, E, K, h)
+    cap = B.moe_rows_capacity(s, 128)
+    assert cap == min(T * K + E * 127, T * E)
+    assert B.moe_rows_capacity(s, 0) == 0
+    assert B.moe_token_rounding_workspace_size(s, 128) >= 4 * T + 16 * E + 4 * cap
+    fwd = B.moe_workspace_size_rows(s, cap, B.MOE_WS_FORWARD)
+    bwd = B.moe_workspace_size_rows(s, cap, B.MOE_WS_BACKWARD)
+    assert fwd >= cap * h * 2 and bwd >= cap * 2 * h * 2
+    assert B.moe_workspace_size_rows(s, 0, B.MOE_WS_FORWARD) == 0
+    # rejected on the host before any device work: nulls, bad tile, bad capacity
+    nul = [None] * 11
+    assert B.LIB.moe_token_rounding(s, 128, *nul, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_token_rounding(s, 5000, *nul, 0, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert B.LIB.moe_forward_rows(s, cap, *([None] * 13), 0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_forward_rows(s, T * E + 1, *([None] * 13), 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_backward_rows(s, cap, *([None] * 20), 0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_forward_slotwise(s, *([None] * 12), 0, None) == B.MOE_ERR_INVALID_ARG
