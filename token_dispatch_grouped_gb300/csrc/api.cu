@@ -273,6 +273,7 @@ size_t layout_rounding(const moe_shape& s, int m_tile, void* ws, TrScratch* o) {
     w.n_t = c.take<int32_t>(s.T);
     w.w_tok = c.take<float>(rows_capacity(s, m_tile));
     w.bm = c.take<uint32_t>(static_cast<size_t>(s.E) * ((s.T + 31) / 32));
+    w.lpT = c.take<float>(static_cast<size_t>(s.E) * s.T);
     if (o) *o = w;
     return align_up(c.off, 256);
 }

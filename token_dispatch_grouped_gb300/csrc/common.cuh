@@ -70,7 +70,7 @@ cudaError_t launch_slot_dispatch(const moe_shape& s, const int32_t* ids, int32_t
                                  cudaStream_t st);
 
 // Token rounding (rounding.cu). Scratch: lse [T], par [E], thr [E], n_t [T],
-// w_tok [rows_max], bm [E][ceil(T/32)] (token-choice bitmap).
+// w_tok [rows_max], bm [E][ceil(T/32)] (token-choice bitmap), lpT [E][T].
 struct TrScratch {
     float* lse;
     int4* par;
@@ -78,6 +78,7 @@ struct TrScratch {
     int32_t* n_t;
     float* w_tok;
     uint32_t* bm;
+    float* lpT;  // [E][T] log-probabilities, expert-major
 };
 cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z,
                                   const int32_t* ids, const int32_t* tc_eti,

@@ -5,7 +5,8 @@
 // Inputs: the router logits z [T, E] (fp32), the token-choice ids [T, K] and
 // the offsets of their dispatch (f_e = token-choice count of expert e).
 //   R0  lse_t = log sum_e exp(z_t,e); the score of (t, e) is the log-probability
-//       z_t,e - lse_t (monotone in the softmax probability S).
+//       z_t,e - lse_t (monotone in the softmax probability S), also stored
+//       expert-major for the per-expert passes.
 //   R1  one CTA: per expert the nearest multiple of M_tile (a tie rounds down;
 //       at most T), the number m_e of tokens to drop or add, and the offsets of
 //       the rounded rows.
@@ -22,7 +23,7 @@
 //   R6  one CTA per expert: compaction of its final tokens in ascending order
 //       into expert_token_indices, with each row's weight and its CSR slot.
 // The expert-side kernels (R2, R6) test token choice in a bitmap [E][T/32]
-// built from the token-choice dispatch.
+// built from the routing.
 // Histogram bins in R2 are counted with shared-memory atomics (exact integer
 // counts); every output is order-independent and bit-reproducible.
 #include <cfloat>
@@ -56,36 +57,21 @@ __device__ __forceinline__ bool tc_bit(const uint32_t* __restrict__ bm, int word
     return (bm[static_cast<size_t>(e) * words + (t >> 5)] >> (t & 31)) & 1u;
 }
 
-// Builds the bitmap from the token-choice dispatch: CTA per expert; the
-// expert's tokens are sorted, so the tokens of one word are adjacent; a
-// warp's lanes that share a word combine their bits by shuffles and the lowest
-// of them ORs them into the word (a word can span two warps' ranges; an
-// integer OR gives the same word in any order).
-__global__ void tr_bitmap_kernel(const int32_t* __restrict__ tc_eti,
-                                 const int32_t* __restrict__ tc_offsets, int words,
+// Builds the bitmap (zeroed before) from the routing: one warp per 32 tokens,
+// lane = token & 31; for each slot, the lanes that chose the same expert form
+// that expert's word bits (their lane mask) and the lowest of them ORs the mask
+// into the word (an integer OR gives the same word in any order).
+__global__ void tr_bitmap_kernel(const int32_t* __restrict__ ids, int T, int K, int words,
                                  uint32_t* __restrict__ bm, int* err) {
     if (has_error(err)) return;
-    const int e = blockIdx.x;
-    uint32_t* row = bm + static_cast<size_t>(e) * words;
-    for (int w = threadIdx.x; w < words; w += blockDim.x) row[w] = 0u;
-    __syncthreads();
-    const int o0 = tc_offsets[e], o1 = tc_offsets[e + 1];
     const int lane = threadIdx.x & 31;
-    for (int base = o0 + (threadIdx.x & ~31); base < o1; base += blockDim.x) {
-        const int i = base + lane;
-        const bool ok = i < o1;
-        const int t = ok ? tc_eti[i] : -1;
-        const int word = ok ? (t >> 5) : -1;
-        const uint32_t bit = ok ? (1u << (t & 31)) : 0u;
-        const unsigned same = __match_any_sync(0xffffffffu, word);
-        // Every lane takes part in all 32 shuffles (a loop over its own group
-        // would leave the other lanes out of a full-mask shuffle).
-        uint32_t acc = 0u;
-        for (int src = 0; src < 32; ++src) {
-            const uint32_t b = __shfl_sync(0xffffffffu, bit, src);
-            if ((same >> src) & 1u) acc |= b;
-        }
-        if (ok && lane == __ffs(same) - 1) atomicOr(&row[word], acc);
+    const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);  // word = 32 tokens
+    if (w >= words) return;  // warp-uniform
+    const int t = w * 32 + lane;
+    for (int k = 0; k < K; ++k) {
+        const int e = t < T ? ids[static_cast<size_t>(t) * K + k] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(same) - 1) atomicOr(&bm[static_cast<size_t>(e) * words + w], same);
     }
 }
 
@@ -104,6 +90,26 @@ __global__ void tr_lse_kernel(const float* __restrict__ z, int T, int E, float* 
     for (int e = lane; e < E; e += 32) s += expf(zt[e] - m);
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (lane == 0) lse[t] = m + logf(s);
+}
+
+// R0': lpT [E][T] = z[t, e] - lse[t], expert-major, through 32 x 32 shared
+// tiles (coalesced reads of z and writes of lpT), so the per-expert passes
+// read their scores contiguously.
+__global__ void tr_transpose_kernel(const float* __restrict__ z, const float* __restrict__ lse,
+                                    int T, int E, float* __restrict__ lpT, int* err) {
+    if (has_error(err)) return;
+    __shared__ float tile[32][33];
+    const int t0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+    for (int r = ty; r < 32; r += 8) {
+        const int t = t0 + r, e = e0 + tx;
+        tile[r][tx] = (t < T && e < E) ? z[static_cast<size_t>(t) * E + e] - lse[t] : 0.f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {
+        const int e = e0 + r, t = t0 + tx;
+        if (t < T && e < E) lpT[static_cast<size_t>(e) * T + t] = tile[tx][r];
+    }
 }
 
 // R1: one CTA of 256 threads (E <= 256).
@@ -140,8 +146,8 @@ __global__ void tr_decide_kernel(const int32_t* __restrict__ tc_offsets, int T, 
 // rounding down, the m-th smallest key among tokens that chose e (keys <= thr
 // are dropped). thr = 0 when nothing changes.
 __global__ void __launch_bounds__(kSelThreads)
-tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
-                 const uint32_t* __restrict__ bm, int words, const int32_t* __restrict__ tc_eti,
+tr_select_kernel(const float* __restrict__ lpT, const uint32_t* __restrict__ bm, int words,
+                 const int32_t* __restrict__ tc_eti,
                  const int32_t* __restrict__ tc_offsets, const int4* __restrict__ par, int T,
                  int E, int K, unsigned long long* __restrict__ thr, int* err) {
     if (has_error(err)) return;
@@ -176,7 +182,7 @@ tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
             } else {
                 t = tc_eti[o0 + i];
             }
-            const uint64_t key = tr_key(z[static_cast<size_t>(t) * E + e] - lse[t], t);
+            const uint64_t key = tr_key(lpT[static_cast<size_t>(e) * T + t], t);
             if ((key & hmask) != prefix) continue;
             // Rounding up ranks from the largest key, rounding down from the smallest.
             const unsigned int dig = static_cast<unsigned int>((key >> shift) & 0xffu);
@@ -200,13 +206,13 @@ tr_select_kernel(const float* __restrict__ z, const float* __restrict__ lse,
     if (threadIdx.x == 0) thr[e] = s_prefix;
 }
 
-// Final membership of (t, e), given whether token t chose e.
-__device__ __forceinline__ bool tr_member(const float* __restrict__ z, float lse_t, bool tc,
-                                          int t, int E, int e, const int4* __restrict__ par,
+// Final membership of (t, e), given whether token t chose e and its score lp.
+__device__ __forceinline__ bool tr_member(float lp, bool tc, int t, int e,
+                                          const int4* __restrict__ par,
                                           const unsigned long long* __restrict__ thr) {
     const int4 pe = par[e];
     if (pe.y == 0) return tc;
-    const uint64_t key = tr_key(z[static_cast<size_t>(t) * E + e] - lse_t, t);
+    const uint64_t key = tr_key(lp, t);
     if (pe.z) return tc || key >= thr[e];
     return tc && key > thr[e];
 }
@@ -224,12 +230,12 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     const int t = blockIdx.x * kTokWarps + threadIdx.x / 32;
     if (t >= T) return;
     const float lt = lse[t];
-    const float* zt = z + static_cast<size_t>(t) * E;
+    const float* zt = z + static_cast<size_t>(t) * E;  // score z - lse: as in the transpose
     int count = 0;
     float zmax = -INFINITY;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
+        const bool mem = e < E && tr_member(zt[e] - lt, is_tc(ids, t, K, e), t, e, par, thr);
         const unsigned b = __ballot_sync(0xffffffffu, mem);
         if (mem) zmax = fmaxf(zmax, zt[e]);
         count += __popc(b);
@@ -244,7 +250,7 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     float den = 0.f;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
+        const bool mem = e < E && tr_member(zt[e] - lt, is_tc(ids, t, K, e), t, e, par, thr);
         float v = mem ? expf(zt[e] - zmax) : 0.f;
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         den += v;
@@ -253,7 +259,7 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     int base = tok_off[t];
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const bool mem = e < E && tr_member(z, lt, is_tc(ids, t, K, e), t, E, e, par, thr);
+        const bool mem = e < E && tr_member(zt[e] - lt, is_tc(ids, t, K, e), t, e, par, thr);
         const unsigned b = __ballot_sync(0xffffffffu, mem);
         if (mem) {
             const int slot = base + __popc(b & ((1u << lane) - 1u));
@@ -264,66 +270,96 @@ __global__ void tr_tokens_kernel(const float* __restrict__ z, const float* __res
     }
 }
 
-// R4: one CTA, exclusive scan of n_t into tok_off [T+1].
+// R4: one CTA, exclusive scan of n_t into tok_off [T+1]: 1024 counts at a
+// time (coalesced), warp scans, then a scan of the 32 warp totals.
 __global__ void __launch_bounds__(1024)
 tr_scan_kernel(const int32_t* __restrict__ n_t, int T, int32_t* __restrict__ tok_off, int* err) {
     if (has_error(err)) return;
-    __shared__ int32_t part[1024];
-    const int per = (T + blockDim.x - 1) / blockDim.x;
-    const int b0 = min(T, static_cast<int>(threadIdx.x) * per);
-    const int b1 = min(T, b0 + per);
-    int32_t s = 0;
-    for (int i = b0; i < b1; ++i) s += n_t[i];
-    part[threadIdx.x] = s;
+    __shared__ int32_t wsum[32];
+    __shared__ int32_t s_run;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_run = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int32_t run = 0;
-        for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
-            const int32_t v = part[i];
-            part[i] = run;
-            run += v;
+    for (int t0 = 0; t0 < T; t0 += 1024) {
+        const int t = t0 + threadIdx.x;
+        const int32_t v = t < T ? n_t[t] : 0;
+        int32_t incl = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
         }
-        tok_off[T] = run;
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t w = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += u;
+            }
+            wsum[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int32_t base = s_run + (warp > 0 ? wsum[warp - 1] : 0);
+        if (t < T) tok_off[t] = base + incl - v;
+        __syncthreads();
+        if (threadIdx.x == 0) s_run += wsum[31];
+        __syncthreads();
     }
-    __syncthreads();
-    int32_t run = part[threadIdx.x];
-    for (int i = b0; i < b1; ++i) {
-        tok_off[i] = run;
-        run += n_t[i];
-    }
+    if (threadIdx.x == 0) tok_off[T] = s_run;
 }
 
-// R6: CTA per expert; tokens in ascending order, 1024 at a time, block scan of
-// the membership flags.
+// R6: CTA per expert; each thread takes 8 consecutive tokens per round
+// (8192 per round), a block scan of the per-thread member counts places them
+// in ascending token order.
 __global__ void __launch_bounds__(kSelThreads)
-tr_compact_kernel(const float* __restrict__ z, const float* __restrict__ lse,
-                  const uint32_t* __restrict__ bm, int words, const int4* __restrict__ par,
-                  const unsigned long long* __restrict__ thr, int T, int E, int K,
-                  const int32_t* __restrict__ offsets_tr, const int32_t* __restrict__ tok_off,
-                  const int32_t* __restrict__ tok_exp, const float* __restrict__ w_tok,
-                  int32_t* __restrict__ eti_tr, float* __restrict__ w_row,
-                  int32_t* __restrict__ tok_rows, int* err) {
+tr_compact_kernel(const float* __restrict__ lpT, const uint32_t* __restrict__ bm, int words,
+                  const int4* __restrict__ par, const unsigned long long* __restrict__ thr,
+                  int T, int E, int K, const int32_t* __restrict__ offsets_tr,
+                  const int32_t* __restrict__ tok_off, const int32_t* __restrict__ tok_exp,
+                  const float* __restrict__ w_tok, int32_t* __restrict__ eti_tr,
+                  float* __restrict__ w_row, int32_t* __restrict__ tok_rows, int* err) {
     if (has_error(err)) return;
-    __shared__ int warp_cnt[kSelThreads / 32];
+    __shared__ int wsum[kSelThreads / 32];
     __shared__ int s_run;
     const int e = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
+    const int lim = offsets_tr[e + 1];
+    const float* lp = lpT + static_cast<size_t>(e) * T;
     if (threadIdx.x == 0) s_run = offsets_tr[e];
     __syncthreads();
-    for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-        const int t = t0 + threadIdx.x;
-        const bool mem = t < T && tr_member(z, lse[t], tc_bit(bm, words, t, e), t, E, e, par, thr);
-        const unsigned b = __ballot_sync(0xffffffffu, mem);
-        if (lane == 0) warp_cnt[warp] = __popc(b);
+    for (int r0 = 0; r0 < T; r0 += kSelThreads * 8) {
+        const int tb = r0 + threadIdx.x * 8;
+        uint32_t mm = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = tb + j;
+            if (t < T && tr_member(lp[t], tc_bit(bm, words, t, e), t, e, par, thr)) mm |= 1u << j;
+        }
+        const int cnt = __popc(mm);
+        int incl = cnt;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        if (lane == 31) wsum[warp] = incl;
         __syncthreads();
-        int before = s_run;
-        for (int w = 0; w < warp; ++w) before += warp_cnt[w];
-        const int lim = offsets_tr[e + 1];
-        const int pos = before + __popc(b & ((1u << lane) - 1u));
-        // More members than the decided count would be an inconsistent state:
-        // flag it and write nothing (every thread still reaches the barriers).
-        if (mem && pos >= lim) raise_error(err, MOE_ERR_CUDA);
-        if (mem && pos < lim) {
+        if (warp == 0) {
+            int v = wsum[lane];
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            wsum[lane] = v;
+        }
+        __syncthreads();
+        int pos = s_run + (warp > 0 ? wsum[warp - 1] : 0) + incl - cnt;
+        for (int j = 0; j < 8; ++j) {
+            if (!((mm >> j) & 1u)) continue;
+            const int t = tb + j;
+            if (pos >= lim) {  // more members than the decided count: inconsistent state
+                raise_error(err, MOE_ERR_CUDA);
+                break;
+            }
             eti_tr[pos] = t;
             // e is in t's list: the same membership test wrote it.
             const int end = tok_off[t + 1];
@@ -335,13 +371,10 @@ tr_compact_kernel(const float* __restrict__ z, const float* __restrict__ lse,
             } else {
                 raise_error(err, MOE_ERR_CUDA);
             }
+            ++pos;
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int add = 0;
-            for (int w = 0; w < static_cast<int>(blockDim.x) / 32; ++w) add += warp_cnt[w];
-            s_run += add;
-        }
+        if (threadIdx.x == 0) s_run += wsum[31];
         __syncthreads();
     }
 }
@@ -362,6 +395,12 @@ cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
+        LaunchScope ls("tr_transpose", st);
+        tr_transpose_kernel<<<dim3((s.T + 31) / 32, (s.E + 31) / 32), 256, 0, st>>>(
+            z, sc.lse, s.T, s.E, sc.lpT, err);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
         LaunchScope ls("tr_decide", st);
         tr_decide_kernel<<<1, 256, 0, st>>>(tc_offsets, s.T, s.E, m_tile, sc.par, offsets_tr,
                                             err);
@@ -370,12 +409,14 @@ cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z
     const int words = (s.T + 31) / 32;
     {
         LaunchScope ls("tr_bitmap", st);
-        tr_bitmap_kernel<<<s.E, 256, 0, st>>>(tc_eti, tc_offsets, words, sc.bm, err);
+        e = cudaMemsetAsync(sc.bm, 0, static_cast<size_t>(s.E) * words * sizeof(uint32_t), st);
+        if (e != cudaSuccess) return e;
+        tr_bitmap_kernel<<<(words + 7) / 8, 256, 0, st>>>(ids, s.T, s.K, words, sc.bm, err);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         LaunchScope ls("tr_select", st);
-        tr_select_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, sc.bm, words, tc_eti, tc_offsets,
+        tr_select_kernel<<<s.E, kSelThreads, 0, st>>>(sc.lpT, sc.bm, words, tc_eti, tc_offsets,
                                                      sc.par, s.T, s.E, s.K, sc.thr, err);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -400,7 +441,7 @@ cudaError_t launch_token_rounding(const moe_shape& s, int m_tile, const float* z
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     {
         LaunchScope ls("tr_compact", st);
-        tr_compact_kernel<<<s.E, kSelThreads, 0, st>>>(z, sc.lse, sc.bm, words, sc.par, sc.thr,
+        tr_compact_kernel<<<s.E, kSelThreads, 0, st>>>(sc.lpT, sc.bm, words, sc.par, sc.thr,
                                                       s.T, s.E, s.K, offsets_tr, tok_off, tok_exp,
                                                       sc.w_tok, eti_tr, w_row, tok_rows, err);
     }
