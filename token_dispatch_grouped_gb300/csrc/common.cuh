@@ -37,9 +37,10 @@ struct LaunchScope {
 };
 
 // Tensor map of a 2D row-major bf16 array [rows, cols] with a box of
-// box_cols x box_rows and 128-byte swizzle (or none). Returns false on failure.
+// box_cols x box_rows and a swizzle of `swizzle` bytes (128, 64, or 0 for
+// none). Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                    uint32_t box_cols, uint32_t box_rows, bool swizzle128 = true);
+                    uint32_t box_cols, uint32_t box_rows, int swizzle = 128);
 // Same for a row-major fp32 array, without swizzle.
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                    uint32_t box_cols, uint32_t box_rows);

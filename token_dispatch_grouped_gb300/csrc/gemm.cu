@@ -96,20 +96,33 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BNL * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
-    static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
     static constexpr int SMEM_MISC = 7168;        // barriers, TMEM slot, segments, tile prefix
     static constexpr int SMEM_EPI = 4 * EPI_BOXES * 2048;  // per epilogue warp: 32x32 bf16 boxes
+    // Pipeline stages: what the 227 KB left after alignment, misc and epilogue
+    // staging holds, at most 8.
+    static constexpr int STAGES_FIT = (232448 - 1024 - SMEM_MISC - SMEM_EPI) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int SMEM_TILES = STAGES * STAGE_BYTES;
     static constexpr int SMEM_TOTAL = 1024 + SMEM_TILES + SMEM_MISC + SMEM_EPI;
+    static_assert(STAGES >= 3 && SMEM_TOTAL <= 232448, "shared memory");
     static_assert(1024 + 16 * kMaxE + 4 * (kMaxE + 1) <= SMEM_MISC, "misc region");
-    static_assert(8 * (3 * STAGES + 4) + 48 <= 1024, "barrier region");
+    // Pipeline barriers, TMEM slot, abort flag and relay slot below 768; the
+    // epilogue's H-ring barriers (4 warps x kHR) from 768 to 1024.
+    static_assert(8 * (3 * STAGES + 4) + 48 <= 768, "barrier region");
 };
 
 constexpr int kGatherThreads = 128;
-// Shared 2 KB staging boxes per epilogue warp (G3 writes three outputs per chunk).
+// G3 epilogue: chunks of H (32 rows x 32 columns of a, and of b when gated) are
+// loaded by TMA into a ring of kHR shared slots per warp, kHR - 1 chunks ahead.
+constexpr int kHR = 3;
+static_assert(768 + 8 * 4 * kHR <= 1024, "H-ring barriers");
+// Shared 2 KB staging boxes per epilogue warp: two for the stored outputs; for
+// G3 the H ring (whose boxes are rewritten in place as dH) plus one box for A'.
 template <GemmKind KIND>
-constexpr int epi_boxes() { return KIND == G3_DH || KIND == G3_DH_ACT ? 3 : 2; }
+__host__ __device__ constexpr int epi_boxes() {
+    return KIND == G3_DH ? 2 * kHR + 1 : KIND == G3_DH_ACT ? kHR + 1 : 2;
+}
 template <GemmKind KIND, int CTAS>
 constexpr int threads_of() {
     return 192 + (Tr<KIND>::A_G ? kGatherThreads : 0) + (Tr<KIND>::A_G && CTAS == 2 ? 32 : 0);
@@ -221,7 +234,9 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
 // box so that global traffic is issued four lanes per 64-byte row segment (8
 // rows per instruction) instead of one lane per row. Inside the box, 16-byte
 // piece c of row l sits at piece c ^ ((l >> 1) & 3): row-wise writes by the
-// 32 lanes then hit 8 distinct 16-byte bank groups per 8 lanes.
+// 32 lanes then hit 8 distinct 16-byte bank groups per 8 lanes. On a box at a
+// 512-byte boundary this is the placement of TMA's 64-byte swizzle for a box of
+// 64-byte rows, so TMA loads and stores of such boxes use the same layout.
 __device__ __forceinline__ uint32_t box_off(int row, int c16) {
     return static_cast<uint32_t>(row * 64 + ((c16 ^ ((row >> 1) & 3)) << 4));
 }
@@ -254,33 +269,6 @@ __device__ __forceinline__ void box_store_rows(const uint8_t* box, int lane, __n
     __syncwarp();
 }
 
-// Global pieces of rows base + row * ld (zeros for row >= nvalid) into registers.
-__device__ __forceinline__ void rows_fetch(uint4 (&pc4)[4], int lane, const __nv_bfloat16* base,
-                                           size_t ld, int nvalid) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pc = lane + 32 * i;
-        const int row = pc >> 2, c16 = pc & 3;
-        pc4[i] = row < nvalid ? *reinterpret_cast<const uint4*>(base + static_cast<size_t>(row) * ld +
-                                                                c16 * 8)
-                              : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// Fetched pieces -> box -> the lane's own row as 4 x 8 packed bf16.
-__device__ __forceinline__ void box_get_row_raw(uint8_t* box, int lane, const uint4 (&pc4)[4],
-                                                uint4 (&u)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int pc = lane + 32 * i;
-        *reinterpret_cast<uint4*>(box + box_off(pc >> 2, pc & 3)) = pc4[i];
-    }
-    __syncwarp();
-#pragma unroll
-    for (int c = 0; c < 4; ++c) u[c] = *reinterpret_cast<const uint4*>(box + box_off(lane, c));
-    __syncwarp();
-}
-
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
@@ -292,11 +280,11 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
 }
 
 // Non-gated backward for one lane's 32 columns: a (packed bf16 in ua) and
-// dA' (v) give dS += <dA', act(a)>, da = w dA' act'(a) into box_da and
-// A' = w act(a) into box_ap.
+// dA' (v) give dS += <dA', act(a)>, da = w dA' act'(a) into the lane's row of
+// box_da and A' = w act(a) packed into ap.
 template <int ACT>
 __device__ __forceinline__ void ng_chunk(const uint4 (&ua)[4], const float (&v)[32], float w,
-                                         float& dsum, uint8_t* box_da, uint8_t* box_ap,
+                                         float& dsum, uint8_t* box_da, uint4 (&ap4)[4],
                                          int lane) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -315,8 +303,55 @@ __device__ __forceinline__ void ng_chunk(const uint4 (&ua)[4], const float (&v)[
             ap[i / 2] = pack_bf16(w * f0, w * f1);
         }
         *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = make_uint4(da[0], da[1], da[2], da[3]);
-        *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = make_uint4(ap[0], ap[1], ap[2], ap[3]);
+        ap4[c] = make_uint4(ap[0], ap[1], ap[2], ap[3]);
     }
+}
+
+// SwiGLU backward for one lane's 32 columns: a, b (packed bf16) and dA' (v),
+// with A = SiLU(a) b, dA = w dA', give dS += <dA', A>, da = dA b SiLU'(a) and
+// db = dA SiLU(a) into the lane's rows of box_da and box_db, and A' = w A
+// packed into ap.
+__device__ __forceinline__ void sw_chunk(const uint4 (&ua)[4], const uint4 (&ub)[4],
+                                         const float (&v)[32], float w, float& dsum,
+                                         uint8_t* box_da, uint8_t* box_db, uint4 (&ap4)[4],
+                                         int lane) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float a8[8], b8[8];
+        unpack8(ua[c], a8);
+        unpack8(ub[c], b8);
+        uint32_t da[4], db[4], ap[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            float dav[2], dbv[2], apv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float a = a8[i + u], b = b8[i + u], vk = v[8 * c + i + u];
+                const float sg = __fdividef(1.f, 1.f + __expf(-a));
+                const float si = a * sg;
+                const float Av = si * b;
+                dsum = fmaf(vk, Av, dsum);
+                const float dA = w * vk;
+                dav[u] = dA * b * (sg + si * (1.f - sg));
+                dbv[u] = dA * si;
+                apv[u] = w * Av;
+            }
+            da[i / 2] = pack_bf16(dav[0], dav[1]);
+            db[i / 2] = pack_bf16(dbv[0], dbv[1]);
+            ap[i / 2] = pack_bf16(apv[0], apv[1]);
+        }
+        *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = make_uint4(da[0], da[1], da[2], da[3]);
+        *reinterpret_cast<uint4*>(box_db + box_off(lane, c)) = make_uint4(db[0], db[1], db[2], db[3]);
+        ap4[c] = make_uint4(ap[0], ap[1], ap[2], ap[3]);
+    }
+}
+
+// Bounded wait that ignores the abort flag: lets a warp's own copies in flight
+// land before it leaves.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u))
+        if (globaltimer_ns() - t0 > kWaitNs) break;
 }
 
 template <GemmKind KIND, int BN, int CTAS>
@@ -394,6 +429,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 4 * CTAS);
         }
+        if constexpr (KIND == G3_DH || KIND == G3_DH_ACT)
+            for (int i = 0; i < 4 * kHR; ++i) mbar_init(bar0 + 768u + 8u * i, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -575,12 +612,44 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         uint8_t* stg = epi + (warp - 2) * epi_boxes<KIND>() * 2048;  // this warp's boxes
         int nstore = 0;                           // TMA stores issued by this warp
+        // G3: this warp's H ring. Slot s holds box a (and box b when gated) of one
+        // chunk; the A' box follows the ring; hc counts the chunks consumed.
+        constexpr bool G3 = KIND == G3_DH || KIND == G3_DH_ACT;
+        constexpr int HSLOT = (KIND == G3_DH ? 2 : 1) * 2048;
+        uint8_t* box_ap = stg + kHR * HSLOT;
+        const uint32_t hbar0 = bar0 + 768u + 8u * kHR * (warp - 2);
+        uint32_t hc = 0;
+        auto h_bar = [&](uint32_t c) { return hbar0 + 8u * (c % kHR); };
+        auto h_load = [&](uint32_t c, int col, int row) {  // lane 0
+            const uint32_t dst = smem_u32(stg + (c % kHR) * HSLOT);
+            mbar_arrive_expect_tx(h_bar(c), HSLOT);
+            tma_load_2d(dst, &mapA, h_bar(c), col, row);
+            if constexpr (KIND == G3_DH) tma_load_2d(dst + 2048, &mapA, h_bar(c), p.h + col, row);
+        };
         int it = 0;
         for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
             const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+            bool stop = false;
+            // G3: the warp's first row and column of H, its chunk count, and the
+            // first kHR chunks, loaded while the MMA finishes the tile.
+            int hrow = 0, hn0 = 0, hn = 0, hissued = 0;
+            if constexpr (G3) {
+                hrow = t.lo + t.m_blk * BMC + rank * BM + q * 32;
+                hn0 = t.n_blk * BN;
+                hn = t.hi > hrow ? min(BN, p.h - hn0) / 32 : 0;
+                hissued = min(kHR, hn);
+                if (lane == 0 && hn > 0) {
+                    bulk_wait_group_read<0>();  // earlier stores have read their slots
+                    for (int c = 0; c < hissued; ++c) h_load(hc + c, hn0 + 32 * c, hrow);
+                }
+                __syncwarp();
+            }
+            if (!warp_wait(tfull_bar(acc), acc_phase, abort_flag)) {
+                for (int c = 0; c < hissued; ++c) mbar_drain(h_bar(hc + c), ((hc + c) / kHR) & 1u);
+                break;
+            }
             tc_fence_after();
             const uint32_t tacc = tmem_base + lane_addr + acc * NMMA;
             const int rbase = t.lo + t.m_blk * BMC + rank * BM;  // VM: first row of this CTA
@@ -712,109 +781,81 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         }
                     }
                 }
-            } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
+            } else if constexpr (G3) {
+                // dA' = dy W2_e is in TMEM, H arrives chunk by chunk in the ring.
+                // dH overwrites H in its slot; dH and A' leave by TMA when all 32
+                // rows of the warp are the expert's, else by row-masked stores.
                 const int r = rbase + row_in_tile;
                 const bool valid = r < t.hi;
-                const int row0w = rbase + q * 32;
-                const int nvalid = t.hi - row0w;
-                const int n0 = t.n_blk * BN;
-                const int ncols = min(BN, p.h - n0);  // the last N tile may be partial
-                const size_t r0 = static_cast<size_t>(row0w > 0 ? row0w : 0);
+                const int nvalid = t.hi - hrow;
                 const float w = valid ? p.wrow[r] : 0.f;
+                const size_t hs = (KIND == G3_DH ? 2 : 1) * static_cast<size_t>(p.h);
+                __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) +
+                                     static_cast<size_t>(hrow) * hs + hn0;
+                __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) +
+                                     static_cast<size_t>(hrow) * p.h + hn0;
                 float dsum = 0.f;
-                if constexpr (KIND == G3_DH_ACT) {
-                    // Non-gated: H = a; A = act(a); dA = w dA'; da = dA act'(a);
-                    // A' = w A. dH and A' are [TK, h].
-                    const __nv_bfloat16* Hw =
-                        static_cast<const __nv_bfloat16*>(p.aux0) + r0 * p.h + n0;
-                    __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * p.h + n0;
-                    __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
-                    uint8_t* box_da = stg;
-                    uint8_t* box_ap = stg + 2048;
-                    uint8_t* box_in = stg + 4096;
-                    uint4 pa[4];
-                    if (nvalid > 0) rows_fetch(pa, lane, Hw, p.h, nvalid);
+                int jj = 0;
 #pragma unroll 1
-                    for (int j = 0; j < ncols; j += 32) {
-                        uint4 ua[4];
-                        if (nvalid > 0) {
-                            box_get_row_raw(box_in, lane, pa, ua);
-                            if (j + 32 < ncols) rows_fetch(pa, lane, Hw + j + 32, p.h, nvalid);
-                        }
-                        tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
-                        if (nvalid > 0) {
-                            if (p.act == 2) ng_chunk<2>(ua, v, w, dsum, box_da, box_ap, lane);
-                            else ng_chunk<1>(ua, v, w, dsum, box_da, box_ap, lane);
-                            box_store_rows(box_da, lane, dHw + j, p.h, nvalid);
-                            box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
+                for (; jj < hn; ++jj) {
+                    const uint32_t c = hc + jj;
+                    uint8_t* box_a = stg + (c % kHR) * HSLOT;
+                    uint8_t* box_b = box_a + 2048;  // gated
+                    if (!warp_wait(h_bar(c), (c / kHR) & 1u, abort_flag)) break;
+                    uint4 ua[4], ub[4], ap4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ua[k] = *reinterpret_cast<const uint4*>(box_a + box_off(lane, k));
+                    if constexpr (KIND == G3_DH) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ub[k] = *reinterpret_cast<const uint4*>(box_b + box_off(lane, k));
+                    }
+                    tmem_ld32f(tacc + 32 * jj, v);  // dA'
+                    if constexpr (KIND == G3_DH) {
+                        sw_chunk(ua, ub, v, w, dsum, box_a, box_b, ap4, lane);
+                    } else {
+                        if (p.act == 2) ng_chunk<2>(ua, v, w, dsum, box_a, ap4, lane);
+                        else ng_chunk<1>(ua, v, w, dsum, box_a, ap4, lane);
+                    }
+                    // The A' box and the previous chunk's slot are free once that
+                    // chunk's stores have read them.
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(box_ap + box_off(lane, k)) = ap4[k];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    // Refill the previous chunk's slot kHR chunks ahead.
+                    const bool refill = jj >= 1 && hissued < hn;
+                    const int col = hn0 + 32 * jj;
+                    if (lane == 0) {
+                        if (refill) h_load(hc + hissued, hn0 + 32 * hissued, hrow);
+                        if (nvalid >= 32) {
+                            tma_store_2d(&mapO, smem_u32(box_a), col, hrow);
+                            if constexpr (KIND == G3_DH)
+                                tma_store_2d(&mapO, smem_u32(box_b), p.h + col, hrow);
+                            tma_store_2d(&mapB1, smem_u32(box_ap), col, hrow);
+                            bulk_commit_group();
                         }
                     }
-                } else {
-                    const __nv_bfloat16* Hw =
-                        static_cast<const __nv_bfloat16*>(p.aux0) + r0 * (2 * p.h) + n0;
-                    __nv_bfloat16* dHw = static_cast<__nv_bfloat16*>(p.out0) + r0 * (2 * p.h) + n0;
-                    __nv_bfloat16* Apw = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
-                    uint8_t* box_da = stg;
-                    uint8_t* box_db = stg + 2048;
-                    uint8_t* box_ap = stg + 4096;
-                    // H (a | b) of the next 32 columns is fetched while this chunk is
-                    // computed.
-                    uint4 pa[4], pb[4];
-                    if (nvalid > 0) {
-                        rows_fetch(pa, lane, Hw, 2 * p.h, nvalid);
-                        rows_fetch(pb, lane, Hw + p.h, 2 * p.h, nvalid);
-                    }
-#pragma unroll 1
-                    for (int j = 0; j < ncols; j += 32) {
-                        uint4 ua[4], ub[4];
-                        if (nvalid > 0) {
-                            box_get_row_raw(box_da, lane, pa, ua);
-                            box_get_row_raw(box_db, lane, pb, ub);
-                            if (j + 32 < ncols) {
-                                rows_fetch(pa, lane, Hw + j + 32, 2 * p.h, nvalid);
-                                rows_fetch(pb, lane, Hw + p.h + j + 32, 2 * p.h, nvalid);
-                            }
-                        }
-                        tmem_ld32f(tacc + j, v);  // dA' = dy W2_e
-                        if (nvalid > 0) {
-                            // 8 columns at a time: dA = w dA'; da = dA b SiLU'(a);
-                            // db = dA SiLU(a); A' = w SiLU(a) b; packed straight into
-                            // the three boxes.
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                float a8[8], b8[8], da8[8], db8[8], ap8[8];
-                                unpack8(ua[c], a8);
-                                unpack8(ub[c], b8);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const float vk = v[8 * c + i];
-                                    const float sg = __fdividef(1.f, 1.f + __expf(-a8[i]));
-                                    const float si = a8[i] * sg;
-                                    const float Av = si * b8[i];
-                                    dsum = fmaf(vk, Av, dsum);
-                                    const float dA = w * vk;
-                                    da8[i] = dA * b8[i] * (sg + a8[i] * sg * (1.f - sg));
-                                    db8[i] = dA * si;
-                                    ap8[i] = w * Av;
-                                }
-                                uint4 u;
-                                u.x = pack_bf16(da8[0], da8[1]); u.y = pack_bf16(da8[2], da8[3]);
-                                u.z = pack_bf16(da8[4], da8[5]); u.w = pack_bf16(da8[6], da8[7]);
-                                *reinterpret_cast<uint4*>(box_da + box_off(lane, c)) = u;
-                                u.x = pack_bf16(db8[0], db8[1]); u.y = pack_bf16(db8[2], db8[3]);
-                                u.z = pack_bf16(db8[4], db8[5]); u.w = pack_bf16(db8[6], db8[7]);
-                                *reinterpret_cast<uint4*>(box_db + box_off(lane, c)) = u;
-                                u.x = pack_bf16(ap8[0], ap8[1]); u.y = pack_bf16(ap8[2], ap8[3]);
-                                u.z = pack_bf16(ap8[4], ap8[5]); u.w = pack_bf16(ap8[6], ap8[7]);
-                                *reinterpret_cast<uint4*>(box_ap + box_off(lane, c)) = u;
-                            }
-                            box_store_rows(box_da, lane, dHw + j, 2 * p.h, nvalid);
-                            box_store_rows(box_db, lane, dHw + p.h + j, 2 * p.h, nvalid);
-                            box_store_rows(box_ap, lane, Apw + j, p.h, nvalid);
-                        }
+                    if (refill) ++hissued;
+                    if (nvalid < 32) {
+                        box_store_rows(box_a, lane, dHw + 32 * jj, hs, nvalid);
+                        if constexpr (KIND == G3_DH)
+                            box_store_rows(box_b, lane, dHw + p.h + 32 * jj, hs, nvalid);
+                        box_store_rows(box_ap, lane, Apw + 32 * jj, p.h, nvalid);
                     }
                 }
-                if (valid) p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
+                if (jj < hn) {  // gave up: let this warp's loads in flight land
+                    for (int k = jj; k < hissued; ++k)
+                        mbar_drain(h_bar(hc + k), ((hc + k) / kHR) & 1u);
+                    stop = true;
+                } else if (valid) {
+                    p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
+                }
+                hc += hn;
             } else if constexpr (KIND == G4_DW2) {
                 // dW2_e [d, h]: the warp's 32 rows x 32 columns at a time go through
                 // a shared-memory box and one TMA store (whole lines, asynchronous).
@@ -872,6 +913,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                 }
             }
+            if (stop) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -1245,9 +1287,13 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             max_tiles = (s.T / bmc + s.E) * prm.n_tiles;
             break;
         case G3_DH:  // A = dy gathered; B = W2 [E*d, h] read MN-major
+            // Epilogue: H [TK, hs] loaded and dH [TK, hs], A' [TK, h] stored in
+            // 32 x 32 boxes with the 64-byte swizzle of its shared staging boxes.
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, 64);
-            mp.a = mp.b1 = mp.o = mp.b0;
+            ok &= make_tmap_bf16(&mp.a, g.aux0, TK, hs, 32, 32, 64);
+            ok &= make_tmap_bf16(&mp.o, g.out0, TK, hs, 32, 32, 64);
+            ok &= make_tmap_bf16(&mp.b1, g.out1, TK, h, 32, 32, 64);
             prm.Kdim = s.d;
             prm.n_tiles = (s.h + BN - 1) / BN;
             max_tiles = vm_mtiles * prm.n_tiles;
@@ -1255,7 +1301,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
         case G4_DW2:  // A = dy gathered (MN-major, M = d); B = A' rows [TK, h]; TMA-stored dW2
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, h, 64, 64);
-            ok &= make_tmap_bf16(&mp.o, g.out0, E * d, h, 32, 32, false);
+            ok &= make_tmap_bf16(&mp.o, g.out0, E * d, h, 32, 32, 0);
             mp.a = mp.b1 = mp.b0;
             prm.M = s.d;
             prm.n_tiles = (s.h + BN - 1) / BN;
@@ -1264,8 +1310,8 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
         case G5_DW13:  // A = x gathered (MN-major, M = d); B = dH rows [TK, hs]; TMA-stored
             prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, TK, hs, 64, 64);
-            ok &= make_tmap_bf16(&mp.o, g.out0, E * h, d, 32, 32, false);  // dW1
-            if (gated) ok &= make_tmap_bf16(&mp.b1, g.out1, E * h, d, 32, 32, false);  // dW3
+            ok &= make_tmap_bf16(&mp.o, g.out0, E * h, d, 32, 32, 0);  // dW1
+            if (gated) ok &= make_tmap_bf16(&mp.b1, g.out1, E * h, d, 32, 32, 0);  // dW3
             else mp.b1 = mp.o;
             mp.a = mp.b0;
             prm.M = s.d;
