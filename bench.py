@@ -363,13 +363,13 @@ def main():
 
     fwd = B.moe_forward_slotwise if args.combine == "slotwise" else B.moe_forward
 
-    def step(x, dy):
+    def step(x, dy, y=y, dx=grads["dx"]):
         B.moe_route(L.s, x, dv["Wg"], bias, r.logits, r.ids, r.w, L.ws)
         B.moe_build_dispatch(L.s, r.ids, dp.eti, dp.offsets, dp.tim, L.ws)
         fwd(L.s, x, dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti, dp.offsets, dp.tim, y, H,
             L.ws)
         B.moe_backward(L.s, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r.ids, r.w, dp.eti,
-                       dp.offsets, dp.tim, H, grads["dx"], grads["dWg"], grads["dW1"],
+                       dp.offsets, dp.tim, H, dx, grads["dWg"], grads["dW1"],
                        grads["dW3"], grads["dW2"], grads["dS"], L.ws)
 
     rows_of_step = None
@@ -391,7 +391,7 @@ def main():
         H = torch.empty(cap, L.hs, dtype=torch.bfloat16, device=dev)
         dS_row = torch.empty(cap, dtype=torch.float32, device=dev)
 
-        def step(x, dy):  # noqa: F811
+        def step(x, dy, y=y, dx=grads["dx"]):  # noqa: F811
             B.moe_route(L.s, x, dv["Wg"], bias, r.logits, r.ids, r.w, L.ws)
             B.moe_build_dispatch(L.s, r.ids, dp.eti, dp.offsets, dp.tim, L.ws)
             B.moe_token_rounding(L.s, m, r.logits, r.ids, dp.eti, dp.offsets, rr.eti, rr.offsets,
@@ -400,7 +400,7 @@ def main():
                                rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, y, H, rows_ws)
             B.moe_backward_rows(L.s, cap, dy, x, dv["Wg"], dv["W1"], dv["W3"], dv["W2"], rr.eti,
                                 rr.offsets, rr.w_row, rr.tok_off, rr.tok_exp, rr.tok_rows, H,
-                                grads["dx"], grads["dWg"], grads["dW1"], grads["dW3"],
+                                dx, grads["dWg"], grads["dW1"], grads["dW3"],
                                 grads["dW2"], dS_row, rows_ws)
 
     # ---- memory: activation bytes of one fwd+bwd beyond inputs/weights/grads/outputs
@@ -421,7 +421,9 @@ def main():
               "workspace_fwd_bytes": ws_f, "workspace_bwd_bytes": ws_b,
               "peak_activation_bytes": saved + max(ws_f, ws_b),
               "peak_activation_over_routed": (saved + max(ws_f, ws_b)) / routed_bytes,
-              "combine_chunk_bytes": B.moe_chunk_tokens(L.s) * s.K * s.d * 2,
+              # the down-projection chunk buffer (plus the segment table): the
+              # forward workspace beyond the [rows, h] SwiGLU output
+              "fwd_workspace_beyond_swiglu_output_bytes": ws_f - TK * s.h * 2,
               "allocator_peak_delta_bytes": torch.cuda.max_memory_allocated(dev) - base_alloc}
 
     # ---- device-resident timing
@@ -496,35 +498,84 @@ def main():
                                 "launches_per_step": sum(per_kernel[n][0] for n in names
                                                          if n in per_kernel) / args.steps}
 
-    # ---- end to end: host buffers in, results out, through the same C ABI calls
+    # ---- end to end: host buffers in, results out, through the same C ABI calls.
+    # Every step copies its inputs from pinned host memory and its results back;
+    # the copies run on two copy streams with double-buffered device inputs and
+    # outputs, so step i+1's upload and step i's download overlap step i's (and
+    # i+1's) compute, as an input pipeline would. The region is timed from an
+    # event before the first upload to one after the last download.
     xh = inp["x"].pin_memory()
     dyh = inp["dO"].pin_memory()
-    yh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
-    dxh = torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(dv["x"])
-    dyd = torch.empty_like(dv["dO"])
+    yh = [torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dxh = [torch.empty(s.T, s.d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(dv["x"]) for _ in range(2)]
+    dyd = [torch.empty_like(dv["dO"]) for _ in range(2)]
+    yd = [y, torch.empty_like(y)]
+    dxd = [grads["dx"], torch.empty_like(grads["dx"])]
+    up = torch.cuda.Stream(dev)
+    down = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        dyd.copy_(dyh, non_blocking=True)
-        step(xd, dyd)
-        yh.copy_(y, non_blocking=True)
-        dxh.copy_(grads["dx"], non_blocking=True)
+    def ev():
+        return torch.cuda.Event()
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def e2e_run(n):
+        in_ready = [None, None]
+        in_free = [None, None]   # the step that read buffer b finished
+        out_ready = [None, None]
+        out_free = [None, None]  # the download of buffer b finished
+
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if in_free[b] is not None:
+                    up.wait_event(in_free[b])
+                xd[b].copy_(xh, non_blocking=True)
+                dyd[b].copy_(dyh, non_blocking=True)
+                in_ready[b] = ev()
+                in_ready[b].record(up)
+
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            st.wait_event(in_ready[b])
+            if out_free[b] is not None:
+                st.wait_event(out_free[b])
+            step(xd[b], dyd[b], yd[b], dxd[b])
+            in_free[b] = ev()
+            in_free[b].record(st)
+            out_ready[b] = in_free[b]
+            with torch.cuda.stream(down):
+                down.wait_event(out_ready[b])
+                yh[i % 2].copy_(yd[b], non_blocking=True)
+                dxh[i % 2].copy_(dxd[b], non_blocking=True)
+                out_free[b] = ev()
+                out_free[b].record(down)
+        for e in out_free:
+            if e is not None:
+                st.wait_event(e)
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize(dev)
     barrier(world)
+    up.wait_stream(st)
+    down.wait_stream(st)
     e0.record(st)
-    for _ in range(args.steps):
-        e2e_step()
+    up.wait_event(e0)
+    e2e_run(args.steps)
     e1.record(st)
     torch.cuda.synchronize(dev)
     barrier(world)
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    # The last step's downloaded results are the device results.
+    last = (args.steps - 1) % 2
+    if not (torch.equal(yh[last], yd[last].cpu()) and torch.equal(dxh[last], dxd[last].cpu())):
+        raise RuntimeError("end-to-end results differ from the device buffers")
     e2e = {"value": world * s.T * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
            "h2d_bytes_per_step": xh.numel() * 2 + dyh.numel() * 2,
-           "d2h_bytes_per_step": yh.numel() * 2 + dxh.numel() * 2}
+           "d2h_bytes_per_step": yh[0].numel() * 2 + dxh[0].numel() * 2,
+           "copies": "two copy streams, double-buffered inputs and outputs"}
     L.check_error()
 
     # ---- routing statistics
@@ -562,12 +613,13 @@ def main():
 
 
 def source_hash() -> str:
+    """Hash of the sources that define the GEMM kernels and their launches (the
+    kernels whose DRAM traffic profiles/traffic.json records)."""
     import hashlib
     h = hashlib.sha1()
-    for f in sorted(os.listdir(os.path.join(ROOT, "token_dispatch_grouped_gb300", "csrc"))):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(ROOT, "token_dispatch_grouped_gb300", "csrc", f), "rb") as fh:
-                h.update(fh.read())
+    for f in ("api.cu", "common.cuh", "gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "token_dispatch_grouped_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:12]
 
 

@@ -95,6 +95,34 @@ def test_layer_small_full_parity(s):
         assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
 
 
+# Column passes: small layers split the down projection and dX into two column
+# passes, larger ones into four. Forcing four passes on a small layer covers that
+# path too; both runs sum every output element over the same k order, so they
+# agree far inside the layer tolerance.
+@pytest.mark.parametrize("s", [I.Shape(1100, 512, 8, 2, 256), I.Shape(1100, 512, 8, 2, 768, "relu")],
+                         ids=_sid)
+def test_column_pass_count_is_bit_identical(s, monkeypatch):
+    inp = I.make_layer_inputs(s, seed=4)
+    dv = to_dev(inp)
+    L = _layer(s)
+    outs = []
+    for passes in ("2", "4"):
+        monkeypatch.setenv("MOE_COLUMN_PASSES", passes)
+        r, dp, y, H, g = L.step(dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], dv["dO"])
+        L.check_error()
+        outs.append((y, g["dx"], g["dS"], g["dWg"]))
+    monkeypatch.delenv("MOE_COLUMN_PASSES")
+    for a, b in zip(*outs):
+        assert rel_fro(cpu(b), cpu(a).astype(np.float64)) <= 1e-3
+    ids, w = cpu(r.ids), cpu(r.w)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w, s.expert)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f,
+                         s.expert)
+    for (y, dx, _, _) in outs:
+        assert rel_fro(cpu(y), f["y"]) <= TOL_BF16
+        assert rel_fro(cpu(dx), b["dx"]) <= TOL_BF16
+
+
 # Slot-wise forward (combine fused into the down projection): ragged tiles, K = 1
 # (no accumulator), K = E = 8, CTA-pair shapes and a non-gated expert.
 SLOTWISE = [I.Shape(300, 256, 6, 3, 512), I.Shape(1500, 128, 16, 1, 256),

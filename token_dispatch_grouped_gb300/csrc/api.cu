@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -107,7 +108,8 @@ int nchunks_of(const moe_shape& s, int tc) { return (s.T + tc - 1) / tc; }
 
 // How a down projection (forward) or dX pass (backward) is split so that its
 // transient [rows, columns] output buffer holds at most a quarter of T*K*d
-// once T >= 1024. Splitting by token chunks streams the expert weights once
+// once T >= 1024 (half of it for column passes of small layers, see
+// column_passes). Splitting by token chunks streams the expert weights once
 // per chunk; splitting by output-column chunks streams the activation
 // operand once per chunk instead. The split that re-reads fewer bytes wins.
 struct Plan {
@@ -117,41 +119,55 @@ struct Plan {
     int dc;        // columns per column chunk
 };
 
+// Column passes over `rows` routed rows: two when the half-width buffer
+// (rows x d/2 bf16) is at most 64 MiB, else four. On small layers each pass
+// costs a launch, a pipeline fill, a tail and a short combine launch, and
+// re-streams the whole activation operand, while the buffer saved is small
+// next to the [rows, h] activations the layer holds anyway.
+// MOE_COLUMN_PASSES=2|4 forces one count (read at every call).
+int column_passes(const moe_shape& s, double rows) {
+    const char* f = std::getenv("MOE_COLUMN_PASSES");
+    if (f != nullptr && (f[0] == '2' || f[0] == '4') && f[1] == '\0') return f[0] - '0';
+    return rows * (s.d / 2) * 2.0 <= 64.0 * 1024 * 1024 ? 2 : 4;
+}
+
 // Row mode (a routing given as rows, e.g. after token rounding): a token chunk
 // may hold any number of rows, so passes split columns only (d % 512 == 0) or
 // there is a single pass over all rows.
-Plan make_plan(const moe_shape& s, double weight_bytes, double act_bytes, bool row_mode) {
+Plan make_plan(const moe_shape& s, double rows, double weight_bytes, double act_bytes,
+               bool row_mode) {
     Plan p{1, false, s.T, s.d};
     if (s.T < 1024) return p;
+    const bool cols_ok = s.d % (4 * 128) == 0;
     if (row_mode) {
-        if (s.d % (4 * 128) == 0) {
-            p.n = 4;
+        if (cols_ok) {
+            p.n = column_passes(s, rows);
             p.by_cols = true;
-            p.dc = s.d / 4;
+            p.dc = s.d / p.n;
         }
         return p;
     }
-    p.n = 4;
     p.tc = moe_chunk_tokens(s);
     p.n = nchunks_of(s, p.tc);
-    const bool cols_ok = s.d % (4 * 128) == 0;
     if (cols_ok && act_bytes < weight_bytes) {
-        p.n = 4;
+        p.n = column_passes(s, rows);
         p.by_cols = true;
         p.tc = s.T;
-        p.dc = s.d / 4;
+        p.dc = s.d / p.n;
     }
     return p;
 }
 
 // rows: row capacity of the routing (T*K for a top-K routing).
 Plan plan_down(const moe_shape& s, size_t rows, bool row_mode) {
-    return make_plan(s, 2.0 * s.E * s.d * s.h, 2.0 * static_cast<double>(rows) * s.h, row_mode);
+    return make_plan(s, static_cast<double>(rows), 2.0 * s.E * s.d * s.h,
+                     2.0 * static_cast<double>(rows) * s.h, row_mode);
 }
 
 Plan plan_dx(const moe_shape& s, size_t rows, bool row_mode) {
     const double hs = static_cast<double>(hs_of(s));
-    return make_plan(s, 2.0 * s.E * s.d * hs, 2.0 * static_cast<double>(rows) * hs, row_mode);
+    return make_plan(s, static_cast<double>(rows), 2.0 * s.E * s.d * hs,
+                     2.0 * static_cast<double>(rows) * hs, row_mode);
 }
 
 size_t chunk_buffer_elems(const moe_shape& s, const Plan& p, size_t rows, bool row_mode) {
