@@ -62,6 +62,9 @@ def memory_kernel_bytes(s) -> dict:
                      2 * TK * 4 + 2 * TK * 4 + (E + 1) * 4),
         "combine": (("combine",), TK * d * 2 + TK * 8 + T * d * 2),
         "dx_combine": (("dx_combine",), TK * d * 2 + TK * 8 + T * d * 2),
+        # router weight gradient: x read once, dz and the row lists, dW_g written
+        "router_dwg": (("router_dwg", "router_dwg_zero", "router_dwg_scatter", "router_dwg_mma",
+                        "router_dwg_reduce"), T * d * 2 + TK * 12 + E * d * 4),
     }
 
 

@@ -123,6 +123,41 @@ def test_column_pass_count_is_bit_identical(s, monkeypatch):
         assert rel_fro(cpu(dx), b["dx"]) <= TOL_BF16
 
 
+# Router weight gradient on the tensor cores (the library takes it once x exceeds
+# 64 MiB): forced on small shapes -- one token chunk and several, E = K, K = 1 (dz = 0),
+# CTA pairs, E = 160 (a partial second N tile) -- against the oracle and against the
+# gathered per-expert path, which sums the same products in another order.
+DWG = [I.WORKLOADS["tiny"], I.Shape(300, 256, 6, 3, 384), I.Shape(129, 384, 8, 8, 128),
+       I.Shape(1500, 128, 16, 1, 256), I.Shape(2100, 512, 4, 2, 512),
+       I.Shape(700, 256, 160, 6, 256)]
+
+
+@pytest.mark.parametrize("s", DWG, ids=_sid)
+def test_router_dwg_tensor_core_path(s, monkeypatch):
+    inp = I.make_layer_inputs(s, seed=6)
+    dv = to_dev(inp)
+    out = {}
+    for path in ("gather", "mma"):
+        monkeypatch.setenv("MOE_ROUTER_DWG", path)
+        L = _layer(s)  # the backward workspace follows the path
+        r, dp, y, H, g = L.step(dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], dv["dO"])
+        L.check_error()
+        out[path] = (r, g)
+    monkeypatch.delenv("MOE_ROUTER_DWG")
+    r, g = out["mma"]
+    dwg = cpu(g["dWg"])
+    if s.K == 1:
+        assert np.all(dwg == 0.0)
+        return
+    ids, w = cpu(r.ids), cpu(r.w)
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids, w, s.expert)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], ids, w, f,
+                         s.expert)
+    assert rel_fro(dwg, b["dWg"]) <= TOL_BF16
+    assert rel_fro(dwg, cpu(out["gather"][1]["dWg"]).astype(np.float64)) <= 1e-4
+    assert np.abs(dwg.sum(axis=0)).max() <= 1e-3 * np.abs(dwg).max()  # sum_k dz_k = 0
+
+
 # Slot-wise forward (combine fused into the down projection): ragged tiles, K = 1
 # (no accumulator), K = E = 8, CTA-pair shapes and a non-gated expert.
 SLOTWISE = [I.Shape(300, 256, 6, 3, 512), I.Shape(1500, 128, 16, 1, 256),

@@ -119,6 +119,32 @@ def test_layer_on_rounded_routing(s):
     assert rel_fro(cpu(g["dS_row"])[:N], ds_ref) <= TOL_BF16
 
 
+def test_router_dwg_paths_on_rounded_routing(monkeypatch):
+    """The router weight gradient of the row-format backward by the tensor-core
+    path (forced) agrees with the gathered path and with the oracle."""
+    s = I.Shape(1000, 256, 8, 2, 256)
+    inp = I.make_layer_inputs(s, seed=3)
+    dv = to_dev(inp)
+    L = _layer(s)
+    r = L.route(dv["x"], dv["Wg"])
+    dp = L.dispatch(r.ids)
+    rr = L.round_tokens(r.logits, r, dp, m_tile=64)
+    dwg = {}
+    for path in ("gather", "mma"):
+        monkeypatch.setenv("MOE_ROUTER_DWG", path)
+        y, H = L.forward_rows(dv["x"], dv["W1"], dv["W3"], dv["W2"], rr)
+        g = L.backward_rows(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], rr, H)
+        L.check_error()
+        dwg[path] = cpu(g["dWg"]).astype(np.float64)
+    monkeypatch.delenv("MOE_ROUTER_DWG")
+    final, w, off = _gpu_sets(rr, s.T, s.E)
+    f = TR.layer_forward_sets(inp["x"], inp["W1"], inp["W3"], inp["W2"], final, w, s.expert)
+    b = TR.layer_backward_sets(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"],
+                               final, w, f, s.expert)
+    assert rel_fro(dwg["mma"], b["dWg"]) <= TOL_BF16
+    assert rel_fro(dwg["mma"], dwg["gather"]) <= 1e-4
+
+
 def test_rounding_is_identity_on_tile_multiples():
     """Every expert chosen by a multiple of M_tile tokens: the rounded routing is
     the token-choice routing and the row layer equals the top-K layer."""

@@ -189,7 +189,11 @@ struct BwdWs {
     __nv_bfloat16* Ap;
     __nv_bfloat16* dH;
     __nv_bfloat16* dXc;
-    float* dwg_part;
+    // router weight gradient on the tensor cores
+    __nv_bfloat16* dwg_B;  // [T, nw] = [dz_hi | dz_lo]
+    int32_t* dwg_iota;     // [T] identity token list
+    Seg* dwg_segs;         // [nchunks] token chunks
+    float* dwg_part;       // [nchunks, d, nw] fp32 partials
 };
 
 size_t layout_fwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, FwdWs* o) {
@@ -224,7 +228,18 @@ size_t layout_bwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, BwdW
     w.dH = c.take<__nv_bfloat16>(rows * hs_of(s));
     w.dXc = c.take<__nv_bfloat16>(
         chunk_buffer_elems(s, plan_dx(s, rows, row_mode), rows, row_mode));
-    w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
+    if (dwg_tensor_cores(s)) {
+        const DwgPlan dp = dwg_plan(s);
+        w.dwg_B = c.take<__nv_bfloat16>(static_cast<size_t>(s.T) * dp.nw);
+        w.dwg_iota = c.take<int32_t>(static_cast<size_t>(s.T));
+        w.dwg_segs = c.take<Seg>(static_cast<size_t>(dp.nchunks));
+        w.dwg_part = c.take<float>(static_cast<size_t>(dp.nchunks) * s.d * dp.nw);
+    } else {
+        w.dwg_B = nullptr;
+        w.dwg_iota = nullptr;
+        w.dwg_segs = nullptr;
+        w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
+    }
     if (o) *o = w;
     return align_up(c.off, 256);
 }
@@ -576,8 +591,29 @@ int backward_impl(const moe_shape& s, const RouteView& rv, const void* dy, const
             MOE_TRY(launch_combine(s, t0, t1, g6.n_off, g6.n_cols, rv.ids, nullptr, rv.tim, sc,
                                    w.dXc, static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
     }
-    MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), rv.eti, rv.offsets,
-                              w.dz_row, w.dwg_part, dWg, err, st));
+    // Router weight gradient dW_g = dz^T x: per-expert gathered sums while x
+    // fits in L2; else the dense [dz_hi | dz_lo] operand, its tensor-core
+    // product with x per token chunk and a fixed-order sum of the chunks.
+    if (!dwg_tensor_cores(s)) {
+        MOE_TRY(launch_router_dwg(s, static_cast<const __nv_bfloat16*>(x), rv.eti, rv.offsets,
+                                  w.dz_row, w.dwg_part, dWg, err, st));
+        return MOE_OK;
+    }
+    const DwgPlan dwp = dwg_plan(s);
+    MOE_TRY(launch_dwg_operand(s, dwp, rows, rv.eti, rv.offsets, w.dz_row, w.dwg_B, w.dwg_iota,
+                               w.dwg_segs, err, st));
+    GemmProblem g7{};
+    g7.kind = G7_DWG;
+    g7.s = s;
+    g7.segs = w.dwg_segs;
+    g7.nseg = dwp.nchunks;
+    g7.eti = w.dwg_iota;
+    g7.a_src = x;
+    g7.b_src0 = w.dwg_B;
+    g7.out0 = w.dwg_part;
+    g7.err = err;
+    MOE_TRY(launch_gemm(g7, st));
+    MOE_TRY(launch_dwg_reduce(s, dwp, w.dwg_part, dWg, err, st));
     return MOE_OK;
 }
 

@@ -3,6 +3,8 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -116,9 +118,42 @@ cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, c
 cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
                              float* dz_row, int* err, cudaStream_t st);
+// Router weight gradient dW_g = dz^T x (R2b), gathered per expert (x rows
+// read through eti, fp32 sums over 32 row parts of each expert, then a
+// fixed-order sum): used while x fits in L2.
 int dwg_parts();
 cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
                               const int32_t* offsets, const float* dz_row, float* part,
+                              float* dWg, int* err, cudaStream_t st);
+// Whether the router weight gradient runs on the tensor cores: once x
+// (T*d bf16) exceeds 64 MiB, so that reading it K times costs HBM traffic.
+// MOE_ROUTER_DWG=mma|gather forces one path (read at every call; the
+// workspace size follows it).
+inline bool dwg_tensor_cores(const moe_shape& s) {
+    const char* f = std::getenv("MOE_ROUTER_DWG");
+    if (f != nullptr && std::strcmp(f, "mma") == 0) return true;
+    if (f != nullptr && std::strcmp(f, "gather") == 0) return false;
+    return static_cast<long long>(s.T) * s.d * 2 > (64ll << 20);
+}
+// Router weight gradient dW_g = dz^T x (R2b) as a tensor-core product: the
+// dense operand B = [dz_hi | dz_lo] [T, nw] (bf16 parts of dz at each token's
+// experts, zeros elsewhere; nw = 2 * e_pad), x^T B over token chunks into fp32
+// partials [nchunks, d, nw], then a fixed-order sum. dwg_plan (gemm.cu) sizes it.
+struct DwgPlan {
+    int e_pad;    // experts padded to a multiple of 64
+    int nw;       // columns of B: 2 * e_pad
+    int nchunks;  // token chunks (split of the reduction over T)
+    int chunk;    // tokens per chunk (multiple of 64)
+};
+DwgPlan dwg_plan(const moe_shape& s);
+// Writes B (zeros, then hi/lo of dz_row[r] at (eti[r], expert of r) for every
+// routed row r < offsets[E]), the identity token list and the chunk segments.
+cudaError_t launch_dwg_operand(const moe_shape& s, const DwgPlan& dp, int rows_cap,
+                               const int32_t* eti, const int32_t* offsets, const float* dz_row,
+                               __nv_bfloat16* B, int32_t* iota, Seg* segs, int* err,
+                               cudaStream_t st);
+// dWg [E, d] = sum over chunks p of part[p][c][e] + part[p][c][e_pad + e], p ascending.
+cudaError_t launch_dwg_reduce(const moe_shape& s, const DwgPlan& dp, const float* part,
                               float* dWg, int* err, cudaStream_t st);
 
 // gemm.cu — the grouped tcgen05 GEMMs.
@@ -128,7 +163,10 @@ enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_D
                 G1_UP_ACT = 6, G3_DH_ACT = 7,
                 // Down projection of one routing slot with the combine fused
                 // into its epilogue (slot-wise forward).
-                G2_SLOT = 8 };
+                G2_SLOT = 8,
+                // Router weight gradient partials: x^T [dz_hi | dz_lo] over token
+                // chunks (the chunks take the place of the experts), fp32 out.
+                G7_DWG = 9 };
 
 struct GemmProblem {
     GemmKind kind;
@@ -153,6 +191,9 @@ struct GemmProblem {
     const int32_t* tim = nullptr;
     int slot = 0;
     int rows = 0;             // row capacity of the routed-row arrays (0: T*K)
+    // G7_DWG: segs = token chunks (nseg of them), eti = identity list, a_src = x,
+    // b_src0 = [dz_hi | dz_lo] [T, nw], out0 = fp32 partials [nseg * d, nw].
+    int nseg = 0;
     int* err;
 };
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t st);

@@ -89,6 +89,7 @@ template <> struct Tr<G6_DX>   { static constexpr bool VK = false; static conste
 template <> struct Tr<G1_UP_ACT> : Tr<G1_UP> {};
 template <> struct Tr<G2_SLOT> : Tr<G1_UP> {};  // gathered K-major A, K-major B
 template <> struct Tr<G3_DH_ACT> : Tr<G3_DH> {};
+template <> struct Tr<G7_DWG> : Tr<G4_DW2> {};  // gathered x (MN-major A), B rows MN-major
 
 template <int BN, int CTAS, int EPI_BOXES = 2>
 struct Cfg {
@@ -479,7 +480,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 if (leader && lane == 0) {
                     uint32_t bytes = CTAS * TMA_BYTES;
                     if constexpr (KIND == G3_DH || KIND == G3_DH_ACT || KIND == G4_DW2 ||
-                                  KIND == G5_DW13) {
+                                  KIND == G5_DW13 || KIND == G7_DWG) {
                         // h need not be a multiple of BN: 64-column B boxes that
                         // start at or past h are not loaded (their output columns
                         // are never stored).
@@ -532,8 +533,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
                     if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.e * p.d + k0);
-                } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13) {
-                    // B rows of this expert (A' for dW2, dH for dW1/dW3), MN-major.
+                } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13 || KIND == G7_DWG) {
+                    // B rows of this expert (A' for dW2, dH for dW1/dW3; the chunk's
+                    // rows of [dz_hi | dz_lo] for the router gradient), MN-major.
                     if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
                         load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.lo + k0);
                 } else {  // G6: K = 2h, first h from W1, then W3 (non-gated: K = h, W1).
@@ -881,6 +883,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         bulk_commit_group();
                     }
                 }
+            } else if constexpr (KIND == G7_DWG) {
+                // Router-gradient partial of token chunk t.e: fp32 rows
+                // t.e * d + m of [nseg * d, nw], each lane its own row, 128
+                // contiguous bytes per 32 columns.
+                const bool empty = t.hi <= t.lo;
+                const int n0 = t.n_blk * BN;
+                const int ncols = min(BN, p.h - n0);  // the last N tile may be partial
+                float* orow = static_cast<float*>(p.out0) +
+                              (static_cast<size_t>(t.e) * p.d + mbase + q * 32 + lane) * p.ldo + n0;
+#pragma unroll 1
+                for (int j = 0; j < ncols; j += 32) {
+                    if (empty) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    } else {
+                        tmem_ld32f(tacc + j, v);
+                    }
+                    float4* dst = reinterpret_cast<float4*>(orow + j);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
             } else {  // G5: tile of (x^T dH)_e [d, 2h]; transposed into dW1/dW3 [h, d]
                 // The warp's 32 d-rows x 32 n-columns are written transposed into
                 // a shared-memory box [n][m] and stored with one TMA store into
@@ -1194,7 +1218,7 @@ cudaError_t launch_ctas(int ctas, int BN, const Maps& mp, const Params& prm, int
 // wherever it is legal.
 int choose_ctas(GemmKind kind, const moe_shape& s) {
     static const char* force = std::getenv("MOE_GEMM_CTAS");
-    const bool vk = kind == G4_DW2 || kind == G5_DW13;
+    const bool vk = kind == G4_DW2 || kind == G5_DW13 || kind == G7_DWG;
     const bool ok2 = vk ? (s.d % 256 == 0) : true;
     if (force != nullptr && (force[0] == '1' || force[0] == '2'))
         return (force[0] == '2' && ok2) ? 2 : 1;
@@ -1216,8 +1240,30 @@ int gemm_bn(GemmKind kind, const moe_shape& s) {
         case G3_DH:
         case G4_DW2:
         case G5_DW13: return s.h >= 256 ? 256 : 128;  // the last N tile (of a half) may be partial
+        case G7_DWG: return dwg_plan(s).nw >= 256 ? 256 : 128;
+        default: break;
     }
     return 128;
+}
+
+// Router-gradient split: B has nw = 2 * e_pad columns; the token range is cut
+// into chunks (multiples of 64 tokens, at least 256 unless T is smaller, at
+// most about 8192) so that the tile count is at least about 152 (two waves of
+// CTA pairs on a 152-SM GB300) and no tile's reduction runs much past 128
+// k-blocks. The split depends on the shape alone, so workspace sizes need no
+// device.
+DwgPlan dwg_plan(const moe_shape& s) {
+    DwgPlan p{};
+    p.e_pad = (s.E + 63) / 64 * 64;
+    p.nw = 2 * p.e_pad;
+    const int bn = p.nw >= 256 ? 256 : 128;
+    const int bmc = (s.d % 256 == 0) ? 256 : 128;  // CTA pairs when d % 256 == 0
+    const int tiles_per_chunk = (s.d / bmc) * ((p.nw + bn - 1) / bn);
+    int n = std::max((152 + tiles_per_chunk - 1) / tiles_per_chunk, (s.T + 8191) / 8192);
+    n = std::max(1, std::min(n, s.T / 256));
+    p.chunk = ((s.T + n - 1) / n + 63) / 64 * 64;
+    p.nchunks = (s.T + p.chunk - 1) / p.chunk;
+    return p;
 }
 
 cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
@@ -1319,6 +1365,19 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             prm.n_tiles = (gated ? 2 : 1) * prm.n_half;
             max_tiles = s.E * (s.d / bmc) * prm.n_tiles;
             break;
+        case G7_DWG: {  // A = x rows (identity list); B = [dz_hi | dz_lo] [T, nw]; fp32 partials
+            const int nw = dwg_plan(s).nw;
+            prm.gsrc = static_cast<const __nv_bfloat16*>(g.a_src);
+            ok &= make_tmap_bf16(&mp.b0, g.b_src0, static_cast<uint64_t>(s.T), nw, 64, 64);
+            mp.a = mp.b1 = mp.o = mp.b0;
+            prm.E = g.nseg;  // token chunks in place of experts
+            prm.h = nw;
+            prm.ldo = nw;
+            prm.M = s.d;
+            prm.n_tiles = (nw + BN - 1) / BN;
+            max_tiles = g.nseg * (s.d / bmc) * prm.n_tiles;
+            break;
+        }
         case G6_DX:  // A = dH rows [TK, hs]; B = W1 | W3 [E*h, d] (or W1) read MN-major
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, hs, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * h, d, 64, 64);
@@ -1345,6 +1404,9 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
         case G4_DW2: return launch_ctas<G4_DW2>(ctas, BN, mp, prm, max_tiles, st, "g4_dw2");
         case G5_DW13: return launch_ctas<G5_DW13>(ctas, BN, mp, prm, max_tiles, st, "g5_dw13");
         case G6_DX: return launch_ctas<G6_DX>(ctas, BN, mp, prm, max_tiles, st, "g6_dx");
+        case G7_DWG:
+            return launch_ctas<G7_DWG>(ctas, BN, mp, prm, max_tiles, st, "router_dwg_mma");
+        default: break;
     }
     return cudaErrorInvalidValue;
 }

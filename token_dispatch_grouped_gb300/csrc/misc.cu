@@ -16,8 +16,17 @@
 //                   dz_{t,k} W_g[e_{t,k}] (added in the dX GEMM's epilogue).
 //                   MoEBlaze paper notes 3.2 (token gradient accumulation over
 //                   the K routed rows).
-//   router_dwg(R2b) dW_g = dz^T x as per-expert sums over the expert's rows
-//                   (partials over 32 row parts, then a fixed-order sum).
+//   router_dwg(R2b) dW_g = dz^T x, two ways. Per-expert sums over the
+//                   expert's rows (x rows gathered, partials over 32 row parts,
+//                   then a fixed-order sum) while x fits in L2 (T*d*2 <= 64 MiB).
+//                   Larger layers: on the tensor cores, dz split into two
+//                   bf16 parts (hi = bf16(dz), lo = bf16(dz - hi), together
+//                   about 16 mantissa bits) scattered into a dense operand
+//                   B = [dz_hi | dz_lo] [T, 2 e_pad] (zeros where a token did
+//                   not choose the expert); the grouped GEMM kind G7_DWG forms
+//                   x^T B per token chunk in fp32, and dwg_reduce adds the chunk
+//                   partials and the two parts in a fixed order. x is read once
+//                   (a per-expert gather would read each token row K times).
 // All sums run in a fixed order, so results are bit-reproducible.
 #include <algorithm>
 
@@ -365,6 +374,82 @@ __global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
     dWg[i] = s;
 }
 
+// Router-gradient operand: zero B [T, nw] (16-byte pieces), the identity
+// token list and the chunk segments (chunk c = tokens [c * chunk, ...)).
+__global__ void dwg_zero_kernel(int T, int nw, int chunk, int nseg, uint4* __restrict__ B,
+                                int32_t* __restrict__ iota, Seg* __restrict__ segs, int* err) {
+    if (has_error(err)) return;
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const size_t n16 = static_cast<size_t>(T) * nw / 8;
+    for (size_t i = i0; i < n16; i += stride) B[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (size_t t = i0; t < static_cast<size_t>(T); t += stride) iota[t] = static_cast<int32_t>(t);
+    if (blockIdx.x == 0)
+        for (int c = threadIdx.x; c < nseg; c += blockDim.x) {
+            Seg sg;
+            sg.lo = c * chunk;
+            sg.hi = min(T, (c + 1) * chunk);
+            sg.out = 0;
+            sg.pad = 0;
+            segs[c] = sg;
+        }
+}
+
+// Routed row r < offsets[E] of expert e (the last e with offsets[e] <= r) and
+// token t = eti[r]: B[t][e] = bf16(dz_r), B[t][e_pad + e] = bf16(dz_r - that).
+// A token meets an expert at most once, so every element has one writer.
+__global__ void dwg_scatter_kernel(int rows_cap, int E, int e_pad, int nw,
+                                   const int32_t* __restrict__ eti,
+                                   const int32_t* __restrict__ offsets,
+                                   const float* __restrict__ dz_row, __nv_bfloat16* __restrict__ B,
+                                   int* err) {
+    if (has_error(err)) return;
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows_cap || r >= offsets[E]) return;
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= r) lo = mid;
+        else hi = mid;
+    }
+    const float z = dz_row[r];
+    const __nv_bfloat16 zh = __float2bfloat16_rn(z);
+    const __nv_bfloat16 zl = __float2bfloat16_rn(z - __bfloat162float(zh));
+    __nv_bfloat16* row = B + static_cast<size_t>(eti[r]) * nw;
+    row[lo] = zh;
+    row[e_pad + lo] = zl;
+}
+
+// dW_g[e][c] = sum over chunks p (ascending) of part[p][c][e] + part[p][c][e_pad + e].
+// Block (32, 8) owns 32 experts x 32 columns: reads run along e, the tile is
+// transposed in shared memory so the writes run along c.
+__global__ void __launch_bounds__(256)
+dwg_reduce_kernel(int d, int E, int e_pad, int nw, int nseg, const float* __restrict__ part,
+                  float* __restrict__ dWg, int* err) {
+    if (has_error(err)) return;
+    __shared__ float tile[32][33];
+    const int e0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int c = c0 + ty * 4 + j, e = e0 + tx;
+        float acc = 0.f;
+        if (c < d && e < E)
+            for (int q = 0; q < nseg; ++q) {
+                const float* row = part + (static_cast<size_t>(q) * d + c) * nw;
+                acc += row[e];
+                acc += row[e_pad + e];
+            }
+        tile[ty * 4 + j][tx] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int e = e0 + ty * 4 + j, c = c0 + tx;
+        if (e < E && c < d) dWg[static_cast<size_t>(e) * d + c] = tile[tx][ty * 4 + j];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchunks,
@@ -465,6 +550,35 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
     const int n = s.E * s.d;
     LaunchScope ls("router_dwg_reduce", st);
     router_dwg_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, part, dWg, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dwg_operand(const moe_shape& s, const DwgPlan& dp, int rows_cap,
+                               const int32_t* eti, const int32_t* offsets, const float* dz_row,
+                               __nv_bfloat16* B, int32_t* iota, Seg* segs, int* err,
+                               cudaStream_t st) {
+    {
+        LaunchScope ls("router_dwg_zero", st);
+        const size_t n16 = static_cast<size_t>(s.T) * dp.nw / 8;
+        const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256,
+                                                           static_cast<size_t>(num_sms()) * 8));
+        dwg_zero_kernel<<<std::max(1, grid), 256, 0, st>>>(s.T, dp.nw, dp.chunk, dp.nchunks,
+                                                           reinterpret_cast<uint4*>(B), iota,
+                                                           segs, err);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    LaunchScope ls("router_dwg_scatter", st);
+    dwg_scatter_kernel<<<(rows_cap + 255) / 256, 256, 0, st>>>(rows_cap, s.E, dp.e_pad, dp.nw,
+                                                               eti, offsets, dz_row, B, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dwg_reduce(const moe_shape& s, const DwgPlan& dp, const float* part,
+                              float* dWg, int* err, cudaStream_t st) {
+    LaunchScope ls("router_dwg_reduce", st);
+    dwg_reduce_kernel<<<dim3((s.d + 31) / 32, (s.E + 31) / 32), dim3(32, 8), 0, st>>>(
+        s.d, s.E, dp.e_pad, dp.nw, dp.nchunks, part, dWg, err);
     return cudaGetLastError();
 }
 
