@@ -133,3 +133,36 @@ def test_row_routing_entry_points_host_checks():
         B.MOE_ERR_INVALID_ARG
     assert B.LIB.moe_backward_rows(s, cap, *([None] * 20), 0, None) == B.MOE_ERR_INVALID_ARG
     assert B.LIB.moe_forward_slotwise(s, *([None] * 12), 0, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_follows_the_pass_and_router_gradient_rules(monkeypatch):
+    """Column passes (two for small layers, four otherwise, forced by
+    MOE_COLUMN_PASSES) and the router weight-gradient path (tensor cores once x
+    exceeds 64 MiB, forced by MOE_ROUTER_DWG) size the workspaces as documented."""
+    from token_dispatch_grouped_gb300 import binding as B
+    s = B.shape(4096, 4096, 8, 2, 14336)      # Mixtral-shaped: x = 32 MiB
+    TK = 4096 * 2
+    A = TK * 14336 * 2                         # SwiGLU output [TK, h]
+    two = B.moe_workspace_size(s, B.MOE_WS_FORWARD)
+    monkeypatch.setenv("MOE_COLUMN_PASSES", "4")
+    four = B.moe_workspace_size(s, B.MOE_WS_FORWARD)
+    monkeypatch.delenv("MOE_COLUMN_PASSES")
+    assert A + TK * 2048 * 2 <= two < A + TK * 2048 * 2 + 2**20    # half-width chunk
+    assert A + TK * 1024 * 2 <= four < A + TK * 1024 * 2 + 2**20   # quarter-width chunk
+    # router gradient: gathered path (32 row parts per expert) below 64 MiB of x ...
+    gather = B.moe_workspace_size(s, B.MOE_WS_BACKWARD)
+    monkeypatch.setenv("MOE_ROUTER_DWG", "mma")
+    mma = B.moe_workspace_size(s, B.MOE_WS_BACKWARD)
+    monkeypatch.delenv("MOE_ROUTER_DWG")
+    # ... the tensor-core path adds B = [dz_hi | dz_lo] [T, 128] bf16, the identity list
+    # and fp32 chunk partials [chunks, d, 128] in place of [32, E, d] fp32 parts
+    diff = mma - gather
+    assert diff >= 4096 * 128 * 2 + 4096 * 4 + 4096 * 128 * 4 - 32 * 8 * 4096 * 4
+    # skew-shaped (x = 128 MiB): the tensor-core path is the default
+    k = B.shape(32768, 2048, 128, 8, 768)
+    default = B.moe_workspace_size(k, B.MOE_WS_BACKWARD)
+    monkeypatch.setenv("MOE_ROUTER_DWG", "mma")
+    assert B.moe_workspace_size(k, B.MOE_WS_BACKWARD) == default
+    monkeypatch.setenv("MOE_ROUTER_DWG", "gather")
+    assert B.moe_workspace_size(k, B.MOE_WS_BACKWARD) != default
+    monkeypatch.delenv("MOE_ROUTER_DWG")
