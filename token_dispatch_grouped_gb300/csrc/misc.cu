@@ -199,32 +199,51 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
     }
 }
 
-__global__ void router_dz_kernel(int T, int K, int TK, int nparts, const float* __restrict__ dS_part,
-                                 const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
-                                 float* __restrict__ dS, float* __restrict__ dz,
-                                 float* __restrict__ dz_row, int* err) {
+// One lane per (t, k): lanes K * j .. K * j + K - 1 of a warp hold token
+// j's slots (32 / K tokens per warp). A lane sums its routed row's partials
+// over the N tiles in order (loads issued 8 ahead), the token's lanes share
+// sum_j w_j dS_j through shuffles in slot order, and each lane writes its dS,
+// dz and the dz of its row.
+__global__ void __launch_bounds__(256)
+router_dz_kernel(int T, int K, int TK, int nparts, const float* __restrict__ dS_part,
+                 const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
+                 float* __restrict__ dS, float* __restrict__ dz, float* __restrict__ dz_row,
+                 int* err) {
     if (has_error(err)) return;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T) return;
-    float s[8], w[8];
-    int rows[8];
-    float sbar = 0.f;
-    for (int k = 0; k < K; ++k) {
-        const size_t i = static_cast<size_t>(t) * K + k;
-        const int r = tim[i];
-        rows[k] = r;
-        float acc = 0.f;
-        for (int p = 0; p < nparts; ++p) acc += dS_part[static_cast<size_t>(p) * TK + r];
-        s[k] = acc;
-        w[k] = topk_w[i];
-        sbar = fmaf(w[k], acc, sbar);
+    const int lane = threadIdx.x & 31;
+    const int tpw = 32 / K;  // tokens per warp
+    const int gw = static_cast<int>((static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+    const int t = gw * tpw + lane / K;
+    const int k = lane % K;
+    const bool active = lane < tpw * K && t < T;
+    const size_t i = static_cast<size_t>(t) * K + k;
+    float acc = 0.f, w = 0.f;
+    int r = 0;
+    if (active) {
+        r = tim[i];
+        w = topk_w[i];
+        int p = 0;
+        for (; p + 8 <= nparts; p += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = dS_part[static_cast<size_t>(p + u) * TK + r];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += v[u];
+        }
+        for (; p < nparts; ++p) acc += dS_part[static_cast<size_t>(p) * TK + r];
     }
-    for (int k = 0; k < K; ++k) {
-        const size_t i = static_cast<size_t>(t) * K + k;
-        const float z = w[k] * (s[k] - sbar);
-        dS[i] = s[k];
+    const int base = (lane / K) * K;
+    float sbar = 0.f;
+    for (int j = 0; j < K; ++j) {
+        const float sj = __shfl_sync(0xffffffffu, acc, base + j);
+        const float wj = __shfl_sync(0xffffffffu, w, base + j);
+        sbar = fmaf(wj, sj, sbar);
+    }
+    if (active) {
+        const float z = w * (acc - sbar);
+        dS[i] = acc;
         dz[i] = z;
-        dz_row[rows[k]] = z;
+        dz_row[r] = z;
     }
 }
 
@@ -507,8 +526,9 @@ cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_par
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
                              float* dz_row, int* err, cudaStream_t st) {
     LaunchScope ls("router_dz", st);
-    router_dz_kernel<<<(s.T + 127) / 128, 128, 0, st>>>(s.T, s.K, s.T * s.K, nparts, dS_part,
-                                                        topk_w, tim, dS, dz, dz_row, err);
+    const long long warps = (static_cast<long long>(s.T) + 32 / s.K - 1) / (32 / s.K);
+    router_dz_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(
+        s.T, s.K, s.T * s.K, nparts, dS_part, topk_w, tim, dS, dz, dz_row, err);
     return cudaGetLastError();
 }
 
