@@ -270,6 +270,17 @@ int moe_backward_rows(moe_shape s, int32_t rows_cap, const void* dy, const void*
                       void* dW1, void* dW3, void* dW2, float* dS_row, void* ws, size_t ws_bytes,
                       void* stream);
 
+/* Self-test of the device failure path (no counterpart in the pages; a test
+ * hook). Enqueues one CTA on `stream` that waits on a shared-memory barrier
+ * that nothing ever arrives at, through the same time-bounded wait as every
+ * pipelined kernel of the library; after limit_ns (1 ns .. 10 s) the wait gives
+ * up and the kernel sets MOE_ERR_TIMEOUT in the device status word, then
+ * returns, leaving the context usable. moe_get_error() then reports and clears
+ * it. Returns MOE_ERR_INVALID_ARG for a limit out of range, else MOE_OK or
+ * MOE_ERR_CUDA (launch failure). Does nothing if the status word is already
+ * set. */
+int moe_selftest_bounded_wait(uint64_t limit_ns, void* stream);
+
 /* Waits for `stream`, then returns and clears the device status word of the
  * current device (MOE_OK if no device-side error happened since the last
  * call). The only call that blocks the host. */

@@ -68,6 +68,9 @@ def test_null_pointers_rejected_before_any_device_work():
     bad = B.shape(16, 128, 8, 9, 128)
     assert B.LIB.moe_route(bad, None, None, None, None, None, None, None, 0, None) == \
         B.MOE_ERR_UNSUPPORTED_SHAPE
+    # the failure-path self-test rejects a wait limit out of range before any launch
+    assert B.LIB.moe_selftest_bounded_wait(0, None) == B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_selftest_bounded_wait(20_000_000_000, None) == B.MOE_ERR_INVALID_ARG
 
 
 def test_oracle_is_not_imported_by_the_product():

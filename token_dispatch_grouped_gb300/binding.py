@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "moe_forward_rows": (I, [MoeShape, ctypes.c_int32] + [P] * 13 + [S, P]),
         "moe_backward_rows": (I, [MoeShape, ctypes.c_int32] + [P] * 20 + [S, P]),
         "moe_get_error": (I, [P]),
+        "moe_selftest_bounded_wait": (I, [ctypes.c_uint64, P]),
         "moe_status_string": (ctypes.c_char_p, [I]),
         "moe_last_cuda_error": (ctypes.c_char_p, []),
         "moe_launch_count": (L, []),
@@ -245,6 +246,12 @@ def moe_backward(s, dy, x, Wg, W1, W3, W2, topk_ids, topk_w, eti, offsets, tim, 
 
 def moe_get_error(stream=None) -> int:
     return int(LIB.moe_get_error(_stream(stream)))
+
+
+def moe_selftest_bounded_wait(limit_ns: int, stream=None) -> int:
+    """Launches the failure-path self-test (a wait that runs out); returns the
+    launch status. moe_get_error() afterwards reports MOE_ERR_TIMEOUT."""
+    return int(LIB.moe_selftest_bounded_wait(int(limit_ns), _stream(stream)))
 
 
 def moe_launch_count() -> int:

@@ -851,6 +851,14 @@ int moe_token_rounding(moe_shape s, int m_tile, const float* logits, const int32
     return MOE_OK;
 }
 
+int moe_selftest_bounded_wait(uint64_t limit_ns, void* stream) {
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return MOE_ERR_INVALID_ARG;
+    int* err = status_ptr();
+    if (!err) return MOE_ERR_NO_DEVICE;
+    MOE_TRY(launch_selftest_wait(limit_ns, err, static_cast<cudaStream_t>(stream)));
+    return MOE_OK;
+}
+
 int moe_get_error(void* stream) {
     int* p = status_ptr();
     if (!p) return MOE_ERR_NO_DEVICE;

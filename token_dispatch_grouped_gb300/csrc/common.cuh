@@ -156,6 +156,10 @@ cudaError_t launch_dwg_operand(const moe_shape& s, const DwgPlan& dp, int rows_c
 cudaError_t launch_dwg_reduce(const moe_shape& s, const DwgPlan& dp, const float* part,
                               float* dWg, int* err, cudaStream_t st);
 
+// One CTA waits on a barrier nothing arrives at, for at most limit_ns; records
+// MOE_ERR_TIMEOUT when the bounded wait gives up (moe_selftest_bounded_wait).
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* err, cudaStream_t st);
+
 // gemm.cu — the grouped tcgen05 GEMMs.
 enum GemmKind { G1_UP = 0, G2_DOWN = 1, G3_DH = 2, G4_DW2 = 3, G5_DW13 = 4, G6_DX = 5,
                 // Non-gated (SiLU/ReLU) variants of G1 and G3; chosen by launch_gemm

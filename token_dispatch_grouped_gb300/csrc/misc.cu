@@ -31,6 +31,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -570,6 +571,32 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
     const int n = s.E * s.d;
     LaunchScope ls("router_dwg_reduce", st);
     router_dwg_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, part, dWg, err);
+    return cudaGetLastError();
+}
+
+// Failure-path self-test: one CTA waits on an mbarrier that nothing arrives
+// at, through the same bounded wait as the pipelined kernels. The wait gives
+// up after limit_ns, the kernel records MOE_ERR_TIMEOUT in the status word and
+// returns; the context stays usable.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int* err) {
+    if (has_error(err)) return;
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t b = ptx::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(b, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    // Phase 0 of the barrier never completes: nothing arrives on it.
+    const bool ok = ptx::mbar_wait(b, 0u, &abort_flag, limit_ns);
+    if (!ok && threadIdx.x == 0) raise_error(err, MOE_ERR_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* err, cudaStream_t st) {
+    LaunchScope ls("selftest_wait", st);
+    selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
     return cudaGetLastError();
 }
 
