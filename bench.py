@@ -68,6 +68,19 @@ def memory_kernel_bytes(s) -> dict:
     }
 
 
+def routing_stats(counts) -> dict:
+    """Per-expert row counts of a routing: their spread, the empty experts, and the
+    256-row M tiles that a CTA-pair GEMM over these rows runs against the tiles the
+    same rows would fill if packed (the partial-tile cost of the row-tiled GEMMs)."""
+    c = counts.to(torch.int64)
+    rows = int(c.sum())
+    return {"min_rows": int(c.min()), "max_rows": int(c.max()),
+            "empty_experts": int((c == 0).sum()),
+            "cv": float(c.float().std() / c.float().mean()),
+            "m_tiles_256": int(((c + 255) // 256).sum()),
+            "m_tiles_256_packed": (rows + 255) // 256}
+
+
 def load_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -582,10 +595,7 @@ def main():
     L.check_error()
 
     # ---- routing statistics
-    counts = (dp.offsets[1:] - dp.offsets[:-1]).cpu()
-    routing = {"min_rows": int(counts.min()), "max_rows": int(counts.max()),
-               "empty_experts": int((counts == 0).sum()),
-               "cv": float(counts.float().std() / counts.float().mean())}
+    routing = routing_stats((dp.offsets[1:] - dp.offsets[:-1]).cpu())
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -1,0 +1,43 @@
+"""Host-side arithmetic of bench.py (no GPU): the FLOP and byte counts it
+reports against, and the routing statistics of its JSON line."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from token_dispatch_grouped_gb300 import inputs as I  # noqa: E402
+
+
+def test_flop_count_is_the_layer_formula():
+    s = I.WORKLOADS["mixtral"]
+    TK = s.T * s.K
+    # 18 TK d h for the expert GEMMs (fwd 6, bwd 12) + 6 T d E for the router
+    assert bench.flops_per_step(s) == 18 * TK * s.d * s.h + 6 * s.T * s.d * s.E
+    ng = I.WORKLOADS["moeblaze_conf7"]
+    assert bench.flops_per_step(ng) == 12 * ng.T * ng.K * ng.d * ng.h + 6 * ng.T * ng.d * ng.E
+
+
+def test_memory_kernel_bytes_and_routed_buffer():
+    s = I.WORKLOADS["mixtral"]
+    b = bench.memory_kernel_bytes(s)
+    TK, d = s.T * s.K, s.d
+    assert b["combine"][1] == TK * d * 2 + TK * 8 + s.T * d * 2
+    assert b["router_dwg"][1] == s.T * d * 2 + TK * 12 + s.E * d * 4
+    assert "router_dwg_mma" in b["router_dwg"][0] and "router_dwg" in b["router_dwg"][0]
+    # the routed [T*K, d] bf16 buffer the layer never allocates: 64 MiB here
+    assert TK * d * 2 == 64 * 2**20
+
+
+def test_routing_stats_counts_partial_tiles():
+    # Mixtral-like: six experts just above 1024 rows get a fifth, nearly empty tile
+    counts = torch.tensor([1030, 1025, 1038, 1026, 1027, 1029, 1001, 1016], dtype=torch.int32)
+    st = bench.routing_stats(counts)
+    assert st["min_rows"] == 1001 and st["max_rows"] == 1038 and st["empty_experts"] == 0
+    assert st["m_tiles_256"] == 6 * 5 + 2 * 4
+    assert st["m_tiles_256_packed"] == (int(counts.sum()) + 255) // 256
+    z = bench.routing_stats(torch.tensor([0, 512, 0, 257], dtype=torch.int32))
+    assert z["empty_experts"] == 2 and z["m_tiles_256"] == 2 + 2
