@@ -54,6 +54,12 @@
 //       w_{t,k} Y into an fp32 accumulator row of token t (each token once per
 //       slot, so no two CTAs touch one row), and the last slot writes bf16 y.
 //       (SonicMoE 3.4.1: O_t = sum_k s_{t,k} Y_{t,k}, in slot order)
+//   G7  (router weight gradient) partials x_c^T B_c [d, nw] of token chunk c,
+//       B = [dz_hi | dz_lo] [T, nw]: the router gradient dz split into two bf16
+//       parts, dense over the (padded) experts; x rows gathered through an
+//       identity list (MN-major A, M = d), B rows MN-major; the epilogue writes
+//       fp32 partial rows, which are summed afterwards in a fixed order
+//       (dW_g = dz^T x, the router term of the backward past dS).
 // The saved pre-activation H and its gradient dH are [TK, hs] with hs = 2h
 // (a | b) for SwiGLU and hs = h (a) for non-gated experts.
 // Rows past an expert's end are zero-filled on the gathered operand, so
