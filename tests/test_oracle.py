@@ -406,3 +406,21 @@ def test_pins_catch_planted_relu_grad_error(monkeypatch):
     monkeypatch.undo()
     _, g = _autograd_reference(inp, ids, expert="relu")
     assert not np.allclose(b["dW1"], g["W1"], rtol=1e-6, atol=1e-8)
+
+
+def test_topk_gap_sees_membership_and_order_gaps():
+    """The gap that decides which router ids the GPU tests compare: the smallest
+    difference among the K+1 largest logits, so both the K-th vs (K+1)-th gap
+    (set membership) and gaps inside the top K (slot order) count."""
+    z = np.array([[5.0, 4.0, 3.0, 2.99995, 0.0],    # K=3: membership decided by 5e-5
+                  [5.0, 4.99995, 3.0, 1.0, 0.0],    # order of slots 0/1 decided by 5e-5
+                  [9.0, 7.0, 5.0, 3.0, 1.0],        # every gap 2
+                  [1.0, 1.0, 0.0, -1.0, -2.0]])     # exact tie in the top K
+    g = O.topk_gap(z, 3)
+    assert g[0] == pytest.approx(5e-5, abs=1e-9) and g[1] == pytest.approx(5e-5, abs=1e-9)
+    assert g[2] == pytest.approx(2.0) and g[3] == 0.0
+    # K = E: only the order inside the top K matters
+    assert O.topk_gap(np.array([[3.0, 1.0, 0.0]]), 3)[0] == pytest.approx(1.0)
+    # the gap is invariant to the order of the experts
+    perm = np.array([4, 2, 0, 3, 1])
+    assert np.allclose(O.topk_gap(z[:, perm], 3), g)
