@@ -81,6 +81,21 @@ def routing_stats(counts) -> dict:
             "m_tiles_256_packed": (rows + 255) // 256}
 
 
+PEAK_RULE = ("the burst bf16 peak applies when the timed region is shorter than 1 s or its "
+             "median SM clock is within 3% of the maximum; otherwise the sustained peak")
+
+
+def choose_bf16_peak(peaks: dict, timed_ms: float, clk: dict) -> tuple[float, str]:
+    """The measured bf16 peak that a timed region is judged against: the burst
+    figure for a short region or one that ran at full clock, the sustained
+    figure (a seconds-long loop under the power cap) otherwise."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    at_max = sm is not None and smax is not None and sm >= 0.97 * smax
+    if timed_ms < 1000.0 or at_max:
+        return peaks["bf16"], "burst"
+    return peaks["bf16_sus"], "sustained"
+
+
 def load_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -436,6 +451,8 @@ def main():
               "saved_over_routed": saved / routed_bytes,
               "workspace_fwd_bytes": ws_f, "workspace_bwd_bytes": ws_b,
               "peak_activation_bytes": saved + max(ws_f, ws_b),
+              "peak_activation_bytes_kind": "computed from the layout: saved tensors plus the "
+                                            "larger workspace (all buffers are preallocated)",
               "peak_activation_over_routed": (saved + max(ws_f, ws_b)) / routed_bytes,
               # the down-projection chunk buffer (plus the segment table): the
               # forward workspace beyond the [rows, h] SwiGLU output
@@ -477,6 +494,7 @@ def main():
     L.check_error()
     ms = max_over_ranks(ms, world)
     ms_step = ms / args.steps
+    bf16_peak, peak_kind = choose_bf16_peak(peaks, ms, clk)
     value = world * s.T * args.steps / (ms / 1e3)
     if args.routing == "tr":
         rows_of_step = int(rr.offsets[-1].item())
@@ -491,17 +509,22 @@ def main():
         per_launch_flop = (units[kname] * (rows_of_step or TK) * s.d * s.h * args.steps
                            / klaunches)
         achieved = per_launch_flop / (kms / klaunches / 1e3) / 1e12
-        peak = peaks["bf16_sus"]
+        peak = bf16_peak
         traffic = None
+        traffic_note = "no capture of the current GEMM sources"
         if os.path.exists(PROFILE_TRAFFIC):
             with open(PROFILE_TRAFFIC) as f:
                 tr = json.load(f)
             ent = tr.get(f"{kname}@{name}")
             if ent and ent.get("source_hash") == source_hash():
                 traffic = ent["dram_bytes_per_launch"]
+                traffic_note = ent.get("note", "profiles/traffic.json")
         roof = {"kernel": kname, "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peaks['src']} bf16 sustained (kernel timed inside the step)"}
+                "frac_burst": achieved / peaks["bf16"],
+                "frac_sustained": achieved / peaks["bf16_sus"],
+                "peak_source": f"{peaks['src']} bf16 {peak_kind}", "peak_rule": PEAK_RULE,
+                "traffic_source": traffic_note}
     kernels = {k: {"launches": n, "ms_per_step": t / args.steps} for k, (n, t) in per_kernel.items()}
     # HBM-bound kernels: algorithmic bytes / event-timed duration vs the measured copy peak
     memory_bound = {}
@@ -614,8 +637,12 @@ def main():
                                 **({"m_tile": args.m_tile, "rows": rows_of_step}
                                    if args.routing == "tr" else {})),
                     tflops=tflops,
-                    frac_of_bf16_peak=tflops / peaks["bf16_sus"],
-                    peak_note=f"{peaks['src']} bf16 sustained {peaks['bf16_sus']} TFLOP/s",
+                    frac_of_bf16_peak=tflops / bf16_peak,
+                    frac_of_bf16_burst=tflops / peaks["bf16"],
+                    frac_of_bf16_sustained=tflops / peaks["bf16_sus"],
+                    peak_note=(f"{peaks['src']} bf16 {peak_kind} {bf16_peak} TFLOP/s "
+                               f"(burst {peaks['bf16']}, sustained {peaks['bf16_sus']}); "
+                               + PEAK_RULE),
                     memory=memory, roofline=roof, kernels=kernels, memory_bound=memory_bound,
                     hbm_peak_gbs=peaks["hbm"], routing=routing,
                     cpu_baseline=cpu_base, e2e=e2e, gpu_launches=launches, clocks=clk)

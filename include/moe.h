@@ -151,7 +151,14 @@ int moe_build_dispatch(moe_shape s, const int32_t* topk_ids,
  *     MOE_ERR_STATIC_SCRATCH_LIMIT and launch nothing.
  *   - The first call on a device looks up the array's device address with
  *     that device current (cudaGetSymbolAddress); make that first call
- *     before any stream capture. Later calls do no set-up.
+ *     before any stream capture. Under CUDA's lazy module loading (the
+ *     default), that first call may also be what loads the library's device
+ *     code and the array onto the device, so device memory can drop by about
+ *     4 MiB at that moment (a one-time load by the driver, not an allocation
+ *     by this call). Later calls do no set-up and change no device memory.
+ *   - Host checks and status codes are those of moe_build_dispatch, in the
+ *     same order; a failed launch returns MOE_ERR_CUDA and leaves its message
+ *     for moe_last_cuda_error().
  *   - All calls on a device share the one array, and it keeps the last
  *     call's contents. Every entry a call reads is first written by the same
  *     call, so nothing needs clearing, but calls whose kernels overlap on the

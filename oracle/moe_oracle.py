@@ -17,8 +17,7 @@ Sources (page title, section):
               step", "A reference implementation", "Worked example: one
               skewed batch".
 
-Readings where the pages are silent or disagree (each one is a choice, listed
-again in the design notes):
+Readings where the pages are silent or disagree (each one is a choice):
   * The router renormalises over the chosen K experts ([Dropless] reference
     implementation); the MoEBlaze gating formula has no renormalisation.
   * Top-K ties go to the lower expert id; slot 0 holds the largest weight.

@@ -169,3 +169,22 @@ def test_workspace_follows_the_pass_and_router_gradient_rules(monkeypatch):
     monkeypatch.setenv("MOE_ROUTER_DWG", "gather")
     assert B.moe_workspace_size(k, B.MOE_WS_BACKWARD) != default
     monkeypatch.delenv("MOE_ROUTER_DWG")
+
+
+def test_dispatch_entry_points_share_host_checks():
+    """moe_build_dispatch and its allocation-free variant reject the same bad
+    calls with the same codes, before any device work."""
+    from token_dispatch_grouped_gb300 import binding as B
+    bad_kind = B.shape(16, 128, 8, 2, 128, 7)            # no such expert kind
+    assert B.LIB.moe_build_dispatch(bad_kind, None, None, None, None, None, 0, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert B.LIB.moe_build_dispatch_noalloc(bad_kind, None, None, None, None, None) == \
+        B.MOE_ERR_INVALID_ARG
+    too_many = B.shape(16, 128, 8, 9, 128)               # K > 8
+    assert B.LIB.moe_build_dispatch(too_many, None, None, None, None, None, 0, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert B.LIB.moe_build_dispatch_noalloc(too_many, None, None, None, None, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
+    ok = B.shape(16, 128, 8, 2, 128)
+    assert B.LIB.moe_build_dispatch_noalloc(ok, None, None, None, None, None) == \
+        B.MOE_ERR_INVALID_ARG

@@ -41,3 +41,14 @@ def test_routing_stats_counts_partial_tiles():
     assert st["m_tiles_256_packed"] == (int(counts.sum()) + 255) // 256
     z = bench.routing_stats(torch.tensor([0, 512, 0, 257], dtype=torch.int32))
     assert z["empty_experts"] == 2 and z["m_tiles_256"] == 2 + 2
+
+
+def test_peak_rule_burst_for_short_or_full_clock_regions():
+    peaks = {"bf16": 1932.0, "bf16_sus": 1741.0}
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
+    capped = {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0}
+    assert bench.choose_bf16_peak(peaks, 130.0, capped) == (1932.0, "burst")     # short region
+    assert bench.choose_bf16_peak(peaks, 5000.0, full) == (1932.0, "burst")      # at max clock
+    assert bench.choose_bf16_peak(peaks, 5000.0, capped) == (1741.0, "sustained")
+    assert bench.choose_bf16_peak(peaks, 5000.0, {"sm_mhz": None, "sm_max_mhz": None}) == \
+        (1741.0, "sustained")

@@ -4,8 +4,10 @@ moe_build_dispatch_noalloc serves callers that cannot allocate device memory
 (hosts that own all device memory, or loops where an allocation's implicit
 synchronisation is not acceptable): its scratch is a static device array in the
 library. It must give exactly the same index as moe_build_dispatch, call after
-call, since the array keeps the previous call's contents. This file is named to
-be collected last."""
+call, since the array keeps the previous call's contents, and after its first
+call on a device (which may load the library's device code and the array) it
+must leave the device's free memory unchanged. This file is named to be
+collected last."""
 import pytest
 import torch
 
@@ -51,3 +53,23 @@ def test_noalloc_dispatch_rejects_shapes_beyond_static_limit():
     dummy = torch.empty(16, dtype=torch.int32, device="cuda")
     rc = B.moe_build_dispatch_noalloc(s, dummy, dummy, dummy, dummy, check=False)
     assert rc == B.MOE_ERR_STATIC_SCRATCH_LIMIT
+
+
+def test_noalloc_dispatch_changes_no_device_memory():
+    from token_dispatch_grouped_gb300 import binding as B
+    T, E, K = 4000, 32, 4
+    s = B.shape(T, 128, E, K, 128)
+    ids = I.random_ids(T, E, K, seed=13).cuda()
+    eti = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    tim = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    B.moe_build_dispatch_noalloc(s, ids, eti, off, tim)   # first call: set-up, module load
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    torch_alloc0 = torch.cuda.memory_allocated()
+    for _ in range(5):
+        B.moe_build_dispatch_noalloc(s, ids, eti, off, tim)
+    torch.cuda.synchronize()
+    assert B.moe_get_error() == B.MOE_OK
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == torch_alloc0

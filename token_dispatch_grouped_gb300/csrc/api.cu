@@ -337,6 +337,9 @@ int record_cuda_error(cudaError_t e) {
 
 }  // namespace
 
+int check_shape_status(const moe_shape& s) { return check_shape(s); }
+int cuda_error_status(cudaError_t e) { return record_cuda_error(e); }
+
 LaunchScope::LaunchScope(const char* name, cudaStream_t st) : name_(name), st_(st), slot_(-1) {
     g_launches.fetch_add(1, std::memory_order_relaxed);
     g_current_launch = name;

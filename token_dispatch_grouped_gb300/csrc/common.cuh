@@ -49,6 +49,14 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t c
 
 int num_sms();
 
+// Host checks shared by the entry points (api.cu): the status of a shape
+// against the supported shapes (MOE_OK, MOE_ERR_INVALID_ARG or
+// MOE_ERR_UNSUPPORTED_SHAPE), and the MOE_ERR_CUDA return of a failed CUDA
+// call, which records "<launch>: <error>" for moe_last_cuda_error() and clears
+// the pending launch error.
+int check_shape_status(const moe_shape& s);
+int cuda_error_status(cudaError_t e);
+
 // Address of the current device's status word (nullptr without a device).
 int* device_status_word();
 

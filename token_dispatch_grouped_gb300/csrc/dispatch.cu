@@ -238,18 +238,20 @@ int32_t* g_noalloc_hist_ptr[kNoAllocMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
 // Device address of g_noalloc_hist on the current device (set up on first use).
-int32_t* noalloc_hist_ptr() {
+cudaError_t noalloc_hist_ptr(int32_t** out) {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
-        return nullptr;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (g_noalloc_hist_ptr[dev] == nullptr) {
         int32_t* ptr = nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_hist) != cudaSuccess)
-            return nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_hist);
+        if (e != cudaSuccess) return e;
         g_noalloc_hist_ptr[dev] = ptr;
     }
-    return g_noalloc_hist_ptr[dev];
+    *out = g_noalloc_hist_ptr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -258,21 +260,21 @@ int32_t* noalloc_hist_ptr() {
 extern "C" int moe_build_dispatch_noalloc(moe_shape s, const int32_t* topk_ids, int32_t* eti,
                                           int32_t* offsets, int32_t* tim, void* stream) {
     using namespace moe;
-    if (moe_workspace_size(s, MOE_WS_DISPATCH) == 0) {
-        if (s.T < 1 || s.d < 1 || s.E < 1 || s.K < 1 || s.h < 1) return MOE_ERR_INVALID_ARG;
-        return MOE_ERR_UNSUPPORTED_SHAPE;
-    }
+    // The same host checks, in the same order, as moe_build_dispatch.
+    const int rc = check_shape_status(s);
+    if (rc != MOE_OK) return rc;
     if (!topk_ids || !eti || !offsets || !tim) return MOE_ERR_INVALID_ARG;
     const long long nblk = (static_cast<long long>(s.T) + kBlockTokens - 1) / kBlockTokens;
     if (nblk * s.E > MOE_NOALLOC_DISPATCH_MAX_ENTRIES) return MOE_ERR_STATIC_SCRATCH_LIMIT;
     int* err = device_status_word();
     if (!err) return MOE_ERR_NO_DEVICE;
-    int32_t* hist = noalloc_hist_ptr();
-    if (!hist) return MOE_ERR_CUDA;
+    int32_t* hist = nullptr;
+    cudaError_t e = noalloc_hist_ptr(&hist);
+    if (e != cudaSuccess) return cuda_error_status(e);
     // Every histogram entry the kernels read is written earlier in the same
     // call (one entry per block and expert), so the array is not cleared.
-    if (launch_dispatch(s, topk_ids, eti, offsets, tim, hist, err,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+    e = launch_dispatch(s, topk_ids, eti, offsets, tim, hist, err,
+                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error_status(e);
     return MOE_OK;
 }

@@ -1,6 +1,6 @@
-// ptx.cuh — thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled and
-// gather4), tcgen05 (TMEM alloc, MMA, commit, load) and shared-memory matrix
-// descriptors. Every wait that can block is bounded in time.
+// ptx.cuh — thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled loads
+// and stores, bulk copies), cp.async, tcgen05 (TMEM alloc, MMA, commit, load)
+// and shared-memory matrix descriptors. Every wait that can block is bounded in time.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -61,19 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-// Non-blocking probe: has the phase with the given parity completed?
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -139,15 +126,6 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
     return v;
 }
-// Arrive on a peer CTA's mbarrier without ordering earlier memory accesses
-// (pair with fence_acq_rel_cluster before it).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
@@ -173,28 +151,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
-}
-
-// Four rows (r0..r3) of a 2D tensor, columns [col, col + box width), into four
-// consecutive box-rows of shared memory. The map's box must be one row high.
-// Rows outside the tensor are filled with zeros.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(col), "r"(r0), "r"(r1), "r"(r2),
-        "r"(r3)
-        : "memory");
-}
-
-// Prefetch a box of a 2D tensor into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
 }
 
 // Store a box from shared memory to a 2D tensor (bulk async group).
@@ -249,14 +205,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Waits until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 // Makes shared-memory writes of the generic proxy (cp.async, st.shared)
 // visible to the async proxy (TMA, tcgen05.mma).
