@@ -71,14 +71,23 @@ def memory_kernel_bytes(s) -> dict:
 def routing_stats(counts) -> dict:
     """Per-expert row counts of a routing: their spread, the empty experts, and the
     256-row M tiles that a CTA-pair GEMM over these rows runs against the tiles the
-    same rows would fill if packed (the partial-tile cost of the row-tiled GEMMs)."""
+    same rows would fill if packed (the partial-tile cost of the row-tiled GEMMs).
+    mma_rows_issued counts the rows the row-tiled GEMMs multiply in CTA-pair mode:
+    whole 256-row tiles, a last partial tile above 128 rows as 256, and one of
+    1..128 rows as a 128-row single-CTA tile; mma_rows_pairs_only is the same with
+    every partial tile at 256 rows."""
     c = counts.to(torch.int64)
     rows = int(c.sum())
+    rem = c % 256
+    issued = (c // 256) * 256 + torch.where(rem > 128, 256, torch.where(rem > 0, 128, 0))
     return {"min_rows": int(c.min()), "max_rows": int(c.max()),
             "empty_experts": int((c == 0).sum()),
             "cv": float(c.float().std() / c.float().mean()),
             "m_tiles_256": int(((c + 255) // 256).sum()),
-            "m_tiles_256_packed": (rows + 255) // 256}
+            "m_tiles_256_packed": (rows + 255) // 256,
+            "routed_rows": rows,
+            "mma_rows_issued": int(issued.sum()),
+            "mma_rows_pairs_only": int(((c + 255) // 256 * 256).sum())}
 
 
 PEAK_RULE = ("the burst bf16 peak applies when the timed region is shorter than 1 s or its "

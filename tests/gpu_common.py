@@ -10,6 +10,7 @@ import torch
 TOL_ROUTER = 1e-5
 TOL_BF16 = 1e-2
 GAP = 1e-3      # router ids are compared where the deciding logit gap exceeds this
+TOL_ROW = 3e-2  # per-row bound beside the whole-tensor Frobenius check
 
 
 def rel_fro(a, b) -> float:
@@ -28,3 +29,18 @@ def cpu(t) -> np.ndarray:
 
 def to_dev(d: dict, device="cuda") -> dict:
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def rel_rows(a, b) -> float:
+    """Largest relative error of one row (last axis) of a against b: a wrong
+    tile cannot hide inside a whole-tensor norm. Rows whose reference norm is
+    below 1e-3 of the median row norm are measured against that floor."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    a = a.reshape(-1, a.shape[-1])
+    b = b.reshape(-1, b.shape[-1])
+    nb = np.linalg.norm(b, axis=1)
+    if nb.size == 0:
+        return 0.0
+    floor = max(1e-3 * float(np.median(nb)), 1e-30)
+    return float(np.max(np.linalg.norm(a - b, axis=1) / np.maximum(nb, floor)))

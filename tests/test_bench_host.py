@@ -39,6 +39,10 @@ def test_routing_stats_counts_partial_tiles():
     assert st["min_rows"] == 1001 and st["max_rows"] == 1038 and st["empty_experts"] == 0
     assert st["m_tiles_256"] == 6 * 5 + 2 * 4
     assert st["m_tiles_256_packed"] == (int(counts.sum()) + 255) // 256
+    # pair tiles for the 1024 (or 768) rows of whole tiles, a 128-row single-CTA tile
+    # for each remainder of 1..14 rows, a 256-row tile for the 233- and 248-row ones
+    assert st["mma_rows_issued"] == 6 * (1024 + 128) + 2 * 1024
+    assert st["mma_rows_pairs_only"] == 38 * 256 and st["routed_rows"] == int(counts.sum())
     z = bench.routing_stats(torch.tensor([0, 512, 0, 257], dtype=torch.int32))
     assert z["empty_experts"] == 2 and z["m_tiles_256"] == 2 + 2
 

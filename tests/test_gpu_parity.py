@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import moe_oracle as O
-from tests.gpu_common import GAP, TOL_BF16, TOL_ROUTER, cpu, rel_fro, to_dev
+from tests.gpu_common import GAP, TOL_BF16, TOL_ROUTER, TOL_ROW, cpu, rel_fro, rel_rows, to_dev
 from token_dispatch_grouped_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -89,10 +89,81 @@ def test_layer_small_full_parity(s):
     assert rel_fro(cpu(g["dS"]), b["dS"]) <= TOL_BF16
     for k in ("dx",) + _wgrad_keys(s):
         assert rel_fro(cpu(g[k]), b[k]) <= TOL_BF16, k
+    # every row (token, expert row, weight row) on its own
+    assert rel_rows(cpu(H), f["H"]) <= TOL_ROW
+    assert rel_rows(cpu(y), f["y"]) <= TOL_ROW
+    for k in ("dx",) + _wgrad_keys(s):
+        assert rel_rows(cpu(g[k]), b[k]) <= TOL_ROW, k
     if s.K == 1:
         assert np.all(cpu(g["dWg"]) == 0.0)
     else:
         assert rel_fro(cpu(g["dWg"]), b["dWg"]) <= TOL_BF16
+
+
+def _ids_with_counts(T, K, counts, seed):
+    """Top-K ids [T, K] whose per-expert counts are exactly `counts` (each at most
+    T, summing to T*K): the expert-sorted labels are dealt column by column, so a
+    token's K experts are distinct, then the tokens are shuffled."""
+    labels = np.repeat(np.arange(len(counts)), counts)
+    assert labels.size == T * K and max(counts) <= T
+    ids = labels.reshape(K, T).T.copy()
+    rng = np.random.default_rng(seed)
+    ids = ids[rng.permutation(T)]
+    for k in range(K):
+        for j in range(k):
+            assert not np.any(ids[:, k] == ids[:, j])
+    return torch.from_numpy(ids.astype(np.int32))
+
+
+# CTA-pair GEMMs send an expert's last partial tile of at most 128 rows to a
+# single-CTA launch. Counts with remainders of 1 and 14 rows (split), an exact
+# multiple of 256 (none), 233 rows (stays in the pair launch), an expert of 100
+# rows (all remainder) and an empty expert; forward and backward on the injected
+# routing against the oracle, and against the unsplit pair launch.
+REMAINDER = [(2300, 256, 2, 512, [1025, 1038, 1280, 1257], "swiglu"),
+             (2000, 384, 3, 256, [1025, 1038, 1280, 1257, 0, 1400], "swiglu"),
+             (2300, 256, 2, 512, [1025, 1038, 1280, 1257], "silu"),
+             (1200, 512, 2, 384, [1025, 100, 1027, 248], "swiglu")]
+
+
+@pytest.mark.parametrize("T,d,K,h,counts,expert", REMAINDER,
+                         ids=lambda v: str(v) if not isinstance(v, list) else "-".join(map(str, v)))
+def test_partial_tile_remainders_single_cta(T, d, K, h, counts, expert, monkeypatch):
+    E = len(counts)
+    s = I.Shape(T, d, E, K, h, expert)
+    inp = I.make_layer_inputs(s, seed=8)
+    ids = _ids_with_counts(T, K, counts, seed=8)
+    w = I.random_weights(T, K, seed=8)
+    dv = to_dev(inp)
+    from token_dispatch_grouped_gb300.layer import Routing
+    out = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("MOE_GEMM_REMAINDER", mode)
+        L = _layer(s)
+        r = Routing(None, ids.cuda(), w.cuda())
+        dp = L.dispatch(r.ids)
+        y, H = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp)
+        g = L.backward(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r, dp, H)
+        L.check_error()
+        out[mode] = (y, H, g)
+    monkeypatch.delenv("MOE_GEMM_REMAINDER")
+    assert np.array_equal(np.diff(cpu(dp.offsets)), np.array(counts))
+    y, H, g = out["1"]
+    f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids.numpy(), w.numpy(), expert)
+    b = O.layer_backward(inp["dO"], inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"],
+                         ids.numpy(), w.numpy(), f, expert)
+    for name, got, ref in (("H", H, f["H"]), ("y", y, f["y"]), ("dS", g["dS"], b["dS"]),
+                           ("dx", g["dx"], b["dx"]), ("dWg", g["dWg"], b["dWg"])) + \
+            tuple((k, g[k], b[k]) for k in _wgrad_keys(s)):
+        assert rel_fro(cpu(got), ref) <= TOL_BF16, name
+        if name != "dS":
+            assert rel_rows(cpu(got), ref) <= TOL_ROW, name
+    # the split and the unsplit launches sum the same products per row
+    y0, H0, g0 = out["0"]
+    assert rel_fro(cpu(y), cpu(y0).astype(np.float64)) <= 1e-3
+    assert rel_fro(cpu(H), cpu(H0).astype(np.float64)) <= 1e-3
+    for k in ("dx", "dS") + _wgrad_keys(s):
+        assert rel_fro(cpu(g[k]), cpu(g0[k]).astype(np.float64)) <= 1e-3, k
 
 
 # Column passes: small layers split the down projection and dX into two column
@@ -269,6 +340,57 @@ def test_dispatch_adversarial(case):
     dp = L.dispatch(ids.cuda())
     L.check_error()
     _check_dispatch(ids, dp, E)
+
+
+# The single-CTA build (T*K <= 32768, ids staged in shared memory) and the
+# three-launch build must give the same bit-exact index. Cases at the size
+# threshold (T*K = 32768 exactly, with E = 256 at the shared-memory limit), just
+# past it (single forced), token counts that leave warps partly or wholly idle,
+# all tokens on one expert, and a Zipf-skewed routing with idle experts.
+SINGLE = [(4096, 256, 8, "random"), (16384, 8, 2, "random"), (32769, 4, 1, "random"),
+          (31, 8, 2, "random"), (1, 4, 4, "random"), (1057, 64, 6, "skew"),
+          (8192, 8, 4, "all_to_one"), (4096, 8, 2, "random")]
+
+
+@pytest.mark.parametrize("T,E,K,kind", SINGLE, ids=lambda v: str(v))
+def test_dispatch_single_cta_and_block_builds_agree(T, E, K, kind, monkeypatch):
+    if kind == "all_to_one":
+        ids = torch.stack([torch.full((T,), 3, dtype=torch.int32)] +
+                          [torch.full((T,), 4 + k, dtype=torch.int32) for k in range(K - 1)], 1)
+    elif kind == "skew":
+        ids = I.random_ids(T, E, K, seed=21, skew=1.8)
+    else:
+        ids = I.random_ids(T, E, K, seed=T + E)
+    s = I.Shape(T, 128, E, K, 128)
+    L = _layer(s)
+    outs = {}
+    for mode in ("single", "blocks"):
+        monkeypatch.setenv("MOE_DISPATCH", mode)
+        dp = L.dispatch(ids.cuda())
+        L.check_error()
+        outs[mode] = [t.clone() for t in (dp.eti, dp.offsets, dp.tim)]
+    monkeypatch.delenv("MOE_DISPATCH")
+    for a, b in zip(outs["single"], outs["blocks"]):
+        assert torch.equal(a, b)
+    _check_dispatch(ids, dp, E)
+
+
+@pytest.mark.parametrize("mode", ["single", "blocks"])
+def test_bad_expert_ids_both_dispatch_builds(mode, monkeypatch):
+    from token_dispatch_grouped_gb300 import binding as B
+    monkeypatch.setenv("MOE_DISPATCH", mode)
+    s = I.Shape(300, 128, 8, 3, 128)
+    L = _layer(s)
+    B.moe_get_error()
+    ids = I.random_ids(300, 8, 3, seed=2)
+    ids[299, 2] = -1                                  # out of range, last token
+    L.dispatch(ids.cuda())
+    assert B.moe_get_error() == B.MOE_ERR_BAD_EXPERT_ID
+    ids = I.random_ids(300, 8, 3, seed=2)
+    ids[0, 2] = ids[0, 1]                             # repeated within the first token
+    L.dispatch(ids.cuda())
+    assert B.moe_get_error() == B.MOE_ERR_BAD_EXPERT_ID
+    assert B.moe_get_error() == B.MOE_OK
 
 
 @pytest.mark.parametrize("T,E,K,skew", [(1000, 8, 2, 0.0), (3000, 64, 6, 1.2),

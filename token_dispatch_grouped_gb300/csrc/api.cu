@@ -477,7 +477,8 @@ int forward_impl(const moe_shape& s, const RouteView& rv, const void* x, const v
                                         static_cast<__nv_bfloat16*>(y), err, st, "combine"));
         else
             MOE_TRY(launch_combine(s, t0, t1, g2.n_off, g2.n_cols, rv.ids, rv.topk_w, rv.tim, sc,
-                                   w.Yc, static_cast<__nv_bfloat16*>(y), err, st));
+                                   w.Yc, static_cast<__nv_bfloat16*>(y), err, st, "combine",
+                                   !per_chunk));
     }
     return MOE_OK;
 }
@@ -592,7 +593,8 @@ int backward_impl(const moe_shape& s, const RouteView& rv, const void* dy, const
                                         static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
         else
             MOE_TRY(launch_combine(s, t0, t1, g6.n_off, g6.n_cols, rv.ids, nullptr, rv.tim, sc,
-                                   w.dXc, static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine"));
+                                   w.dXc, static_cast<__nv_bfloat16*>(dx), err, st, "dx_combine",
+                                   !per_chunk));
     }
     // Router weight gradient dW_g = dz^T x: per-expert gathered sums while x
     // fits in L2; else the dense [dz_hi | dz_lo] operand, its tensor-core

@@ -118,11 +118,13 @@ cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchu
 cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const int32_t* tim,
                                float* wrow, int* err, cudaStream_t st);
 // topk_w == nullptr sums with weight 1 (the token-gradient sum); `name` labels
-// the launch for the kernel timer.
+// the launch for the kernel timer. direct: the chunk buffer holds every routed
+// row in expert-sorted order (column passes, single passes), so the row of
+// (t, k) is token_index_map[t*K+k] and seg is not read.
 cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st,
-                           const char* name = "combine");
+                           const char* name = "combine", bool direct = false);
 cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_part,
                              const float* topk_w, const int32_t* tim, float* dS, float* dz,
                              float* dz_row, int* err, cudaStream_t st);

@@ -21,6 +21,12 @@
 //       (t, k) is the number of lower lanes in its warp's mask plus the counts
 //       of earlier warps; position = offsets[e] + base[block][e] + rank. This
 //       is exactly the order of a stable sort of the flattened ids by expert.
+// Layers with T*K <= 32768 take a single launch instead: one CTA stages the
+// ids in shared memory and runs the same three steps with warps in place of
+// blocks (dispatch_single_kernel below), which removes two launches and the
+// round trips of the block histogram through global memory.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -176,6 +182,198 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, i
     }
 }
 
+// ---------------------------------------------------------------------------
+// Single-CTA build (one launch) for layers whose T*K ids fit in one CTA's
+// shared memory: the same lane masks, scans and stable positions as D1..D3,
+// with warps in place of blocks. The ids are staged in shared memory; warp w
+// owns the contiguous tokens [w*Tw, (w+1)*Tw) (Tw a multiple of 32) and walks
+// them 32 at a time.
+//   pass 1  per round and slot, __match_any_sync groups the lanes that chose
+//           the same expert and the group's leader adds the group's size to
+//           cnt[w][e] (only warp w writes row w: no atomics);
+//   scan    cnt[w][e] becomes the exclusive prefix over warps of expert e, and
+//           the expert totals are scanned into offsets;
+//   pass 2  per round, the slot groups' leaders OR their lane masks into
+//           msk[w][e]; (t, k) lands at offsets[e] + cnt[w][e] + the number of
+//           lower lanes in msk[w][e]; then cnt[w][e] advances by the round's
+//           group sizes and msk[w][e] is cleared by the lanes that used it.
+// Token order inside an expert is warp order, then round, then lane: ascending
+// token, so the index equals that of a stable sort of the flattened ids.
+constexpr int kSingleThreads = 1024;
+constexpr int kSingleWarps = kSingleThreads / 32;
+constexpr int kSingleMaxTK = 32768;
+constexpr size_t kSingleMaxSmem = 200 * 1024;
+
+size_t single_smem_bytes(int T, int E, int K) {
+    const size_t tk4 = (static_cast<size_t>(T) * K + 3) / 4 * 4;
+    return 4 * (tk4 + 2 * static_cast<size_t>(kSingleWarps) * E + (E + 1) + kSingleWarps);
+}
+
+template <int K>
+__global__ void __launch_bounds__(kSingleThreads, 1)
+dispatch_single_kernel(const int32_t* __restrict__ ids, int T, int E, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ eti, int32_t* __restrict__ tim, int* err) {
+    if (has_error(err)) return;
+    extern __shared__ int32_t s_dyn[];
+    const int TK = T * K;
+    int32_t* s_ids = s_dyn;                                         // [TK]
+    int32_t* cnt = s_ids + (TK + 3) / 4 * 4;                        // [warps][E]
+    uint32_t* msk = reinterpret_cast<uint32_t*>(cnt + kSingleWarps * E);  // [warps][E]
+    int32_t* s_off = reinterpret_cast<int32_t*>(msk + kSingleWarps * E);  // [E + 1]
+    int32_t* wsum = s_off + E + 1;                                  // [warps]
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+#pragma unroll 4
+    for (int i = tid; i < TK; i += kSingleThreads) s_ids[i] = ids[i];
+    for (int i = tid; i < 2 * kSingleWarps * E; i += kSingleThreads) cnt[i] = 0;
+    __syncthreads();
+
+    const int Tw = ((T + kSingleWarps - 1) / kSingleWarps + 31) / 32 * 32;
+    const int tbeg = warp * Tw;
+    const int tend = min(T, tbeg + Tw);
+    int32_t* my_cnt = cnt + warp * E;
+    uint32_t* my_msk = msk + warp * E;
+    // Expert of (t, k) for a live lane, or -1 for a lane past the end and for an
+    // id out of range or repeated within the token (both passes drop the same
+    // entries, so every position stays inside [0, TK)).
+    auto load_slots = [&](int t, int (&e)[K]) -> bool {
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            int v = t < tend ? s_ids[t * K + k] : -1;
+            if (t < tend) {
+                bool dup = false;
+#pragma unroll
+                for (int j = 0; j < k; ++j) dup |= (e[j] == v);
+                if (v < 0 || v >= E || dup) {
+                    bad = true;
+                    v = -1;
+                }
+            }
+            e[k] = v;
+        }
+        return bad;
+    };
+
+    bool bad = false;
+    for (int t0 = tbeg; t0 < tend; t0 += 32) {  // warp-uniform
+        int e[K];
+        bad |= load_slots(t0 + lane, e);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const uint32_t m = __match_any_sync(0xffffffffu, e[k]);
+            if (e[k] >= 0 && lane == __ffs(m) - 1) my_cnt[e[k]] += __popc(m);
+            __syncwarp();
+        }
+    }
+    if (bad) raise_error(err, MOE_ERR_BAD_EXPERT_ID);
+    __syncthreads();
+
+    // Exclusive scan over warps per expert, then over experts.
+    int32_t tot = 0;
+    if (tid < E) {
+        for (int w = 0; w < kSingleWarps; ++w) {
+            const int32_t c = cnt[w * E + tid];
+            cnt[w * E + tid] = tot;
+            tot += c;
+        }
+    }
+    const int scan_warps = (E + 31) / 32;
+    int32_t inc = tot;
+    if (warp < scan_warps) {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        if (lane == 31) wsum[warp] = inc;
+    }
+    __syncthreads();
+    if (tid < E) {
+        int32_t pre = 0;
+        for (int w = 0; w < warp; ++w) pre += wsum[w];
+        const int32_t excl = pre + inc - tot;
+        s_off[tid] = excl;
+        offsets[tid] = excl;
+        if (tid == E - 1) {
+            s_off[E] = excl + tot;
+            offsets[E] = excl + tot;
+        }
+    }
+    __syncthreads();
+
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int t0 = tbeg; t0 < tend; t0 += 32) {
+        const int t = t0 + lane;
+        int e[K];
+        uint32_t m[K];
+        load_slots(t, e);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            m[k] = __match_any_sync(0xffffffffu, e[k]);
+            if (e[k] >= 0 && lane == __ffs(m[k]) - 1) my_msk[e[k]] |= m[k];
+            __syncwarp();
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (e[k] < 0) continue;
+            const int32_t pos = s_off[e[k]] + my_cnt[e[k]] + __popc(my_msk[e[k]] & lt);
+            eti[pos] = t;
+            tim[static_cast<size_t>(t) * K + k] = pos;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (e[k] >= 0 && lane == __ffs(m[k]) - 1) {
+                my_cnt[e[k]] += __popc(m[k]);
+                my_msk[e[k]] = 0u;
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// Which build a shape takes: the single CTA while T*K <= 32768 and its shared
+// memory fits, else D1..D3. MOE_DISPATCH=single|blocks forces one (single only
+// where it fits); read at every call.
+bool use_single(int T, int E, int K) {
+    const size_t smem = single_smem_bytes(T, E, K);
+    const bool fits = smem <= kSingleMaxSmem;
+    const char* f = std::getenv("MOE_DISPATCH");
+    if (f != nullptr && std::strcmp(f, "blocks") == 0) return false;
+    if (f != nullptr && std::strcmp(f, "single") == 0) return fits;
+    return fits && static_cast<long long>(T) * K <= kSingleMaxTK;
+}
+
+template <int K>
+cudaError_t launch_single_k(int T, int E, const int32_t* ids, int32_t* eti, int32_t* offsets,
+                            int32_t* tim, int* err, cudaStream_t st) {
+    const size_t smem = single_smem_bytes(T, E, K);
+    cudaError_t e = cudaFuncSetAttribute(dispatch_single_kernel<K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    LaunchScope ls("dispatch_single", st);
+    dispatch_single_kernel<K><<<1, kSingleThreads, smem, st>>>(ids, T, E, offsets, eti, tim, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_single(int T, int E, int K, const int32_t* ids, int32_t* eti, int32_t* offsets,
+                          int32_t* tim, int* err, cudaStream_t st) {
+    switch (K) {
+        case 1: return launch_single_k<1>(T, E, ids, eti, offsets, tim, err, st);
+        case 2: return launch_single_k<2>(T, E, ids, eti, offsets, tim, err, st);
+        case 3: return launch_single_k<3>(T, E, ids, eti, offsets, tim, err, st);
+        case 4: return launch_single_k<4>(T, E, ids, eti, offsets, tim, err, st);
+        case 5: return launch_single_k<5>(T, E, ids, eti, offsets, tim, err, st);
+        case 6: return launch_single_k<6>(T, E, ids, eti, offsets, tim, err, st);
+        case 7: return launch_single_k<7>(T, E, ids, eti, offsets, tim, err, st);
+        case 8: return launch_single_k<8>(T, E, ids, eti, offsets, tim, err, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int dispatch_block_tokens() { return kBlockTokens; }
@@ -210,6 +408,7 @@ cudaError_t launch_views(int T, int E, int K, int ld, int views, const int32_t* 
 cudaError_t launch_dispatch(const moe_shape& s, const int32_t* ids, int32_t* eti,
                             int32_t* offsets, int32_t* tim, int32_t* hist, int* err,
                             cudaStream_t st) {
+    if (use_single(s.T, s.E, s.K)) return launch_single(s.T, s.E, s.K, ids, eti, offsets, tim, err, st);
     return launch_views(s.T, s.E, s.K, s.K, 1, ids, eti, offsets, tim, hist, err, st,
                         "dispatch_hist", "dispatch_scan", "dispatch_scatter");
 }

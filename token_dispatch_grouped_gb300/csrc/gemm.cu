@@ -145,6 +145,8 @@ struct Params {
     int slot;      // G2_SLOT: routing slot k of this launch (of K = nslot)
     int nslot;
     const int32_t* tim;  // G2_SLOT: token_index_map
+    int part;      // row-tiled kinds: 0 all rows; 1 the rows of whole 256-row pair
+                   // tiles plus remainders above 128 rows; 2 remainders of 1..128 rows
     int n_off;     // G2/G6: first output column of this launch (column chunk)
     int ldo;       // G2/G6: row stride of the output chunk buffer (elements)
     const Seg* segs;
@@ -415,7 +417,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     if (!PAIR && has_error(p.err)) return;
 
     // ---- setup: segments, tile prefix, barriers, TMEM
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];
+    // Split launches of a row-tiled GEMM: an expert's last partial 256-row tile
+    // holding at most 128 rows leaves the pair launch (part 1) for a single-CTA
+    // launch with 128-row tiles (part 2), so that it costs one SM, not two.
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        Seg sg = p.segs[e];
+        if (p.part != 0) {
+            const int rows = sg.hi - sg.lo;
+            const int whole = rows / (2 * BM) * (2 * BM);
+            const bool split = rows > whole && rows - whole <= BM;
+            if (p.part == 1) {
+                if (split) sg.hi = sg.lo + whole;
+            } else if (split) {
+                sg.lo += whole;
+                sg.out += whole;
+            } else {
+                sg.lo = sg.hi;  // no remainder rows for this launch
+            }
+        }
+        s_segs[e] = sg;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
@@ -1272,12 +1293,15 @@ DwgPlan dwg_plan(const moe_shape& s) {
     return p;
 }
 
-cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
+namespace {
+
+// One launch of a GEMM problem with `ctas` CTAs per tile over the rows that
+// `part` selects (Params::part).
+cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStream_t st) {
     const moe_shape& s = g.s;
     // G2/G6 may cover a column chunk; their N tile must divide it.
     const int BN = (g.kind == G2_DOWN || g.kind == G6_DX) ? (g.n_cols % 256 == 0 ? 256 : 128)
                                                           : gemm_bn(g.kind, s);
-    const int ctas = choose_ctas(g.kind, s);
     // Row capacity of the routed-row arrays (H, A, dH, A', the chunk buffer).
     const uint64_t TK = g.rows > 0 ? static_cast<uint64_t>(g.rows) : static_cast<uint64_t>(s.T) * s.K;
     const uint64_t d = s.d, h = s.h, E = s.E;
@@ -1304,6 +1328,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     prm.wrow = g.wrow;
     prm.dS_part = g.dS_part;
     prm.err = g.err;
+    prm.part = part;
     // Upper bound on the tile count (rows of all experts + one partial tile
     // per expert), only used to size the persistent grid.
     const int bmc = BM * ctas;
@@ -1398,6 +1423,7 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
+    if (part == 2) max_tiles = s.E * prm.n_tiles;  // at most one 128-row tile per expert
     switch (g.kind) {
         case G1_UP:
             return gated ? launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu")
@@ -1415,6 +1441,29 @@ cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
         default: break;
     }
     return cudaErrorInvalidValue;
+}
+
+// Whether a row-tiled GEMM in CTA-pair mode sends each expert's last partial
+// tile of at most 128 rows to a second, single-CTA launch: a pair tile with r
+// valid rows costs the MMA work of 256 rows on two SMs, a single-CTA tile that
+// of 128 rows on one SM. MOE_GEMM_REMAINDER=0 keeps them in the pair launch
+// (read at every call).
+bool split_remainders(GemmKind kind) {
+    if (kind != G1_UP && kind != G2_DOWN && kind != G3_DH && kind != G6_DX) return false;
+    const char* f = std::getenv("MOE_GEMM_REMAINDER");
+    return !(f != nullptr && f[0] == '0' && f[1] == '\0');
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
+    const int ctas = choose_ctas(g.kind, g.s);
+    if (ctas == 2 && split_remainders(g.kind)) {
+        const cudaError_t e = launch_gemm_part(g, 2, 1, st);
+        if (e != cudaSuccess) return e;
+        return launch_gemm_part(g, 1, 2, st);
+    }
+    return launch_gemm_part(g, ctas, 0, st);
 }
 
 }  // namespace moe

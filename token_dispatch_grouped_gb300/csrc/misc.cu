@@ -128,18 +128,22 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 
 constexpr int kCombThreads = 256;   // 8 warps; one warp per token at a time
 constexpr int kCombWarps = kCombThreads / 32;
-// A lane loads the K rows' pieces of U = max(1, 8 / K) 8-column pieces at once:
-// about 8 16-byte loads (4 KB per warp) in flight before any arithmetic.
+// A lane loads the K rows' pieces of U = max(1, min(8, 16 / K)) 8-column pieces
+// at once: about 16 16-byte loads (8 KB per warp) in flight before any
+// arithmetic (a 2048-column pass of a K = 2 layer in one round).
 template <int K>
-constexpr int comb_u() { return K >= 8 ? 1 : 8 / K; }
+constexpr int comb_u() { return K >= 16 ? 1 : (16 / K > 8 ? 8 : 16 / K); }
 
 // Weighted combine of one chunk. Each warp takes a token (grid-stride), reads
-// its K (expert, position, weight) triples once, then every lane sums 8-column
-// pieces of the K expert-output rows in slot order and stores bf16; a lane
-// loads the pieces of all K rows for U column pieces before any arithmetic.
-// The chunk buffer's rows hold columns [c0, c0 + nc) of the expert outputs,
-// and row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo).
-template <int K>
+// its K (position, weight) pairs once, then every lane sums 8-column pieces of
+// the K expert-output rows in slot order and stores bf16; a lane loads the
+// pieces of all K rows for U column pieces before any arithmetic.
+// The chunk buffer's rows hold columns [c0, c0 + nc) of the expert outputs.
+// DIRECT (column passes and single passes: the buffer holds every routed row
+// in the expert-sorted order): row(t, k) = token_index_map[t*K+k]. Otherwise
+// (token chunks) row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo)
+// with e = ids[t*K+k].
+template <int K, bool DIRECT>
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ ids,
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
@@ -153,8 +157,12 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
         float wl = 0.f;
         if (lane < K) {
             const size_t i = static_cast<size_t>(t) * K + lane;
-            const Seg sg = seg[ids[i]];
-            off = static_cast<size_t>(sg.out + (tim[i] - sg.lo)) * nc;
+            int row = tim[i];
+            if constexpr (!DIRECT) {
+                const Seg sg = seg[ids[i]];
+                row = sg.out + (row - sg.lo);
+            }
+            off = static_cast<size_t>(row) * nc;
             wl = topk_w != nullptr ? topk_w[i] : 1.f;
         }
         constexpr int U = comb_u<K>();
@@ -505,15 +513,21 @@ int comb_grid(int tokens) {
 cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, const int32_t* ids,
                            const float* topk_w, const int32_t* tim, const Seg* seg,
                            const __nv_bfloat16* Yc, __nv_bfloat16* y, int* err, cudaStream_t st,
-                           const char* name) {
+                           const char* name, bool direct) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls(name, st);
     const int grid = comb_grid(t1 - t0);
     switch (s.K) {
 #define MOE_COMBINE_CASE(KK)                                                                  \
     case KK:                                                                                  \
-        combine_kernel<KK><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, topk_w,   \
-                                                          tim, seg, Yc, y, err);              \
+        if (direct)                                                                           \
+            combine_kernel<KK, true><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, \
+                                                                    topk_w, tim, seg, Yc, y,  \
+                                                                    err);                     \
+        else                                                                                  \
+            combine_kernel<KK, false><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d,     \
+                                                                     ids, topk_w, tim, seg,   \
+                                                                     Yc, y, err);             \
         break;
         MOE_COMBINE_CASE(1) MOE_COMBINE_CASE(2) MOE_COMBINE_CASE(3) MOE_COMBINE_CASE(4)
         MOE_COMBINE_CASE(5) MOE_COMBINE_CASE(6) MOE_COMBINE_CASE(7) MOE_COMBINE_CASE(8)
