@@ -206,7 +206,7 @@ constexpr size_t kSingleMaxSmem = 200 * 1024;
 
 size_t single_smem_bytes(int T, int E, int K) {
     const size_t tk4 = (static_cast<size_t>(T) * K + 3) / 4 * 4;
-    return 4 * (tk4 + 2 * static_cast<size_t>(kSingleWarps) * E + (E + 1) + kSingleWarps);
+    return 4 * (tk4 + 2 * static_cast<size_t>(kSingleWarps) * E + (E + 1) + kSingleWarps + E);
 }
 
 template <int K>
@@ -221,11 +221,21 @@ dispatch_single_kernel(const int32_t* __restrict__ ids, int T, int E, int32_t* _
     uint32_t* msk = reinterpret_cast<uint32_t*>(cnt + kSingleWarps * E);  // [warps][E]
     int32_t* s_off = reinterpret_cast<int32_t*>(msk + kSingleWarps * E);  // [E + 1]
     int32_t* wsum = s_off + E + 1;                                  // [warps]
+    int32_t* s_tot = wsum + kSingleWarps;                           // [E]
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    if ((reinterpret_cast<uintptr_t>(ids) & 15u) == 0) {  // 16-byte pieces, then the tail
+        const int n4 = TK / 4;
+        const int4* src = reinterpret_cast<const int4*>(ids);
+        int4* dst = reinterpret_cast<int4*>(s_ids);
 #pragma unroll 4
-    for (int i = tid; i < TK; i += kSingleThreads) s_ids[i] = ids[i];
+        for (int i = tid; i < n4; i += kSingleThreads) dst[i] = src[i];
+        for (int i = 4 * n4 + tid; i < TK; i += kSingleThreads) s_ids[i] = ids[i];
+    } else {
+#pragma unroll 4
+        for (int i = tid; i < TK; i += kSingleThreads) s_ids[i] = ids[i];
+    }
     for (int i = tid; i < 2 * kSingleWarps * E; i += kSingleThreads) cnt[i] = 0;
     __syncthreads();
 
@@ -270,15 +280,21 @@ dispatch_single_kernel(const int32_t* __restrict__ ids, int T, int E, int32_t* _
     if (bad) raise_error(err, MOE_ERR_BAD_EXPERT_ID);
     __syncthreads();
 
-    // Exclusive scan over warps per expert, then over experts.
-    int32_t tot = 0;
-    if (tid < E) {
-        for (int w = 0; w < kSingleWarps; ++w) {
-            const int32_t c = cnt[w * E + tid];
-            cnt[w * E + tid] = tot;
-            tot += c;
+    // Exclusive scan over warps per expert (warp e % 32 scans expert e with one
+    // lane per warp of counts), then over experts.
+    for (int e = warp; e < E; e += kSingleWarps) {
+        const int32_t v = cnt[lane * E + e];
+        int32_t run = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, run, o);
+            if (lane >= o) run += u;
         }
+        cnt[lane * E + e] = run - v;
+        if (lane == 31) s_tot[e] = run;
     }
+    __syncthreads();
+    const int32_t tot = tid < E ? s_tot[tid] : 0;
     const int scan_warps = (E + 31) / 32;
     int32_t inc = tot;
     if (warp < scan_warps) {

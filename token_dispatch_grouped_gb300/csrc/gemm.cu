@@ -412,9 +412,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int tile0 = blockIdx.x / CTAS;   // first tile of this CTA (pair)
     const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
 
+    // A remainder launch (part 2) may start while the pair launch of the same
+    // problem still runs (programmatic dependent launch): this grid's tiles are
+    // other rows, and before it ends it waits for that launch (griddep_wait), so
+    // that later launches on the stream still follow both. Every grid lets its
+    // dependent start at once; it then takes SMs as this grid's CTAs leave.
+    griddep_launch_dependents();
     // Skip the work after an earlier error; a CTA of a pair never leaves alone
     // (its peer would wait at the cluster barrier), so pairs run on.
-    if (!PAIR && has_error(p.err)) return;
+    if (!PAIR && has_error(p.err)) {
+        griddep_wait();
+        return;
+    }
 
     // ---- setup: segments, tile prefix, barriers, TMEM
     // Split launches of a row-tiled GEMM: an expert's last partial 256-row tile
@@ -1186,6 +1195,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
         else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    griddep_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -1196,6 +1206,8 @@ struct Maps {
 template <GemmKind KIND, int BN, int CTAS>
 cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                         const char* name) {
+    // A remainder launch (part 2) overlaps the pair launch before it.
+    const bool pdl = prm.part == 2;
     using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
     auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1207,13 +1219,15 @@ cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaSt
     cfg.blockDim = dim3(threads_of<KIND, CTAS>());
     cfg.dynamicSmemBytes = C::SMEM_TOTAL;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CTAS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     LaunchScope ls(name, st);
     return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b0, mp.b1, mp.o, prm);
 }
@@ -1448,17 +1462,34 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
 // valid rows costs the MMA work of 256 rows on two SMs, a single-CTA tile that
 // of 128 rows on one SM. MOE_GEMM_REMAINDER=0 keeps them in the pair launch
 // (read at every call).
-bool split_remainders(GemmKind kind) {
+// The split pays where the pair launch runs many waves of tiles: its last,
+// partly idle wave then takes in the remainder tiles (the remainder launch
+// starts as pair CTAs leave). With few waves (a column pass of the down
+// projection: tens of tiles of a long reduction) the remainders would add a
+// wave of their own, so the split is made from about 8 waves of pair tiles
+// up, estimated from the mean rows per expert (the counts stay on the device).
+// MOE_GEMM_REMAINDER=0|1 forces it off or on (read at every call).
+bool split_remainders(const GemmProblem& g) {
+    const GemmKind kind = g.kind;
     if (kind != G1_UP && kind != G2_DOWN && kind != G3_DH && kind != G6_DX) return false;
     const char* f = std::getenv("MOE_GEMM_REMAINDER");
-    return !(f != nullptr && f[0] == '0' && f[1] == '\0');
+    if (f != nullptr && (f[0] == '0' || f[0] == '1') && f[1] == '\0') return f[0] == '1';
+    const moe_shape& s = g.s;
+    const bool gated = s.expert == MOE_EXPERT_SWIGLU;
+    int n_tiles;
+    if (kind == G1_UP) n_tiles = gated ? s.h / 128 : s.h / 256;
+    else if (kind == G3_DH) n_tiles = (s.h + gemm_bn(G3_DH, s) - 1) / gemm_bn(G3_DH, s);
+    else n_tiles = g.n_cols / (g.n_cols % 256 == 0 ? 256 : 128);
+    const double rows = g.rows > 0 ? g.rows : static_cast<double>(s.T) * s.K;
+    const double pair_tiles = rows / 256.0 * n_tiles;
+    return pair_tiles >= 8.0 * (num_sms() / 2);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
     const int ctas = choose_ctas(g.kind, g.s);
-    if (ctas == 2 && split_remainders(g.kind)) {
+    if (ctas == 2 && split_remainders(g)) {
         const cudaError_t e = launch_gemm_part(g, 2, 1, st);
         if (e != cudaSuccess) return e;
         return launch_gemm_part(g, 1, 2, st);

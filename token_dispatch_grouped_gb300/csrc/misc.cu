@@ -128,11 +128,12 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
 
 constexpr int kCombThreads = 256;   // 8 warps; one warp per token at a time
 constexpr int kCombWarps = kCombThreads / 32;
-// A lane loads the K rows' pieces of U = max(1, min(8, 16 / K)) 8-column pieces
-// at once: about 16 16-byte loads (8 KB per warp) in flight before any
-// arithmetic (a 2048-column pass of a K = 2 layer in one round).
+// A lane loads the K rows' pieces of U = max(1, 8 / K) 8-column pieces at once:
+// about 8 16-byte loads (4 KB per warp) in flight before any arithmetic. (16
+// loads per lane measured slower on GB300: the extra registers cut the resident
+// CTAs below one wave of a 4096-token pass.)
 template <int K>
-constexpr int comb_u() { return K >= 16 ? 1 : (16 / K > 8 ? 8 : 16 / K); }
+constexpr int comb_u() { return K >= 8 ? 1 : 8 / K; }
 
 // Weighted combine of one chunk. Each warp takes a token (grid-stride), reads
 // its K (position, weight) pairs once, then every lane sums 8-column pieces of

@@ -206,6 +206,18 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// ---------------------------------------------------------------- dependent launch
+// Lets a grid launched with programmatic stream serialization (the next launch
+// on the stream) be scheduled once every CTA of this grid has executed this.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this grid depends on programmatically have completed
+// and their memory operations are visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Makes shared-memory writes of the generic proxy (cp.async, st.shared)
 // visible to the async proxy (TMA, tcgen05.mma).
 __device__ __forceinline__ void fence_proxy_async_smem() {
