@@ -118,7 +118,15 @@ int moe_chunk_tokens(moe_shape s);
  * Outputs: logits [T,E] fp32 (NULL to skip), topk_ids [T,K] int32 (descending
  * weight, ties to the lower id), topk_w [T,K] fp32 (sum to 1 per token).
  * Selection is on the fp32 logits z + bias; weights are exp(z_k - z_max)
- * normalised over the chosen K (equal to the renormalised softmax). */
+ * normalised over the chosen K (equal to the renormalised softmax).
+ * Workspace: moe_workspace_size(s, MOE_WS_ROUTE) bytes. For E <= 128 the
+ * logits are computed on the tensor cores from three bf16 parts of W_g
+ * (W_g = W0 + W1 + W2 to fp32 precision, each product with the bf16 x exact in
+ * fp32, fp32 accumulation), which the call writes into the workspace
+ * (3 * max(16, E rounded up to a power of two) rows of d bf16 values); a
+ * workspace that is NULL or smaller returns MOE_ERR_INVALID_ARG or
+ * MOE_ERR_WORKSPACE_TOO_SMALL. For E > 128 the logits are fp32 FFMA sums and
+ * no workspace is needed (ws may be NULL). */
 int moe_route(moe_shape s, const void* x, const float* Wg, const float* bias,
               float* logits, int32_t* topk_ids, float* topk_w,
               void* ws, size_t ws_bytes, void* stream);

@@ -424,3 +424,83 @@ def hidden_unit_grads(e: int, j: int, x, dO, W1, W3, W2, ids, w, expert: str = "
     A = act(a, expert)
     da = dA * act_grad(a, expert)
     return da @ xe, None, dY.T @ A
+
+
+def tokens_forward_backward_batched(tokens, x, dO, Wg, W1, W3, W2, ids, w,
+                                    expert: str = "swiglu"):
+    """Same outputs as tokens_forward_backward (y_t, dS_t and dx_t with the
+    router term, for the given distinct tokens), evaluated one expert at a time
+    over the sampled (token, slot) pairs routed to it, with matrix products.
+    The expert FFN and its backward are the definitions of layer_forward and
+    layer_backward ([MB-notes] 5.1, Algorithm 1; [Sonic] 3.4.1), restricted to
+    the sampled tokens; a token's K expert outputs are added in fp64."""
+    tokens = _asint(tokens)
+    ids = _asint(ids)
+    w = _as64(w)
+    d = W1.shape[2]
+    K = ids.shape[1]
+    gated = expert == "swiglu"
+    sub_ids = ids[tokens]
+    sub_w = w[tokens]
+    n = len(tokens)
+    y = np.zeros((n, d))
+    dS = np.zeros((n, K))
+    dx = np.zeros((n, d))
+    for e in np.unique(sub_ids):
+        ii, kk = np.nonzero(sub_ids == e)      # a token meets expert e at most once
+        xe = _as64(x[tokens[ii]])
+        dOe = _as64(dO[tokens[ii]])
+        W1e = _as64(W1[e])
+        W2e = _as64(W2[e])
+        a = xe @ W1e.T
+        if gated:
+            W3e = _as64(W3[e])
+            b = xe @ W3e.T
+            A = silu(a) * b
+        else:
+            A = act(a, expert)
+        Y = A @ W2e.T
+        wk = sub_w[ii, kk][:, None]
+        y[ii] += wk * Y
+        dS[ii, kk] = np.sum(dOe * Y, axis=1)
+        dA = (wk * dOe) @ W2e
+        if gated:
+            da = dA * b * silu_grad(a)
+            db = dA * silu(a)
+            dx[ii] += da @ W1e + db @ W3e
+        else:
+            da = dA * act_grad(a, expert)
+            dx[ii] += da @ W1e
+    dz = router_backward_dz(sub_w, dS)
+    Wg = _as64(Wg)
+    for k in range(K):
+        dx += dz[:, k:k + 1] * Wg[sub_ids[:, k]]
+    return y, dS, dx
+
+
+def hidden_units_grads(e: int, js, x, dO, W1, W3, W2, ids, w, expert: str = "swiglu"):
+    """hidden_unit_grads for several hidden units js of expert e at once:
+    dW1[e][js, :], dW3[e][js, :] (None for non-gated experts) and dW2[e][:, js],
+    each summed over the tokens routed to e."""
+    ids = _asint(ids)
+    w = _as64(w)
+    js = _asint(js)
+    sel_t, sel_k = np.nonzero(ids == e)
+    d = W1.shape[2]
+    gated = expert == "swiglu"
+    if len(sel_t) == 0:
+        z = np.zeros((len(js), d))
+        return z, (z.copy() if gated else None), np.zeros((d, len(js)))
+    xe = _as64(x[sel_t])
+    dY = w[sel_t, sel_k][:, None] * _as64(dO[sel_t])
+    a = xe @ _as64(W1[e][js]).T
+    dA = dY @ _as64(W2[e][:, js])
+    if gated:
+        b = xe @ _as64(W3[e][js]).T
+        A = silu(a) * b
+        da = dA * b * silu_grad(a)
+        db = dA * silu(a)
+        return da.T @ xe, db.T @ xe, dY.T @ A
+    A = act(a, expert)
+    da = dA * act_grad(a, expert)
+    return da.T @ xe, None, dY.T @ A

@@ -47,7 +47,12 @@ def test_host_functions():
     # larger layers keep the chunk at a quarter of T*K*d
     big = B.shape(65536, 4096, 8, 2, 14336)
     assert B.moe_workspace_size(big, B.MOE_WS_FORWARD) < 131072 * 14336 * 2 + 131072 * 1024 * 2 + 2**20
-    assert B.moe_workspace_size(s, B.MOE_WS_ROUTE) == 0
+    # route: the three bf16 parts of W_g, 3 x max(16, E padded) rows of d, for the
+    # tensor-core router (E <= 128); none for the FFMA router (E > 128)
+    assert B.moe_workspace_size(s, B.MOE_WS_ROUTE) == 3 * 16 * 4096 * 2
+    assert B.moe_workspace_size(B.shape(512, 2048, 100, 8, 768), B.MOE_WS_ROUTE) == \
+        3 * 128 * 2048 * 2
+    assert B.moe_workspace_size(B.shape(512, 2048, 200, 8, 768), B.MOE_WS_ROUTE) == 0
     # slot-wise forward: no chunk buffer, an fp32 [T, d] accumulator instead
     slot = B.moe_workspace_size(s, B.MOE_WS_FORWARD_SLOTWISE)
     assert slot >= TK * 14336 * 2 + 4096 * 4096 * 4

@@ -257,15 +257,22 @@ def test_forward_slotwise_parity(s):
 
 
 # Router shapes that exercise the cluster split of the reduction over d (2, 4 and
-# 8 CTAs), every padded expert width (8 .. 256), E not a multiple of 8, and a bias.
+# 8 CTAs), every padded expert width (8 .. 256), E not a multiple of 8, a bias,
+# and long reductions (d = 2048, 4096) at the expert counts of the workloads.
+# Both paths: the tensor-core router (E <= 128, three bf16 parts of W_g) and the
+# FFMA router (forced; the only one above E = 128).
 ROUTER = [(256, 2048, 8, 2), (1000, 1024, 16, 4), (300, 512, 64, 6), (500, 1024, 128, 8),
-          (200, 2048, 256, 8), (5000, 256, 5, 3), (777, 384, 40, 5)]
+          (200, 2048, 256, 8), (5000, 256, 5, 3), (777, 384, 40, 5), (4096, 4096, 8, 2),
+          (1024, 4096, 16, 4), (2000, 2048, 64, 6), (3000, 2048, 128, 8), (600, 4096, 128, 8)]
 
 
 @pytest.mark.parametrize("T,d,E,K", ROUTER, ids=lambda v: str(v))
 @pytest.mark.parametrize("with_bias", [False, True])
-def test_router_shapes(T, d, E, K, with_bias):
+@pytest.mark.parametrize("path", ["default", "ffma"])
+def test_router_shapes(T, d, E, K, with_bias, path, monkeypatch):
     from token_dispatch_grouped_gb300.layer import MoELayer
+    if path == "ffma":
+        monkeypatch.setenv("MOE_ROUTER", "ffma")
     s = I.Shape(T, d, E, K, 256)
     inp = I.make_layer_inputs(s, seed=3, parts=("x", "Wg"))
     bias = None
@@ -472,42 +479,74 @@ def _full(name):
     return s, inp, r, dp, y, H, g
 
 
+def _stratified_rows(offsets, blk=128, all_blocks_max=16):
+    """Expert-sorted rows compared at full size: for every non-empty expert, the
+    first and the last row of each of its 128-row blocks (a single-CTA M tile;
+    a CTA-pair tile is two of them), or of its first, middle and last block
+    when it has more than 16 blocks. Partial last blocks are included."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        nb = (hi - lo + blk - 1) // blk
+        blocks = range(nb) if nb <= all_blocks_max else sorted({0, nb // 2, nb - 1})
+        for b in blocks:
+            r0 = lo + b * blk
+            rows += [r0, min(hi, r0 + blk) - 1]
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def _units_per_n_tile(h, bn=256):
+    """One hidden unit in every bn-wide N tile of the weight-gradient GEMMs (the
+    same index serves the dW1 and the dW3 halves), at a position that moves
+    from tile to tile."""
+    return np.array([n * bn + (97 * n + 31) % min(bn, h - n * bn) for n in range((h + bn - 1) // bn)])
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "fine", "skew", "long", "moeblaze_conf7",
                                   "moeblaze_conf4"])
 def test_full_workload_sampled(name):
     s, inp, r, dp, y, H, g = _full(name)
-    rng = np.random.default_rng(0)
-    toks = np.sort(rng.choice(s.T, size=6, replace=False))
-    toks[-1] = s.T - 1
     bias = inp["bias"]
-    _check_route(r.logits, r.ids, r.w, inp["x"], inp["Wg"], s.K, bias, rows=toks)
     ids, w = cpu(r.ids), cpu(r.w)
     _check_dispatch(r.ids, dp, s.E)
-    counts = np.diff(cpu(dp.offsets))
+    offsets = cpu(dp.offsets)
+    counts = np.diff(offsets)
     if name == "skew":
         assert (counts == 0).sum() >= 4
-    ys, dSs, dxs = O.tokens_forward_backward(toks, inp["x"], inp["dO"], inp["Wg"], inp["W1"],
-                                             inp["W3"], inp["W2"], ids, w, s.expert)
+    eti = cpu(dp.eti)
+    rows = _stratified_rows(offsets)
+    rows = np.union1d(rows, np.arange(s.TK - 4, s.TK))     # largest H offsets
+    toks = np.union1d(eti[rows], [0, s.T - 1])
+    _check_route(r.logits, r.ids, r.w, inp["x"], inp["Wg"], s.K, bias, rows=toks)
+    ys, dSs, dxs = O.tokens_forward_backward_batched(toks, inp["x"], inp["dO"], inp["Wg"],
+                                                     inp["W1"], inp["W3"], inp["W2"], ids, w,
+                                                     s.expert)
     assert rel_fro(cpu(y)[toks], ys) <= TOL_BF16
+    assert rel_rows(cpu(y)[toks], ys) <= TOL_ROW
     if name in ("mixtral", "skew"):  # slot-wise forward at full size (K = 2 and K = 8)
         L = _layer(s)
         dv = to_dev(inp)
         y_s, _ = L.forward(dv["x"], dv["W1"], dv["W3"], dv["W2"], r, dp, combine="slotwise")
         L.check_error()
         assert rel_fro(cpu(y_s)[toks], ys) <= TOL_BF16
+        assert rel_rows(cpu(y_s)[toks], ys) <= TOL_ROW
     assert rel_fro(cpu(g["dS"])[toks], dSs) <= TOL_BF16
     assert rel_fro(cpu(g["dx"])[toks], dxs) <= TOL_BF16
-    # weight gradients on sampled (expert, hidden unit) pairs
+    assert rel_rows(cpu(g["dx"])[toks], dxs) <= TOL_ROW
+    # weight gradients: one hidden unit per 256-wide N tile (both halves of dW1/dW3)
+    # of the largest and of the smallest non-empty expert
     busy = np.nonzero(counts > 0)[0]
-    for e in rng.choice(busy, size=min(2, len(busy)), replace=False):
-        j = int(rng.integers(0, s.h))
-        g1, g3, g2 = O.hidden_unit_grads(int(e), j, inp["x"], inp["dO"], inp["W1"], inp["W3"],
-                                         inp["W2"], ids, w, s.expert)
-        assert rel_fro(cpu(g["dW1"][e, j]), g1) <= TOL_BF16
+    js = _units_per_n_tile(s.h)
+    for e in sorted({int(busy[np.argmax(counts[busy])]), int(busy[np.argmin(counts[busy])])}):
+        g1, g3, g2 = O.hidden_units_grads(e, js, inp["x"], inp["dO"], inp["W1"], inp["W3"],
+                                          inp["W2"], ids, w, s.expert)
+        pairs = [("dW1", cpu(g["dW1"][e])[js], g1), ("dW2", cpu(g["dW2"][e])[:, js].T, g2.T)]
         if s.gated:
-            assert rel_fro(cpu(g["dW3"][e, j]), g3) <= TOL_BF16
-        assert rel_fro(cpu(g["dW2"][e, :, j]), g2) <= TOL_BF16
+            pairs.append(("dW3", cpu(g["dW3"][e])[js], g3))
+        for k, got, ref in pairs:
+            assert rel_fro(got, ref) <= TOL_BF16, (k, e)
+            assert rel_rows(got, ref) <= TOL_ROW, (k, e)
     # properties at any size: dW_g rows sum to zero over experts (sum_k dz_k = 0),
     # empty experts have exact-zero weight gradients, outputs are finite
     dWg = cpu(g["dWg"])

@@ -424,3 +424,37 @@ def test_topk_gap_sees_membership_and_order_gaps():
     # the gap is invariant to the order of the experts
     perm = np.array([4, 2, 0, 3, 1])
     assert np.allclose(O.topk_gap(z[:, perm], 3), g)
+
+
+@pytest.mark.parametrize("expert", ["swiglu", "silu", "relu"])
+def test_batched_sampled_definitions_match_full_oracle(expert):
+    """The batched sampled helpers (one expert at a time over the sampled rows;
+    many hidden units at once) give the full oracle's values, including a token
+    list with every token and an expert that no sampled token uses."""
+    s, inp = _small(T=24, d=10, E=5, K=3, h=14, seed=17)
+    W3 = inp["W3"] if expert == "swiglu" else None
+    st = O.layer_step(inp["x"], inp["Wg"], inp["W1"], W3, inp["W2"], inp["dO"], 3,
+                      expert=expert)
+    for toks in ([0, 5, 23], list(range(24))):
+        y, dS, dx = O.tokens_forward_backward_batched(toks, inp["x"], inp["dO"], inp["Wg"],
+                                                      inp["W1"], W3, inp["W2"], st["ids"],
+                                                      st["w"], expert)
+        assert np.allclose(y, st["fwd"]["y"][toks], rtol=1e-11, atol=1e-12)
+        assert np.allclose(dS, st["bwd"]["dS"][toks], rtol=1e-11, atol=1e-12)
+        assert np.allclose(dx, st["bwd"]["dx"][toks], rtol=1e-10, atol=1e-12)
+    js = [0, 6, 13]
+    for e in range(5):
+        g1, g3, g2 = O.hidden_units_grads(e, js, inp["x"], inp["dO"], inp["W1"], W3, inp["W2"],
+                                          st["ids"], st["w"], expert)
+        assert np.allclose(g1, st["bwd"]["dW1"][e][js], rtol=1e-10, atol=1e-12)
+        assert np.allclose(g2, st["bwd"]["dW2"][e][:, js], rtol=1e-10, atol=1e-12)
+        if expert == "swiglu":
+            assert np.allclose(g3, st["bwd"]["dW3"][e][js], rtol=1e-10, atol=1e-12)
+        else:
+            assert g3 is None
+    # an expert without tokens: exact zeros of the right shapes
+    ids = np.where(st["ids"] == 4, 0, st["ids"])
+    ids[:, 1:] = np.where(ids[:, 1:] == ids[:, :1], 3, ids[:, 1:])
+    g1, g3, g2 = O.hidden_units_grads(4, js, inp["x"], inp["dO"], inp["W1"], W3, inp["W2"],
+                                      ids, st["w"], expert)
+    assert g1.shape == (3, 10) and g2.shape == (10, 3) and not g1.any() and not g2.any()

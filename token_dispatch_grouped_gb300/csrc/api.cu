@@ -637,7 +637,7 @@ int moe_chunk_tokens(moe_shape s) {
 size_t moe_workspace_size(moe_shape s, int which) {
     if (check_shape(s) != MOE_OK) return 0;
     switch (which) {
-        case MOE_WS_ROUTE: return 0;
+        case MOE_WS_ROUTE: return router_ws_bytes(s);
         case MOE_WS_DISPATCH: return layout_dispatch(s, nullptr, nullptr);
         case MOE_WS_FORWARD: return layout_fwd(s, tk_of(s), false, nullptr, nullptr);
         case MOE_WS_BACKWARD: return layout_bwd(s, tk_of(s), false, nullptr, nullptr);
@@ -648,17 +648,19 @@ size_t moe_workspace_size(moe_shape s, int which) {
 
 int moe_route(moe_shape s, const void* x, const float* Wg, const float* bias, float* logits,
               int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, void* stream) {
-    (void)ws;
-    (void)ws_bytes;
     int rc = check_shape(s);
     if (rc) return rc;
     if (!x || !Wg || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(Wg) || (logits && !aligned16(logits)))
         return MOE_ERR_MISALIGNED;
+    const size_t need = router_ws_bytes(s);
+    if (need > 0 && !ws) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !aligned16(ws)) return MOE_ERR_MISALIGNED;
     int* err = status_ptr();
     if (!err) return MOE_ERR_NO_DEVICE;
     MOE_TRY(launch_router(s, static_cast<const __nv_bfloat16*>(x), Wg, bias, logits, topk_ids,
-                          topk_w, err, static_cast<cudaStream_t>(stream)));
+                          topk_w, ws, err, static_cast<cudaStream_t>(stream)));
     return MOE_OK;
 }
 

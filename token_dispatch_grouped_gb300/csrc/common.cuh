@@ -64,9 +64,20 @@ int* device_status_word();
 // Every launcher enqueues on `st` and returns a cudaError_t of the launch.
 
 // router.cu
+// Whether the router logits run on the tensor cores (E <= 128; three bf16 parts
+// of W_g in the route workspace) or as fp32 FFMA (E > 128). MOE_ROUTER=ffma|mma
+// forces one (mma only where E <= 128); read at every call.
+inline bool router_tensor_cores(const moe_shape& s) {
+    const char* f = std::getenv("MOE_ROUTER");
+    if (f != nullptr && std::strcmp(f, "ffma") == 0) return false;
+    return s.E <= 128;
+}
+// Route workspace: the three bf16 parts of W_g [3 * max(16, E_pad), d] for the
+// tensor-core router, else 0.
+size_t router_ws_bytes(const moe_shape& s);
 cudaError_t launch_router(const moe_shape& s, const __nv_bfloat16* x, const float* Wg,
-                          const float* bias, float* logits, int32_t* ids, float* w, int* err,
-                          cudaStream_t st);
+                          const float* bias, float* logits, int32_t* ids, float* w, void* ws,
+                          int* err, cudaStream_t st);
 
 // dispatch.cu
 int dispatch_block_tokens();

@@ -1458,31 +1458,19 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
 }
 
 // Whether a row-tiled GEMM in CTA-pair mode sends each expert's last partial
-// tile of at most 128 rows to a second, single-CTA launch: a pair tile with r
-// valid rows costs the MMA work of 256 rows on two SMs, a single-CTA tile that
-// of 128 rows on one SM. MOE_GEMM_REMAINDER=0 keeps them in the pair launch
-// (read at every call).
-// The split pays where the pair launch runs many waves of tiles: its last,
-// partly idle wave then takes in the remainder tiles (the remainder launch
-// starts as pair CTAs leave). With few waves (a column pass of the down
-// projection: tens of tiles of a long reduction) the remainders would add a
-// wave of their own, so the split is made from about 8 waves of pair tiles
-// up, estimated from the mean rows per expert (the counts stay on the device).
-// MOE_GEMM_REMAINDER=0|1 forces it off or on (read at every call).
+// tile of at most 128 rows to a second, single-CTA launch (which starts as the
+// pair launch's CTAs leave): a pair tile with r valid rows costs the MMA work of
+// 256 rows on two SMs, a single-CTA tile that of 128 rows on one SM. Off by
+// default: measured on GB300 it saved no time on the Mixtral-shaped, skewed or
+// fine-grained layers (0-2% slower), because a remainder tile that runs apart
+// from its expert's other tiles streams the expert's weight panel from DRAM
+// again (for the up projection of the Mixtral-shaped layer, about 1.3 GB) for
+// a handful of rows. MOE_GEMM_REMAINDER=1 turns it on (read at every call).
 bool split_remainders(const GemmProblem& g) {
     const GemmKind kind = g.kind;
     if (kind != G1_UP && kind != G2_DOWN && kind != G3_DH && kind != G6_DX) return false;
     const char* f = std::getenv("MOE_GEMM_REMAINDER");
-    if (f != nullptr && (f[0] == '0' || f[0] == '1') && f[1] == '\0') return f[0] == '1';
-    const moe_shape& s = g.s;
-    const bool gated = s.expert == MOE_EXPERT_SWIGLU;
-    int n_tiles;
-    if (kind == G1_UP) n_tiles = gated ? s.h / 128 : s.h / 256;
-    else if (kind == G3_DH) n_tiles = (s.h + gemm_bn(G3_DH, s) - 1) / gemm_bn(G3_DH, s);
-    else n_tiles = g.n_cols / (g.n_cols % 256 == 0 ? 256 : 128);
-    const double rows = g.rows > 0 ? g.rows : static_cast<double>(s.T) * s.K;
-    const double pair_tiles = rows / 256.0 * n_tiles;
-    return pair_tiles >= 8.0 * (num_sms() / 2);
+    return f != nullptr && f[0] == '1' && f[1] == '\0';
 }
 
 }  // namespace
