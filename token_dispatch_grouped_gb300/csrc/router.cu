@@ -81,8 +81,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // adds the bias, writes the logits, picks the K largest (ties to the lower id)
 // and their weights exp(z_k - z_0) / sum_j exp(z_j - z_0). G = EP / 8
 // consecutive threads hold one token's logits, 8 each; the K arg-maxes are
-// butterflies over those G lanes. nthr (a multiple of 32) threads take part.
-template <int EP>
+// butterflies over those G lanes. Each lane group works on NT tokens at once,
+// so that NT independent compare-and-shuffle chains overlap. nthr (a multiple
+// of 32) threads take part.
+template <int EP, int NT>
 __device__ __forceinline__ void router_topk_tail(const float* zs, int epp, int bt, int t0, int T,
                                                  int E, int K, const float* __restrict__ bias,
                                                  float* __restrict__ logits,
@@ -90,67 +92,97 @@ __device__ __forceinline__ void router_topk_tail(const float* zs, int epp, int b
                                                  float* __restrict__ wout, int* err, int tid,
                                                  int nthr) {
     constexpr int G = EP / 8;
-    const int TPP = nthr / G;  // tokens per pass
+    const int groups = nthr / G;  // lane groups; each takes NT tokens per pass
     const int g = tid % G;
-#pragma unroll 1
-    for (int base = 0; base < bt; base += TPP) {
-        const int r = base + tid / G;
-        const int t = t0 + r;
-        const bool live = r < bt && t < T;
-        float v[8];
+    float bz[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int e = g * 8 + j;
-            const float b = (bias != nullptr && e < E) ? bias[e] : 0.f;
-            v[j] = (live && e < E) ? zs[r * epp + e] + b : -INFINITY;
-        }
-        if (logits != nullptr && live) {
+    for (int j = 0; j < 8; ++j) {
+        const int e = g * 8 + j;
+        bz[j] = (bias != nullptr && e < E) ? bias[e] : 0.f;
+    }
+#pragma unroll 1
+    for (int base = 0; base < bt; base += groups * NT) {
+        float v[NT][8];
+        bool live[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int r = base + n * groups + tid / G;
+            const int t = t0 + r;
+            live[n] = r < bt && t < T;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int e = g * 8 + j;
-                if (e < E) logits[static_cast<size_t>(t) * E + e] = v[j];
+                v[n][j] = (live[n] && e < E) ? zs[r * epp + e] + bz[j] : -INFINITY;
+            }
+            if (logits != nullptr && live[n]) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int e = g * 8 + j;
+                    if (e < E) logits[static_cast<size_t>(t) * E + e] = v[n][j];
+                }
             }
         }
-        uint32_t taken = 0;
-        float zsel[8];
-        int isel[8];
-#pragma unroll 1
-        for (int k = 0; k < K; ++k) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
+        uint32_t taken[NT];
+        float zsel[NT][8];
+        int isel[NT][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = g * 8 + j;
-                const bool ok = e < E && !((taken >> j) & 1u);
-                if (ok && (v[j] > bv || (v[j] == bv && e < bi))) {
-                    bv = v[j];
-                    bi = e;
+        for (int n = 0; n < NT; ++n) taken[n] = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (k >= K) break;
+            float bv[NT];
+            int bi[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                bv[n] = -INFINITY;
+                bi[n] = 0x7fffffff;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int e = g * 8 + j;
+                    const bool ok = e < E && !((taken[n] >> j) & 1u);
+                    if (ok && (v[n][j] > bv[n] || (v[n][j] == bv[n] && e < bi[n]))) {
+                        bv[n] = v[n][j];
+                        bi[n] = e;
+                    }
                 }
             }
 #pragma unroll
             for (int off = 1; off < G; off <<= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
-                    bi = oi;
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv[n], off);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi[n], off);
+                    if (ov > bv[n] || (ov == bv[n] && oi < bi[n])) {
+                        bv[n] = ov;
+                        bi[n] = oi;
+                    }
                 }
             }
-            if (bi / 8 == g && bi < E) taken |= 1u << (bi % 8);
-            zsel[k] = bv;
-            isel[k] = bi;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                if (bi[n] / 8 == g && bi[n] < E) taken[n] |= 1u << (bi[n] % 8);
+                zsel[n][k] = bv[n];
+                isel[n][k] = bi[n];
+            }
         }
-        if (live && g == 0) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            if (!(live[n] && g == 0)) continue;
+            const int t = t0 + base + n * groups + tid / G;
             float den = 0.f;
             float ex[8];
-            for (int k = 0; k < K; ++k) {
-                ex[k] = expf(zsel[k] - zsel[0]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k >= K) break;
+                ex[k] = expf(zsel[n][k] - zsel[n][0]);
                 den += ex[k];
             }
             const float inv = 1.f / den;
             bool bad = false;
-            for (int k = 0; k < K; ++k) {
-                const int e = isel[k];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k >= K) break;
+                const int e = isel[n][k];
                 bad |= (e < 0 || e >= E);
                 ids[static_cast<size_t>(t) * K + k] = e;
                 wout[static_cast<size_t>(t) * K + k] = ex[k] * inv;
@@ -312,8 +344,8 @@ router_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ 
     __syncthreads();
     if (warp >= kCompute / 32) return;
 
-    router_topk_tail<EP>(zs, C::EPP, C::BT, t0, T, E, K, bias, logits, ids, wout, err, tid,
-                         kCompute);
+    router_topk_tail<EP, 1>(zs, C::EPP, C::BT, t0, T, E, K, bias, logits, ids, wout, err, tid,
+                            kCompute);
 }
 
 // ---------------------------------------------------------------------------
@@ -528,8 +560,9 @@ router_mma_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constan
     } else {
         zs = red;
     }
-    router_topk_tail<EP>(zs, C::EPP, C::BT, t0, T, E, K, bias, logits, ids, wout, err, tid,
-                         C::THREADS);
+    router_topk_tail<EP, (EP >= 64 ? 4 : EP >= 32 ? 2 : 1)>(zs, C::EPP, C::BT, t0, T, E, K, bias,
+                                                             logits, ids, wout, err, tid,
+                                                             C::THREADS);
 }
 
 template <int EP, int S>
