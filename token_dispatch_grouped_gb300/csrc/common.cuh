@@ -13,6 +13,51 @@
 
 namespace moe {
 
+// ---- programmatic dependent launch
+// Kernels of the layer can be launched with programmatic stream serialization
+// (launch_k below and the GEMM and router launchers), so a kernel may be
+// scheduled while the previous kernel on the stream still runs. Each such kernel first waits until its predecessor
+// has completed and its memory is visible (pdl_wait), before it touches global
+// memory, and then lets its own successor be scheduled (pdl_trigger). Waiting
+// before triggering keeps the order transitive: when a kernel starts, the
+// kernel two launches back has completed. Only launch latency and CTA
+// scheduling overlap; no kernel reads or writes early.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// By default only the grouped GEMMs are launched this way: measured on GB300
+// (three runs each), that saved 1% of the step on the Mixtral-shaped and the
+// skewed layers, while launching the small kernels this way as well cost the
+// skewed layer (35 launches per step) 0.6%. MOE_PDL=1 launches every kernel of
+// the layer this way, MOE_PDL=0 none, MOE_PDL=small the small kernels only
+// (read at every call). gemm_launch tells which kind of launch asks.
+inline bool pdl_enabled(bool gemm_launch = false) {
+    const char* f = std::getenv("MOE_PDL");
+    if (f == nullptr || std::strcmp(f, "gemm") == 0) return gemm_launch;
+    if (std::strcmp(f, "0") == 0) return false;
+    if (std::strcmp(f, "small") == 0) return !gemm_launch;
+    return true;
+}
+// kernel<<<grid, block, smem, st>>>(args...), with programmatic stream
+// serialization where pdl_enabled() says so; the kernel calls pdl_wait() before
+// it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Device status word layout: the first error code that was raised wins.
 __device__ __forceinline__ void raise_error(int* err, int code) {
     atomicCAS(err, 0, code);

@@ -79,6 +79,8 @@ __device__ __forceinline__ void build_masks(const int32_t* __restrict__ ids, int
 __global__ void __launch_bounds__(kBlockTokens)
 dispatch_hist_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, int K,
                      int32_t* __restrict__ hist, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     __shared__ uint32_t masks[kWarps][kMaxE];
     int my_e[8];
@@ -98,6 +100,8 @@ dispatch_hist_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, int 
 __global__ void __launch_bounds__(kScanThreads)
 dispatch_scan_kernel(int32_t* __restrict__ hist, int nblk, int E, int32_t* __restrict__ offsets,
                      int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     hist += static_cast<size_t>(blockIdx.x) * nblk * E;  // one CTA per slot view
     offsets += static_cast<size_t>(blockIdx.x) * (E + 1);
@@ -148,6 +152,8 @@ __global__ void __launch_bounds__(kBlockTokens)
 dispatch_scatter_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, int K,
                         const int32_t* __restrict__ base, const int32_t* __restrict__ offsets,
                         int32_t* __restrict__ eti, int32_t* __restrict__ tim, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     __shared__ uint32_t masks[kWarps][kMaxE];
     __shared__ int32_t wbase[kWarps][kMaxE];
@@ -214,6 +220,8 @@ template <int K>
 __global__ void __launch_bounds__(kSingleThreads, 1)
 dispatch_single_kernel(const int32_t* __restrict__ ids, int T, int E, int32_t* __restrict__ offsets,
                        int32_t* __restrict__ eti, int32_t* __restrict__ tim, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     extern __shared__ int32_t s_dyn[];
     const int TK = T * K;
@@ -376,7 +384,7 @@ cudaError_t launch_single_k(int T, int E, const int32_t* ids, int32_t* eti, int3
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     LaunchScope ls("dispatch_single", st);
-    dispatch_single_kernel<K><<<1, kSingleThreads, smem, st>>>(ids, T, E, offsets, eti, tim, err);
+    launch_k(dispatch_single_kernel<K>, dim3(1), dim3(kSingleThreads), smem, st, ids, T, E, offsets, eti, tim, err);
     return cudaGetLastError();
 }
 
@@ -406,20 +414,20 @@ cudaError_t launch_views(int T, int E, int K, int ld, int views, const int32_t* 
     const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
     {
         LaunchScope ls(n1, st);
-        dispatch_hist_kernel<<<dim3(nblk, views), kBlockTokens, 0, st>>>(ids, ld, T, E, K, hist,
+        launch_k(dispatch_hist_kernel, dim3(dim3(nblk, views)), dim3(kBlockTokens), 0, st, ids, ld, T, E, K, hist,
                                                                          err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     {
         LaunchScope ls(n2, st);
-        dispatch_scan_kernel<<<views, kScanThreads, 0, st>>>(hist, nblk, E, offsets, err);
+        launch_k(dispatch_scan_kernel, dim3(views), dim3(kScanThreads), 0, st, hist, nblk, E, offsets, err);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     {
         LaunchScope ls(n3, st);
-        dispatch_scatter_kernel<<<dim3(nblk, views), kBlockTokens, 0, st>>>(
+        launch_k(dispatch_scatter_kernel, dim3(dim3(nblk, views)), dim3(kBlockTokens), 0, st, 
             ids, ld, T, E, K, hist, offsets, eti, tim, err);
     }
     return cudaGetLastError();

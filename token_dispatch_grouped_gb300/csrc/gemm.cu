@@ -412,11 +412,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int tile0 = blockIdx.x / CTAS;   // first tile of this CTA (pair)
     const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
 
-    // A remainder launch (part 2) may start while the pair launch of the same
-    // problem still runs (programmatic dependent launch): this grid's tiles are
-    // other rows, and before it ends it waits for that launch (griddep_wait), so
-    // that later launches on the stream still follow both. Every grid lets its
-    // dependent start at once; it then takes SMs as this grid's CTAs leave.
+    // Programmatic dependent launch (see pdl_wait in common.cuh): wait for the
+    // previous kernel, then let the next one be scheduled. A remainder launch
+    // (part 2) is the exception: its tiles are other rows of the pair launch
+    // just before it, whose own wait already covered the kernels before both,
+    // so it starts at once and waits for the pair launch only before it ends,
+    // so that later launches on the stream still follow both.
+    if (p.part != 2) griddep_wait();
     griddep_launch_dependents();
     // Skip the work after an earlier error; a CTA of a pair never leaves alone
     // (its peer would wait at the cluster barrier), so pairs run on.
@@ -1206,8 +1208,7 @@ struct Maps {
 template <GemmKind KIND, int BN, int CTAS>
 cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                         const char* name) {
-    // A remainder launch (part 2) overlaps the pair launch before it.
-    const bool pdl = prm.part == 2;
+    const bool pdl = pdl_enabled(true);
     using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
     auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,

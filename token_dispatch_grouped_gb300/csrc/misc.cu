@@ -61,6 +61,8 @@ __global__ void chunk_search_kernel(const int32_t* __restrict__ eti,
                                     const int32_t* __restrict__ offsets, int E, int T,
                                     int chunk_tokens, int nchunks, Seg* __restrict__ segs,
                                     int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int lane = threadIdx.x & 31;
     const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -79,6 +81,8 @@ __global__ void chunk_search_kernel(const int32_t* __restrict__ eti,
 // e); the last block writes the whole-row-space segments {o_e, o_e+1, o_e}.
 __global__ void chunk_pack_kernel(const int32_t* __restrict__ offsets, int E, int nchunks,
                                   Seg* __restrict__ segs, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     __shared__ int cnt[256];
     const int c = blockIdx.x;
@@ -103,6 +107,8 @@ __global__ void chunk_pack_kernel(const int32_t* __restrict__ offsets, int E, in
 __global__ void row_weights_kernel(const float* __restrict__ topk_w,
                                    const int32_t* __restrict__ tim, int TK,
                                    float* __restrict__ wrow, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < TK) wrow[tim[i]] = topk_w[i];
@@ -150,6 +156,8 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ Yc,
                __nv_bfloat16* __restrict__ y, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int lane = threadIdx.x & 31;
     for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
@@ -219,6 +227,8 @@ router_dz_kernel(int T, int K, int TK, int nparts, const float* __restrict__ dS_
                  const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                  float* __restrict__ dS, float* __restrict__ dz, float* __restrict__ dz_row,
                  int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int lane = threadIdx.x & 31;
     const int tpw = 32 / K;  // tokens per warp
@@ -266,6 +276,8 @@ combine_rows_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __rest
                     const int32_t* __restrict__ tok_exp, const int32_t* __restrict__ tok_rows,
                     const float* __restrict__ w_row, const Seg* __restrict__ seg,
                     const __nv_bfloat16* __restrict__ Yc, __nv_bfloat16* __restrict__ y, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int lane = threadIdx.x & 31;
     constexpr int U = 4;
@@ -326,6 +338,8 @@ __global__ void router_dz_rows_kernel(int T, int rows_cap, int nparts,
                                       const int32_t* __restrict__ tok_rows,
                                       const float* __restrict__ w_row, float* __restrict__ dS_row,
                                       float* __restrict__ dz_row, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
@@ -355,6 +369,8 @@ __global__ void __launch_bounds__(256)
 router_dwg_part_kernel(int d, int E, const __nv_bfloat16* __restrict__ x,
                        const int32_t* __restrict__ eti, const int32_t* __restrict__ offsets,
                        const float* __restrict__ dz_row, float* __restrict__ part, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int e = blockIdx.x;
     const int c = blockIdx.y * kDwgCols + threadIdx.x * 8;
@@ -395,6 +411,8 @@ router_dwg_part_kernel(int d, int E, const __nv_bfloat16* __restrict__ x,
 
 __global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
                                          float* __restrict__ dWg, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
@@ -407,6 +425,8 @@ __global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
 // token list and the chunk segments (chunk c = tokens [c * chunk, ...)).
 __global__ void dwg_zero_kernel(int T, int nw, int chunk, int nseg, uint4* __restrict__ B,
                                 int32_t* __restrict__ iota, Seg* __restrict__ segs, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -432,6 +452,8 @@ __global__ void dwg_scatter_kernel(int rows_cap, int E, int e_pad, int nw,
                                    const int32_t* __restrict__ offsets,
                                    const float* __restrict__ dz_row, __nv_bfloat16* __restrict__ B,
                                    int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows_cap || r >= offsets[E]) return;
@@ -455,6 +477,8 @@ __global__ void dwg_scatter_kernel(int rows_cap, int E, int e_pad, int nw,
 __global__ void __launch_bounds__(256)
 dwg_reduce_kernel(int d, int E, int e_pad, int nw, int nseg, const float* __restrict__ part,
                   float* __restrict__ dWg, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     __shared__ float tile[32][33];
     const int e0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
@@ -487,13 +511,13 @@ cudaError_t launch_chunk_segments(const moe_shape& s, int chunk_tokens, int nchu
     if (nchunks > 0) {
         LaunchScope ls("chunk_search", st);
         const int warps = nchunks * s.E;
-        chunk_search_kernel<<<(warps + 7) / 8, 256, 0, st>>>(eti, offsets, s.E, s.T,
+        launch_k(chunk_search_kernel, dim3((warps + 7) / 8), dim3(256), 0, st, eti, offsets, s.E, s.T,
                                                              chunk_tokens, nchunks, segs, err);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     LaunchScope ls("chunk_pack", st);
-    chunk_pack_kernel<<<nchunks + 1, 256, 0, st>>>(offsets, s.E, nchunks, segs, err);
+    launch_k(chunk_pack_kernel, dim3(nchunks + 1), dim3(256), 0, st, offsets, s.E, nchunks, segs, err);
     return cudaGetLastError();
 }
 
@@ -501,7 +525,7 @@ cudaError_t launch_row_weights(const moe_shape& s, const float* topk_w, const in
                                float* wrow, int* err, cudaStream_t st) {
     const int TK = s.T * s.K;
     LaunchScope ls("row_weights", st);
-    row_weights_kernel<<<(TK + 255) / 256, 256, 0, st>>>(topk_w, tim, TK, wrow, err);
+    launch_k(row_weights_kernel, dim3((TK + 255) / 256), dim3(256), 0, st, topk_w, tim, TK, wrow, err);
     return cudaGetLastError();
 }
 
@@ -522,11 +546,11 @@ cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, c
 #define MOE_COMBINE_CASE(KK)                                                                  \
     case KK:                                                                                  \
         if (direct)                                                                           \
-            combine_kernel<KK, true><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d, ids, \
+            launch_k(combine_kernel<KK, true>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d, ids, \
                                                                     topk_w, tim, seg, Yc, y,  \
                                                                     err);                     \
         else                                                                                  \
-            combine_kernel<KK, false><<<grid, kCombThreads, 0, st>>>(t0, t1, c0, nc, s.d,     \
+            launch_k(combine_kernel<KK, false>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d,     \
                                                                      ids, topk_w, tim, seg,   \
                                                                      Yc, y, err);             \
         break;
@@ -543,7 +567,7 @@ cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_par
                              float* dz_row, int* err, cudaStream_t st) {
     LaunchScope ls("router_dz", st);
     const long long warps = (static_cast<long long>(s.T) + 32 / s.K - 1) / (32 / s.K);
-    router_dz_kernel<<<static_cast<int>((warps * 32 + 255) / 256), 256, 0, st>>>(
+    launch_k(router_dz_kernel, dim3(static_cast<int>((warps * 32 + 255) / 256)), dim3(256), 0, st, 
         s.T, s.K, s.T * s.K, nparts, dS_part, topk_w, tim, dS, dz, dz_row, err);
     return cudaGetLastError();
 }
@@ -555,7 +579,7 @@ cudaError_t launch_combine_rows(const moe_shape& s, int t0, int t1, int c0, int 
                                 cudaStream_t st, const char* name) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls(name, st);
-    combine_rows_kernel<<<comb_grid(t1 - t0), kCombThreads, 0, st>>>(
+    launch_k(combine_rows_kernel, dim3(comb_grid(t1 - t0)), dim3(kCombThreads), 0, st, 
         t0, t1, c0, nc, s.d, tok_off, tok_exp, tok_rows, w_row, seg, Yc, y, err);
     return cudaGetLastError();
 }
@@ -565,7 +589,7 @@ cudaError_t launch_router_dz_rows(const moe_shape& s, int rows_cap, int nparts,
                                   const int32_t* tok_rows, const float* w_row, float* dS_row,
                                   float* dz_row, int* err, cudaStream_t st) {
     LaunchScope ls("router_dz", st);
-    router_dz_rows_kernel<<<(s.T + 255) / 256, 256, 0, st>>>(s.T, rows_cap, nparts, dS_part,
+    launch_k(router_dz_rows_kernel, dim3((s.T + 255) / 256), dim3(256), 0, st, s.T, rows_cap, nparts, dS_part,
                                                              tok_off, tok_rows, w_row, dS_row,
                                                              dz_row, err);
     return cudaGetLastError();
@@ -578,14 +602,13 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
                               float* dWg, int* err, cudaStream_t st) {
     {
         LaunchScope ls("router_dwg", st);
-        router_dwg_part_kernel<<<dim3(s.E, (s.d + kDwgCols - 1) / kDwgCols, kDwgParts), 256, 0,
-                                 st>>>(s.d, s.E, x, eti, offsets, dz_row, part, err);
+        launch_k(router_dwg_part_kernel, dim3(dim3(s.E, (s.d + kDwgCols - 1) / kDwgCols, kDwgParts)), dim3(256), 0, st, s.d, s.E, x, eti, offsets, dz_row, part, err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n = s.E * s.d;
     LaunchScope ls("router_dwg_reduce", st);
-    router_dwg_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, part, dWg, err);
+    launch_k(router_dwg_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, st, n, part, dWg, err);
     return cudaGetLastError();
 }
 
@@ -594,6 +617,8 @@ cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const 
 // up after limit_ns, the kernel records MOE_ERR_TIMEOUT in the status word and
 // returns; the context stays usable.
 __global__ void selftest_wait_kernel(uint64_t limit_ns, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
@@ -611,7 +636,7 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, int* err) {
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int* err, cudaStream_t st) {
     LaunchScope ls("selftest_wait", st);
-    selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+    launch_k(selftest_wait_kernel, dim3(1), dim3(32), 0, st, limit_ns, err);
     return cudaGetLastError();
 }
 
@@ -624,14 +649,14 @@ cudaError_t launch_dwg_operand(const moe_shape& s, const DwgPlan& dp, int rows_c
         const size_t n16 = static_cast<size_t>(s.T) * dp.nw / 8;
         const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256,
                                                            static_cast<size_t>(num_sms()) * 8));
-        dwg_zero_kernel<<<std::max(1, grid), 256, 0, st>>>(s.T, dp.nw, dp.chunk, dp.nchunks,
+        launch_k(dwg_zero_kernel, dim3(std::max(1, grid)), dim3(256), 0, st, s.T, dp.nw, dp.chunk, dp.nchunks,
                                                            reinterpret_cast<uint4*>(B), iota,
                                                            segs, err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     LaunchScope ls("router_dwg_scatter", st);
-    dwg_scatter_kernel<<<(rows_cap + 255) / 256, 256, 0, st>>>(rows_cap, s.E, dp.e_pad, dp.nw,
+    launch_k(dwg_scatter_kernel, dim3((rows_cap + 255) / 256), dim3(256), 0, st, rows_cap, s.E, dp.e_pad, dp.nw,
                                                                eti, offsets, dz_row, B, err);
     return cudaGetLastError();
 }
@@ -639,7 +664,7 @@ cudaError_t launch_dwg_operand(const moe_shape& s, const DwgPlan& dp, int rows_c
 cudaError_t launch_dwg_reduce(const moe_shape& s, const DwgPlan& dp, const float* part,
                               float* dWg, int* err, cudaStream_t st) {
     LaunchScope ls("router_dwg_reduce", st);
-    dwg_reduce_kernel<<<dim3((s.d + 31) / 32, (s.E + 31) / 32), dim3(32, 8), 0, st>>>(
+    launch_k(dwg_reduce_kernel, dim3(dim3((s.d + 31) / 32, (s.E + 31) / 32)), dim3(dim3(32, 8)), 0, st, 
         s.d, s.E, dp.e_pad, dp.nw, dp.nchunks, part, dWg, err);
     return cudaGetLastError();
 }

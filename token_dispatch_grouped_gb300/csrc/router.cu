@@ -201,6 +201,8 @@ router_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ 
     using C = RouterCfg<EP>;
     constexpr int kCompute = 32 * C::CW;
     constexpr int kThreads = C::THREADS;
+    pdl_wait();
+    pdl_trigger();
     // A CTA of a cluster must not leave alone (its peers would wait at the
     // cluster barrier), so only single-CTA launches skip work after an error.
     if (S == 1 && has_error(err)) return;
@@ -390,6 +392,8 @@ struct RmCfg {
 // Three bf16 parts of W_g: Wsp[p * EB + e][c] for e < EB (zeros past E).
 __global__ void router_wsplit_kernel(const float* __restrict__ Wg, int E, int EB, int d,
                                      __nv_bfloat16* __restrict__ Wsp, int* err) {
+    pdl_wait();
+    pdl_trigger();
     if (has_error(err)) return;
     const size_t n = static_cast<size_t>(EB) * d;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -413,6 +417,8 @@ router_mma_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constan
                   int32_t* __restrict__ ids, float* __restrict__ wout, int T, int d, int E, int K,
                   int* err) {
     using C = RmCfg<EP>;
+    pdl_wait();
+    pdl_trigger();
     if (S == 1 && has_error(err)) return;  // a cluster's CTAs never leave alone
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -583,13 +589,15 @@ cudaError_t launch_mma_eps(const moe_shape& s, const __nv_bfloat16* x, const __n
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     LaunchScope ls("router", st);
     return cudaLaunchKernelEx(&cfg, kfn, mapX, mapB, bias, logits, ids, w, s.T, s.d, s.E, s.K, err);
 }
@@ -605,7 +613,7 @@ cudaError_t launch_mma_ep(const moe_shape& s, const __nv_bfloat16* x, const floa
         LaunchScope ls("router_wsplit", st);
         const size_t n = static_cast<size_t>(C::EB) * s.d;
         const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 4 * 152));
-        router_wsplit_kernel<<<grid, 256, 0, st>>>(Wg, s.E, C::EB, s.d, Wsp, err);
+        launch_k(router_wsplit_kernel, dim3(grid), dim3(256), 0, st, Wg, s.E, C::EB, s.d, Wsp, err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -641,13 +649,15 @@ cudaError_t launch_eps(const moe_shape& s, const __nv_bfloat16* x, const float* 
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
     LaunchScope ls("router", st);
     return cudaLaunchKernelEx(&cfg, kfn, mapX, mapW, bias, logits, ids, w, s.T, s.d, s.E, s.K,
                               err);
