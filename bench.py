@@ -59,7 +59,7 @@ def memory_kernel_bytes(s) -> dict:
     return {
         # the tensor-core router's split of W_g into bf16 parts counts with it
         "router": (("router", "router_wsplit"), T * d * 2 + E * d * 4 + TK * 8 + T * E * 4),
-        "dispatch": (("dispatch_hist", "dispatch_scan", "dispatch_scatter"),
+        "dispatch": (("dispatch_single", "dispatch_hist", "dispatch_scan", "dispatch_scatter"),
                      2 * TK * 4 + 2 * TK * 4 + (E + 1) * 4),
         "combine": (("combine",), TK * d * 2 + TK * 8 + T * d * 2),
         "dx_combine": (("dx_combine",), TK * d * 2 + TK * 8 + T * d * 2),

@@ -349,14 +349,17 @@ def test_dispatch_adversarial(case):
     _check_dispatch(ids, dp, E)
 
 
-# The single-CTA build (T*K <= 32768, ids staged in shared memory) and the
-# three-launch build must give the same bit-exact index. Cases at the size
-# threshold (T*K = 32768 exactly, with E = 256 at the shared-memory limit), just
-# past it (single forced), token counts that leave warps partly or wholly idle,
-# all tokens on one expert, and a Zipf-skewed routing with idle experts.
-SINGLE = [(4096, 256, 8, "random"), (16384, 8, 2, "random"), (32769, 4, 1, "random"),
-          (31, 8, 2, "random"), (1, 4, 4, "random"), (1057, 64, 6, "skew"),
-          (8192, 8, 4, "all_to_one"), (4096, 8, 2, "random")]
+# The single-CTA build (ids staged in shared memory; the default for E <= 16 and
+# T*K <= 16384) and the three-launch build must give the same bit-exact index,
+# both forced on every case. Cases at the default threshold (T*K = 16384 with
+# E = 16) and just past it, at the shared-memory limit of a forced single CTA
+# (T*K = 32768 with E = 256) and past T*K = 32768, token counts that leave warps
+# partly or wholly idle, all tokens on one expert, and a Zipf-skewed routing
+# with idle experts.
+SINGLE = [(8192, 16, 2, "random"), (5462, 8, 3, "random"), (4096, 256, 8, "random"),
+          (16384, 8, 2, "random"), (32769, 4, 1, "random"), (31, 8, 2, "random"),
+          (1, 4, 4, "random"), (1057, 64, 6, "skew"), (8192, 8, 4, "all_to_one"),
+          (4096, 8, 2, "random")]
 
 
 @pytest.mark.parametrize("T,E,K,kind", SINGLE, ids=lambda v: str(v))

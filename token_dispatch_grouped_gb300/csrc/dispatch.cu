@@ -21,7 +21,7 @@
 //       (t, k) is the number of lower lanes in its warp's mask plus the counts
 //       of earlier warps; position = offsets[e] + base[block][e] + rank. This
 //       is exactly the order of a stable sort of the flattened ids by expert.
-// Layers with E <= 16 and T*K <= 32768 take a single launch instead: one CTA
+// Layers with E <= 16 and T*K <= 16384 take a single launch instead: one CTA
 // stages the ids in shared memory and runs the same three steps with warps in
 // place of blocks (dispatch_single_kernel below), which removes two launches
 // and the round trips of the block histogram through global memory.
@@ -207,7 +207,7 @@ dispatch_scatter_kernel(const int32_t* __restrict__ ids, int ld, int T, int E, i
 // token, so the index equals that of a stable sort of the flattened ids.
 constexpr int kSingleThreads = 1024;
 constexpr int kSingleWarps = kSingleThreads / 32;
-constexpr int kSingleMaxTK = 32768;
+constexpr int kSingleMaxTK = 16384;
 constexpr int kSingleMaxE = 16;  // default single-CTA builds: E <= 16
 constexpr size_t kSingleMaxSmem = 200 * 1024;
 
@@ -359,11 +359,13 @@ dispatch_single_kernel(const int32_t* __restrict__ ids, int T, int E, int32_t* _
     }
 }
 
-// Which build a shape takes: the single CTA while E <= 16, T*K <= 32768 and its
+// Which build a shape takes: the single CTA while E <= 16, T*K <= 16384 and its
 // shared memory fits, else D1..D3. Measured on GB300 (20 calls replayed from a
 // CUDA graph): 8.3 us against 9.2 us for D1..D3 at T = 4096, E = 8, K = 2, but
 // 52-87 us against 14-18 us at E = 64-128, where __match_any_sync meets up to
-// 32 distinct experts per warp and one SM does all the work.
+// 32 distinct experts per warp and one SM does all the work; under ncu the
+// single CTA took 10 us at T*K = 8192 and 27 us at T*K = 32768 (E = 8), where
+// the three launches take about 18 us.
 // MOE_DISPATCH=single|blocks forces one (single only where it fits); read at
 // every call.
 bool use_single(int T, int E, int K) {
