@@ -145,6 +145,7 @@ struct Params {
     int slot;      // G2_SLOT: routing slot k of this launch (of K = nslot)
     int nslot;
     const int32_t* tim;  // G2_SLOT: token_index_map
+    int half;      // 1: half-height pair tiles for the last partial tile (see half_ok)
     int part;      // row-tiled kinds: 0 all rows; 1 the rows of whole 256-row pair
                    // tiles plus remainders above 128 rows; 2 remainders of 1..128 rows
     int n_off;     // G2/G6: first output column of this launch (column chunk)
@@ -186,6 +187,23 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
     t.m_blk = local % mt;
     t.n_blk = local / mt;
     return t;
+}
+
+// Half-height pair tiles. A row-tiled CTA-pair tile whose expert has at most
+// 128 rows left (its last, partial tile) is issued as M = 128 cta_group::2 MMAs:
+// each CTA supplies 64 rows of A instead of 128, which halves the tile's MMA
+// work. The accumulator of such an MMA is folded in each CTA's TMEM (measured on
+// GB300): lanes 0..63 hold the CTA's 64 rows for the first N/2 columns and lanes
+// 64..127 the same rows for the last N/2 columns. So epilogue warps 2 and 3
+// (lane quarters 0, 1) take the CTA's rows 0..31 and 32..63 over the first half
+// of the columns, warps 4 and 5 (quarters 2, 3) the same rows over the second.
+// Kinds whose epilogue handles this set HALF.
+template <GemmKind KIND>
+__host__ __device__ constexpr bool half_ok() {
+    return KIND == G2_DOWN || KIND == G6_DX;
+}
+__device__ __forceinline__ bool half_tile(const Tile& t, int bmc) {
+    return t.hi - (t.lo + t.m_blk * bmc) <= bmc / 2;
 }
 
 // Warp-uniform bounded wait: every lane polls, all lanes agree on the result.
@@ -377,6 +395,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     constexpr int NMMA = BN;        // MMA N (for G1: 128 gate + 128 up columns)
     constexpr int BNL = C::BNL;     // N columns whose B rows this CTA stages
     constexpr uint32_t IDESC = idesc_bf16(BMC, NMMA, TR::A_MN, TR::B_MN);
+    // Half-height pair tiles (see half_ok): M = 128 over the pair, 64 rows per CTA.
+    constexpr bool HALF = PAIR && !VK && half_ok<KIND>();
+    constexpr uint32_t IDESC_HALF = idesc_bf16(BM, NMMA, TR::A_MN, TR::B_MN);
     // Bytes one CTA's TMA producer brings per stage (gather warps bring A otherwise).
     constexpr uint32_t TMA_BYTES = TR::A_G ? C::B_BYTES : C::A_BYTES + C::B_BYTES;
 
@@ -505,7 +526,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
             const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
-            const int row0 = t.lo + t.m_blk * BMC + rank * BM;   // VM: this CTA's A rows
+            const bool half = HALF && p.half && half_tile(t, BMC);
+            const int row0 = t.lo + t.m_blk * BMC + rank * (half ? BM / 2 : BM);  // VM: this CTA's A rows
             // First B column of the tile inside its half (G5: dW1 | dW3), and
             // this CTA's first B column in the B tensor.
             const int nin = (KIND == G5_DW13 ? t.n_blk % p.n_half : t.n_blk) * BN;
@@ -606,6 +628,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, PAIR)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * NMMA;
+                const uint32_t idesc = (HALF && p.half && half_tile(t, BMC)) ? IDESC_HALF : IDESC;
                 bool ok = true;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!warp_wait(full_bar(stage), phase, abort_flag, PAIR)) {
@@ -625,8 +648,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                                                          : sdesc_sw128(a_s + k * 32, 16, 1024);
                             const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, 8192, 1024)
                                                          : sdesc_sw128(b_s + k * 32, 16, 1024);
-                            if constexpr (PAIR) mma_bf16_pair(d_tmem, ad, bd, IDESC, (kb | k) != 0);
-                            else mma_bf16(d_tmem, ad, bd, IDESC, (kb | k) != 0 ? 1u : 0u);
+                            if constexpr (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                            else mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         }
                         if constexpr (PAIR) mma_commit_pair(empty_bar(stage));
                         else mma_commit(empty_bar(stage));
@@ -694,6 +717,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const uint32_t tacc = tmem_base + lane_addr + acc * NMMA;
             const int rbase = t.lo + t.m_blk * BMC + rank * BM;  // VM: first row of this CTA
             const int mbase = t.m_blk * BMC + rank * BM;         // VK: first output row
+            // This warp's rows and columns: 32 rows x all NMMA columns, or, in a
+            // half-height pair tile, 32 of the CTA's 64 rows x half the columns
+            // (TMEM column j - ccol0 holds logical column j).
+            const bool half = HALF && p.half && half_tile(t, BMC);
+            const int wrow0 = half ? t.lo + t.m_blk * BMC + rank * (BM / 2) + (q & 1) * 32
+                                   : rbase + q * 32;
+            const int ccol0 = half ? (q >> 1) * (NMMA / 2) : 0;
+            const int ncolw = half ? NMMA / 2 : NMMA;
             float v[32];
             if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
                 const int row0w = rbase + q * 32;  // this warp's first row
@@ -746,7 +777,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                 }
             } else if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
-                const int row0w = rbase + q * 32;
+                const int row0w = wrow0;
                 const int nvalid = t.hi - row0w;
                 __nv_bfloat16* out =
                     static_cast<__nv_bfloat16*>(p.out0) +
@@ -756,14 +787,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 float dzr = 0.f;
                 const float* wg = nullptr;
                 if constexpr (KIND == G6_DX) {
-                    const int r = rbase + row_in_tile;
+                    const int r = row0w + lane;
                     dzr = r < t.hi ? p.wrow[r] : 0.f;
                     wg = static_cast<const float*>(p.aux0) + static_cast<size_t>(t.e) * p.d +
                          p.n_off + t.n_blk * BN;
                 }
 #pragma unroll 1
-                for (int j = 0; j < BN; j += 32) {
-                    tmem_ld32f(tacc + j, v);
+                for (int j = ccol0; j < ccol0 + ncolw; j += 32) {
+                    tmem_ld32f(tacc + (j - ccol0), v);
                     if (nvalid > 0) {
                         if constexpr (KIND == G6_DX) {
 #pragma unroll
@@ -1344,6 +1375,12 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
     prm.dS_part = g.dS_part;
     prm.err = g.err;
     prm.part = part;
+    // Half-height pair tiles for an expert's last tile of at most 128 rows;
+    // MOE_GEMM_HALF=0 turns them off (read at every call).
+    {
+        const char* f = std::getenv("MOE_GEMM_HALF");
+        prm.half = (f != nullptr && f[0] == '0' && f[1] == '\0') ? 0 : 1;
+    }
     // Upper bound on the tile count (rows of all experts + one partial tile
     // per expert), only used to size the persistent grid.
     const int bmc = BM * ctas;
