@@ -215,7 +215,7 @@ size_t layout_bwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, BwdW
     const int nc = nchunks_of(s, tc);
     const size_t TK = static_cast<size_t>(s.T) * s.K;
     const int bn3 = gemm_bn(G3_DH, s);
-    const int nparts = (s.h + bn3 - 1) / bn3;
+    const int nparts = 2 * ((s.h + bn3 - 1) / bn3);  // two dS partial slots per G3 N tile
     Carve c;
     c.base = static_cast<char*>(ws);
     BwdWs w;
@@ -534,7 +534,7 @@ int backward_impl(const moe_shape& s, const RouteView& rv, const void* dy, const
     g3.err = err;
     MOE_TRY(launch_gemm(g3, st));
     const int bn3 = gemm_bn(G3_DH, s);
-    const int nparts = (s.h + bn3 - 1) / bn3;  // G3's N tiles, one dS partial each
+    const int nparts = 2 * ((s.h + bn3 - 1) / bn3);  // G3's N tiles, two dS partial slots each
     if (rm)
         MOE_TRY(launch_router_dz_rows(s, rows, nparts, w.dS_part, rv.tok_off, rv.tok_rows,
                                       rv.w_row, dS, w.dz_row, err, st));

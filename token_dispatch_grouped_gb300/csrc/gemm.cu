@@ -197,10 +197,15 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
 // 64..127 the same rows for the last N/2 columns. So epilogue warps 2 and 3
 // (lane quarters 0, 1) take the CTA's rows 0..31 and 32..63 over the first half
 // of the columns, warps 4 and 5 (quarters 2, 3) the same rows over the second.
-// Kinds whose epilogue handles this set HALF.
+// Kinds whose epilogue handles this set HALF. The SwiGLU up projection stages,
+// for a half tile, 64 gate rows and the matching 64 up rows of B in each CTA
+// (instead of 128 gate rows in one CTA and 128 up rows in the other), so every
+// warp holds matched gate and up columns. The dH GEMM's two warps of a row each
+// write their own dS partial (two partial slots per N tile).
 template <GemmKind KIND>
 __host__ __device__ constexpr bool half_ok() {
-    return KIND == G2_DOWN || KIND == G6_DX;
+    return KIND == G1_UP || KIND == G1_UP_ACT || KIND == G2_DOWN || KIND == G3_DH ||
+           KIND == G3_DH_ACT || KIND == G6_DX;
 }
 __device__ __forceinline__ bool half_tile(const Tile& t, int bmc) {
     return t.hi - (t.lo + t.m_blk * bmc) <= bmc / 2;
@@ -572,7 +577,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     if (lane == 0) {
                         if constexpr (KIND == G1_UP) {
                             const int brow = t.e * p.h + t.n_blk * 128;
-                            if constexpr (PAIR) {
+                            if (PAIR && half) {
+                                // 64 gate rows then the same 64 up rows (64-row boxes
+                                // of W1 and W3 in the A and output map slots).
+                                const int hrow = brow + static_cast<int>(rank) * 64;
+                                load(b_dst, &mapA, k0, hrow);
+                                load(b_dst + 8192, &mapO, k0, hrow);
+                            } else if constexpr (PAIR) {
                                 load(b_dst, leader ? &mapB0 : &mapB1, k0, brow);
                             } else {
                                 load(b_dst, &mapB0, k0, brow);
@@ -699,9 +710,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             // first kHR chunks, loaded while the MMA finishes the tile.
             int hrow = 0, hn0 = 0, hn = 0, hissued = 0;
             if constexpr (G3) {
-                hrow = t.lo + t.m_blk * BMC + rank * BM + q * 32;
-                hn0 = t.n_blk * BN;
-                hn = t.hi > hrow ? min(BN, p.h - hn0) / 32 : 0;
+                const bool hf = HALF && p.half && half_tile(t, BMC);
+                hrow = hf ? t.lo + t.m_blk * BMC + rank * (BM / 2) + (q & 1) * 32
+                          : t.lo + t.m_blk * BMC + rank * BM + q * 32;
+                hn0 = t.n_blk * BN + (hf ? (q >> 1) * (BN / 2) : 0);
+                hn = t.hi > hrow ? max(0, min(hf ? BN / 2 : BN, p.h - hn0)) / 32 : 0;
                 hissued = min(kHR, hn);
                 if (lane == 0 && hn > 0) {
                     bulk_wait_group_read<0>();  // earlier stores have read their slots
@@ -727,7 +740,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             const int ncolw = half ? NMMA / 2 : NMMA;
             float v[32];
             if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
-                const int row0w = rbase + q * 32;  // this warp's first row
+                const int row0w = wrow0;  // this warp's first row
                 const int nvalid = t.hi - row0w;
                 if constexpr (KIND == G1_UP_ACT) {
                     // Non-gated: 256 columns of a; H = a, A = act(a), both [TK, h].
@@ -736,8 +749,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) + r0 * p.h + n0;
                     __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) + r0 * p.h + n0;
 #pragma unroll 1
-                    for (int j = 0; j < 256; j += 32) {
-                        tmem_ld32f(tacc + j, v);
+                    for (int j = ccol0; j < ccol0 + ncolw; j += 32) {
+                        tmem_ld32f(tacc + (j - ccol0), v);
                         if (nvalid > 0) {
                             box_put_row(stg, lane, v);
                             box_store_rows(stg, lane, H + j, p.h, nvalid);
@@ -753,16 +766,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         }
                     }
                 } else {
-                    const int n0 = t.n_blk * 128;
+                    // Hidden units n0 .. n0 + nu of this warp; gate in TMEM columns
+                    // [0, nu), up in [ub, ub + nu): 128 units with up at 128, or in
+                    // a half tile 64 units with up at 64 (see the B loads).
+                    const int nu = half ? 64 : 128;
+                    const int n0 = t.n_blk * 128 + (q >> 1) * (half ? 64 : 0);
+                    const int ub = nu;
                     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out0) +
                                        static_cast<size_t>(row0w > 0 ? row0w : 0) * (2 * p.h) + n0;
                     __nv_bfloat16* Aact = static_cast<__nv_bfloat16*>(p.out1) +
                                           static_cast<size_t>(row0w > 0 ? row0w : 0) * p.h + n0;
 #pragma unroll 1
-                    for (int j = 0; j < 128; j += 32) {
+                    for (int j = 0; j < nu; j += 32) {
                         float b[32];
                         tmem_ld32f(tacc + j, v);
-                        tmem_ld32f(tacc + 128 + j, b);
+                        tmem_ld32f(tacc + ub + j, b);
                         if (nvalid > 0) {
                             box_put_row(stg, lane, v);
                             box_store_rows(stg, lane, H + j, 2 * p.h, nvalid);
@@ -856,7 +874,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 // dA' = dy W2_e is in TMEM, H arrives chunk by chunk in the ring.
                 // dH overwrites H in its slot; dH and A' leave by TMA when all 32
                 // rows of the warp are the expert's, else by row-masked stores.
-                const int r = rbase + row_in_tile;
+                const int r = hrow + lane;
                 const bool valid = r < t.hi;
                 const int nvalid = t.hi - hrow;
                 const float w = valid ? p.wrow[r] : 0.f;
@@ -924,7 +942,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         mbar_drain(h_bar(hc + k), ((hc + k) / kHR) & 1u);
                     stop = true;
                 } else if (valid) {
-                    p.dS_part[static_cast<size_t>(t.n_blk) * p.TK + r] = dsum;
+                    // Two partial slots per N tile: a half tile's two warps of a row
+                    // write one each; otherwise the second is zero.
+                    const size_t slot = 2 * static_cast<size_t>(t.n_blk) + (half ? (q >> 1) : 0);
+                    p.dS_part[slot * p.TK + r] = dsum;
+                    if (!half) p.dS_part[(slot + 1) * p.TK + r] = 0.f;
                 }
                 hc += hn;
             } else if constexpr (KIND == G4_DW2) {
@@ -1039,9 +1061,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 const int rb = g >> 3;
                 const uint32_t soff = static_cast<uint32_t>(rb * 128 + ((col16 ^ (rb & 7)) << 4));
                 auto load_idx = [&](const Tile& tt, int (&dst)[8]) {
+                    const bool hf = HALF && p.half && half_tile(tt, BMC);
+                    const int rcta = tt.lo + tt.m_blk * BMC + rank * (hf ? BM / 2 : BM);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int r = tt.lo + tt.m_blk * BMC + rank * BM + rb + 16 * j;
+                        const int r = rcta + rb + 16 * j;
                         if constexpr (KIND == G2_SLOT)
                             dst[j] = r < tt.hi ? p.tim[static_cast<size_t>(p.eti[r]) * p.nslot + p.slot]
                                                : -1;
@@ -1393,6 +1417,10 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
             if (gated) ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 128);
             else mp.b1 = mp.b0;
             mp.a = mp.o = mp.b0;
+            if (gated && ctas == 2) {  // half tiles: 64-row boxes of W1 and W3
+                ok &= make_tmap_bf16(&mp.a, g.b_src0, E * h, d, 64, 64);
+                ok &= make_tmap_bf16(&mp.o, g.b_src1, E * h, d, 64, 64);
+            }
             prm.Kdim = s.d;
             prm.n_tiles = gated ? s.h / 128 : s.h / 256;
             max_tiles = vm_mtiles * prm.n_tiles;
