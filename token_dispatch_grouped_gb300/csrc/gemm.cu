@@ -544,6 +544,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 }
                 if (leader && lane == 0) {
                     uint32_t bytes = CTAS * TMA_BYTES;
+                    if constexpr ((KIND == G2_DOWN || KIND == G6_DX) && HALF)
+                        if (half) bytes -= CTAS * (C::A_BYTES / 2);  // 64-row A boxes
                     if constexpr (KIND == G3_DH || KIND == G3_DH_ACT || KIND == G4_DW2 ||
                                   KIND == G5_DW13 || KIND == G7_DWG) {
                         // h need not be a multiple of BN: 64-column B boxes that
@@ -568,7 +570,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     else tma_load_2d(dst, m, fb, c0, c1);
                 };
                 if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
-                    if (lane == 0) load(a_dst, &mapA, k0, row0);
+                    // Half tiles read 64 rows (a 64-row box map in the output slot).
+                    if (lane == 0) load(a_dst, (HALF && half) ? &mapO : &mapA, k0, row0);
                 }
                 if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
                     // SwiGLU: B = 128 gate rows (W1) then 128 up rows (W3); in a
@@ -1066,6 +1069,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int r = rcta + rb + 16 * j;
+                        // A half tile's MMA reads the first 64 rows of the stage:
+                        // the rest are zero-filled without a read.
+                        if (hf && rb + 16 * j >= BM / 2) {
+                            dst[j] = -1;
+                            continue;
+                        }
                         if constexpr (KIND == G2_SLOT)
                             dst[j] = r < tt.hi ? p.tim[static_cast<size_t>(p.eti[r]) * p.nslot + p.slot]
                                                : -1;
@@ -1429,6 +1438,7 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
             ok &= make_tmap_bf16(&mp.a, g.a_src, TK, h, 64, 128);
             ok &= make_tmap_bf16(&mp.b0, g.b_src0, E * d, h, 64, bnl);
             mp.b1 = mp.o = mp.b0;
+            if (ctas == 2) ok &= make_tmap_bf16(&mp.o, g.a_src, TK, h, 64, 64);  // half tiles
             prm.Kdim = s.h;
             prm.n_off = g.n_off;
             prm.ldo = g.n_cols;
@@ -1495,6 +1505,7 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
             if (gated) ok &= make_tmap_bf16(&mp.b1, g.b_src1, E * h, d, 64, 64);
             else mp.b1 = mp.b0;
             mp.o = mp.b0;
+            if (ctas == 2) ok &= make_tmap_bf16(&mp.o, g.a_src, TK, hs, 64, 64);  // half tiles
             prm.Kdim = static_cast<int>(hs);
             prm.n_off = g.n_off;
             prm.ldo = g.n_cols;
