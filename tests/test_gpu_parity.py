@@ -115,11 +115,12 @@ def _ids_with_counts(T, K, counts, seed):
     return torch.from_numpy(ids.astype(np.int32))
 
 
-# CTA-pair GEMMs send an expert's last partial tile of at most 128 rows to a
-# single-CTA launch. Counts with remainders of 1 and 14 rows (split), an exact
-# multiple of 256 (none), 233 rows (stays in the pair launch), an expert of 100
-# rows (all remainder) and an empty expert; forward and backward on the injected
-# routing against the oracle, and against the unsplit pair launch.
+# CTA-pair GEMMs run an expert's last partial tile of at most 128 rows as a
+# half-height tile (M = 128 over the pair, 64 rows per CTA). Counts with
+# remainders of 1 and 14 rows (half tiles), an exact multiple of 256 (none), 233
+# rows (a whole tile), an expert of 100 rows (only a half tile) and an empty
+# expert; forward and backward on the injected routing against the oracle, and
+# against the same layer with whole tiles only (MOE_GEMM_HALF=0).
 REMAINDER = [(2300, 256, 2, 512, [1025, 1038, 1280, 1257], "swiglu"),
              (2000, 384, 3, 256, [1025, 1038, 1280, 1257, 0, 1400], "swiglu"),
              (2300, 256, 2, 512, [1025, 1038, 1280, 1257], "silu"),
@@ -128,7 +129,7 @@ REMAINDER = [(2300, 256, 2, 512, [1025, 1038, 1280, 1257], "swiglu"),
 
 @pytest.mark.parametrize("T,d,K,h,counts,expert", REMAINDER,
                          ids=lambda v: str(v) if not isinstance(v, list) else "-".join(map(str, v)))
-def test_partial_tile_remainders_single_cta(T, d, K, h, counts, expert, monkeypatch):
+def test_partial_tiles_half_height(T, d, K, h, counts, expert, monkeypatch):
     E = len(counts)
     s = I.Shape(T, d, E, K, h, expert)
     inp = I.make_layer_inputs(s, seed=8)
@@ -138,7 +139,7 @@ def test_partial_tile_remainders_single_cta(T, d, K, h, counts, expert, monkeypa
     from token_dispatch_grouped_gb300.layer import Routing
     out = {}
     for mode in ("1", "0"):
-        monkeypatch.setenv("MOE_GEMM_REMAINDER", mode)
+        monkeypatch.setenv("MOE_GEMM_HALF", mode)
         L = _layer(s)
         r = Routing(None, ids.cuda(), w.cuda())
         dp = L.dispatch(r.ids)
@@ -146,7 +147,7 @@ def test_partial_tile_remainders_single_cta(T, d, K, h, counts, expert, monkeypa
         g = L.backward(dv["dO"], dv["x"], dv["Wg"], dv["W1"], dv["W3"], dv["W2"], r, dp, H)
         L.check_error()
         out[mode] = (y, H, g)
-    monkeypatch.delenv("MOE_GEMM_REMAINDER")
+    monkeypatch.delenv("MOE_GEMM_HALF")
     assert np.array_equal(np.diff(cpu(dp.offsets)), np.array(counts))
     y, H, g = out["1"]
     f = O.layer_forward(inp["x"], inp["W1"], inp["W3"], inp["W2"], ids.numpy(), w.numpy(), expert)
@@ -158,7 +159,8 @@ def test_partial_tile_remainders_single_cta(T, d, K, h, counts, expert, monkeypa
         assert rel_fro(cpu(got), ref) <= TOL_BF16, name
         if name != "dS":
             assert rel_rows(cpu(got), ref) <= TOL_ROW, name
-    # the split and the unsplit launches sum the same products per row
+    # half and whole tiles sum the same products per row (the dS partials in
+    # another grouping)
     y0, H0, g0 = out["0"]
     assert rel_fro(cpu(y), cpu(y0).astype(np.float64)) <= 1e-3
     assert rel_fro(cpu(H), cpu(H0).astype(np.float64)) <= 1e-3

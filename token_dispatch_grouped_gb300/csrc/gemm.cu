@@ -146,8 +146,6 @@ struct Params {
     int nslot;
     const int32_t* tim;  // G2_SLOT: token_index_map
     int half;      // 1: half-height pair tiles for the last partial tile (see half_ok)
-    int part;      // row-tiled kinds: 0 all rows; 1 the rows of whole 256-row pair
-                   // tiles plus remainders above 128 rows; 2 remainders of 1..128 rows
     int n_off;     // G2/G6: first output column of this launch (column chunk)
     int ldo;       // G2/G6: row stride of the output chunk buffer (elements)
     const Seg* segs;
@@ -439,41 +437,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
 
     // Programmatic dependent launch (see pdl_wait in common.cuh): wait for the
-    // previous kernel, then let the next one be scheduled. A remainder launch
-    // (part 2) is the exception: its tiles are other rows of the pair launch
-    // just before it, whose own wait already covered the kernels before both,
-    // so it starts at once and waits for the pair launch only before it ends,
-    // so that later launches on the stream still follow both.
-    if (p.part != 2) griddep_wait();
+    // previous kernel, then let the next one be scheduled.
+    griddep_wait();
     griddep_launch_dependents();
     // Skip the work after an earlier error; a CTA of a pair never leaves alone
     // (its peer would wait at the cluster barrier), so pairs run on.
-    if (!PAIR && has_error(p.err)) {
-        griddep_wait();
-        return;
-    }
+    if (!PAIR && has_error(p.err)) return;
 
     // ---- setup: segments, tile prefix, barriers, TMEM
-    // Split launches of a row-tiled GEMM: an expert's last partial 256-row tile
-    // holding at most 128 rows leaves the pair launch (part 1) for a single-CTA
-    // launch with 128-row tiles (part 2), so that it costs one SM, not two.
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        Seg sg = p.segs[e];
-        if (p.part != 0) {
-            const int rows = sg.hi - sg.lo;
-            const int whole = rows / (2 * BM) * (2 * BM);
-            const bool split = rows > whole && rows - whole <= BM;
-            if (p.part == 1) {
-                if (split) sg.hi = sg.lo + whole;
-            } else if (split) {
-                sg.lo += whole;
-                sg.out += whole;
-            } else {
-                sg.lo = sg.hi;  // no remainder rows for this launch
-            }
-        }
-        s_segs[e] = sg;
-    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];
     __syncthreads();
     if (threadIdx.x == 0) {
         int run = 0;
@@ -1261,7 +1233,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
         else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    griddep_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -1374,9 +1345,8 @@ DwgPlan dwg_plan(const moe_shape& s) {
 
 namespace {
 
-// One launch of a GEMM problem with `ctas` CTAs per tile over the rows that
-// `part` selects (Params::part).
-cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStream_t st) {
+// One launch of a GEMM problem with `ctas` CTAs per tile.
+cudaError_t launch_gemm_ctas(const GemmProblem& g, int ctas, cudaStream_t st) {
     const moe_shape& s = g.s;
     // G2/G6 may cover a column chunk; their N tile must divide it.
     const int BN = (g.kind == G2_DOWN || g.kind == G6_DX) ? (g.n_cols % 256 == 0 ? 256 : 128)
@@ -1407,7 +1377,6 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
     prm.wrow = g.wrow;
     prm.dS_part = g.dS_part;
     prm.err = g.err;
-    prm.part = part;
     // Half-height pair tiles for an expert's last tile of at most 128 rows;
     // MOE_GEMM_HALF=0 turns them off (read at every call).
     {
@@ -1514,7 +1483,6 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
-    if (part == 2) max_tiles = s.E * prm.n_tiles;  // at most one 128-row tile per expert
     switch (g.kind) {
         case G1_UP:
             return gated ? launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu")
@@ -1534,32 +1502,10 @@ cudaError_t launch_gemm_part(const GemmProblem& g, int ctas, int part, cudaStrea
     return cudaErrorInvalidValue;
 }
 
-// Whether a row-tiled GEMM in CTA-pair mode sends each expert's last partial
-// tile of at most 128 rows to a second, single-CTA launch (which starts as the
-// pair launch's CTAs leave): a pair tile with r valid rows costs the MMA work of
-// 256 rows on two SMs, a single-CTA tile that of 128 rows on one SM. Off by
-// default: measured on GB300 it saved no time on the Mixtral-shaped, skewed or
-// fine-grained layers (0-2% slower), because a remainder tile that runs apart
-// from its expert's other tiles streams the expert's weight panel from DRAM
-// again (for the up projection of the Mixtral-shaped layer, about 1.3 GB) for
-// a handful of rows. MOE_GEMM_REMAINDER=1 turns it on (read at every call).
-bool split_remainders(const GemmProblem& g) {
-    const GemmKind kind = g.kind;
-    if (kind != G1_UP && kind != G2_DOWN && kind != G3_DH && kind != G6_DX) return false;
-    const char* f = std::getenv("MOE_GEMM_REMAINDER");
-    return f != nullptr && f[0] == '1' && f[1] == '\0';
-}
-
 }  // namespace
 
 cudaError_t launch_gemm(const GemmProblem& g, cudaStream_t st) {
-    const int ctas = choose_ctas(g.kind, g.s);
-    if (ctas == 2 && split_remainders(g)) {
-        const cudaError_t e = launch_gemm_part(g, 2, 1, st);
-        if (e != cudaSuccess) return e;
-        return launch_gemm_part(g, 1, 2, st);
-    }
-    return launch_gemm_part(g, ctas, 0, st);
+    return launch_gemm_ctas(g, choose_ctas(g.kind, g.s), st);
 }
 
 }  // namespace moe
