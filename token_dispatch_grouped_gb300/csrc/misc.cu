@@ -150,9 +150,12 @@ constexpr int comb_u() { return K >= 8 ? 1 : 8 / K; }
 // in the expert-sorted order): row(t, k) = token_index_map[t*K+k]. Otherwise
 // (token chunks) row(t, k) = seg[e].out + (token_index_map[t*K+k] - seg[e].lo)
 // with e = ids[t*K+k].
+// A work item is (token, column slice): the 2^cs_log2 slices of a token split
+// its nc columns evenly, so passes with few tokens still keep enough warps in
+// flight.
 template <int K, bool DIRECT>
 __global__ void __launch_bounds__(kCombThreads)
-combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict__ ids,
+combine_kernel(int t0, int t1, int c0, int nc, int d, int cs_log2, const int32_t* __restrict__ ids,
                const float* __restrict__ topk_w, const int32_t* __restrict__ tim,
                const Seg* __restrict__ seg, const __nv_bfloat16* __restrict__ Yc,
                __nv_bfloat16* __restrict__ y, int* err) {
@@ -160,8 +163,12 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
     pdl_trigger();
     if (has_error(err)) return;
     const int lane = threadIdx.x & 31;
-    for (int t = t0 + blockIdx.x * kCombWarps + threadIdx.x / 32; t < t1;
-         t += gridDim.x * kCombWarps) {
+    const int ncs = nc >> cs_log2;  // columns per slice
+    const int items = (t1 - t0) << cs_log2;
+    for (int it = blockIdx.x * kCombWarps + threadIdx.x / 32; it < items;
+         it += gridDim.x * kCombWarps) {
+        const int t = t0 + (it >> cs_log2);
+        const int cbeg = (it & ((1 << cs_log2) - 1)) * ncs;  // first column of the slice
         size_t off = 0;
         float wl = 0.f;
         if (lane < K) {
@@ -182,15 +189,16 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
             ok[k] = __shfl_sync(0xffffffffu, off, k);
             w[k] = __shfl_sync(0xffffffffu, wl, k);
         }
-        for (int cb = lane * 8; cb < nc; cb += 32 * 8 * U) {
+        const int cend = cbeg + ncs;
+        for (int cb = cbeg + lane * 8; cb < cend; cb += 32 * 8 * U) {
             uint4 v[K][U];
 #pragma unroll
             for (int k = 0; k < K; ++k)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int c = cb + u * 256;
-                    v[k][u] = c < nc ? *reinterpret_cast<const uint4*>(Yc + ok[k] + c)
-                                     : make_uint4(0, 0, 0, 0);
+                    v[k][u] = c < cend ? *reinterpret_cast<const uint4*>(Yc + ok[k] + c)
+                                       : make_uint4(0, 0, 0, 0);
                 }
             float acc[U][8];
 #pragma unroll
@@ -209,7 +217,7 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, const int32_t* __restrict_
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = cb + u * 256;
-                if (c < nc)
+                if (c < cend)
                     *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * d + c0 + c) =
                         f32_to_bf16x8(acc[u]);
             }
@@ -541,16 +549,25 @@ cudaError_t launch_combine(const moe_shape& s, int t0, int t1, int c0, int nc, c
                            const char* name, bool direct) {
     if (t1 <= t0) return cudaSuccess;
     LaunchScope ls(name, st);
-    const int grid = comb_grid(t1 - t0);
+    // Column slices per token: doubled while the pass has fewer than 24 warps'
+    // worth of items per SM and each slice keeps a multiple of 256 columns (one
+    // 16-byte piece per lane per row). Measured on GB300: MoEBlaze conf7's
+    // passes of 2048 tokens 0.40 -> 0.44 of HBM with slices; the Mixtral-shaped
+    // passes of 4096 tokens lost 1-4% with them, so they stay whole.
+    int cs_log2 = 0;
+    while (static_cast<long long>(t1 - t0) << cs_log2 < 24ll * num_sms() &&
+           nc % (512 << cs_log2) == 0)
+        ++cs_log2;
+    const int grid = comb_grid((t1 - t0) << cs_log2);
     switch (s.K) {
 #define MOE_COMBINE_CASE(KK)                                                                  \
     case KK:                                                                                  \
         if (direct)                                                                           \
-            launch_k(combine_kernel<KK, true>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d, ids, \
+            launch_k(combine_kernel<KK, true>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d, cs_log2, ids, \
                                                                     topk_w, tim, seg, Yc, y,  \
                                                                     err);                     \
         else                                                                                  \
-            launch_k(combine_kernel<KK, false>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d,     \
+            launch_k(combine_kernel<KK, false>, dim3(grid), dim3(kCombThreads), 0, st, t0, t1, c0, nc, s.d, cs_log2, \
                                                                      ids, topk_w, tim, seg,   \
                                                                      Yc, y, err);             \
         break;
