@@ -560,3 +560,27 @@ def test_full_workload_sampled(name):
         assert not cpu(g["dW1"][e]).any() and not cpu(g["dW2"][e]).any()
     for t in (y, g["dx"]):
         assert torch.isfinite(t).all()
+
+
+@pytest.mark.parametrize("s", [I.Shape(2100, 512, 4, 2, 512), I.Shape(1500, 128, 16, 1, 256)],
+                         ids=_sid)
+def test_programmatic_launch_modes_are_bit_identical(s, monkeypatch):
+    """Programmatic dependent launch only overlaps launch latency: with every
+    kernel launched that way (MOE_PDL=1), none (0), the small kernels only
+    (small) or the default (GEMMs only), the layer's outputs are the same bits."""
+    inp = to_dev(I.make_layer_inputs(s, seed=12))
+    L = _layer(s)
+    outs = {}
+    for mode in (None, "1", "0", "small"):
+        if mode is None:
+            monkeypatch.delenv("MOE_PDL", raising=False)
+        else:
+            monkeypatch.setenv("MOE_PDL", mode)
+        r, dp, y, H, g = L.step(inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], inp["dO"])
+        L.check_error()
+        outs[mode] = [t.clone() for t in (r.ids, r.w, dp.eti, dp.tim, y, H, *g.values())
+                      if t is not None]
+    monkeypatch.delenv("MOE_PDL", raising=False)
+    for mode in ("1", "0", "small"):
+        for a, b in zip(outs[None], outs[mode]):
+            assert torch.equal(a, b), mode
