@@ -41,7 +41,11 @@
  *   - Execution: every call enqueues kernels on `stream` (a cudaStream_t; NULL
  *     means the legacy default stream) and returns without waiting. Per-expert
  *     counts never leave the device. Workspace contents need not survive
- *     between calls.
+ *     between calls. Some kernels are launched with programmatic stream
+ *     serialization (the grouped GEMMs by default; MOE_PDL=1|0|small|gemm
+ *     chooses): such a kernel may be scheduled early but waits for the work
+ *     before it on the stream to complete before it reads or writes memory, so
+ *     stream order holds as for ordinary launches.
  *   - Errors: a call returns MOE_OK or a status code. Arguments that the host
  *     can check (null pointers, unsupported shapes, misalignment, workspace too
  *     small) are rejected before anything is launched. Errors that only the
