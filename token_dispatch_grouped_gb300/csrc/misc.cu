@@ -227,7 +227,7 @@ combine_kernel(int t0, int t1, int c0, int nc, int d, int cs_log2, const int32_t
 
 // One lane per (t, k): lanes K * j .. K * j + K - 1 of a warp hold token
 // j's slots (32 / K tokens per warp). A lane sums its routed row's partials
-// over the N tiles in order (loads issued 8 ahead), the token's lanes share
+// over the N tiles in order (loads issued 16 ahead), the token's lanes share
 // sum_j w_j dS_j through shuffles in slot order, and each lane writes its dS,
 // dz and the dz of its row.
 __global__ void __launch_bounds__(256)
@@ -251,12 +251,12 @@ router_dz_kernel(int T, int K, int TK, int nparts, const float* __restrict__ dS_
         r = tim[i];
         w = topk_w[i];
         int p = 0;
-        for (; p + 8 <= nparts; p += 8) {
-            float v[8];
+        for (; p + 16 <= nparts; p += 16) {
+            float v[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = dS_part[static_cast<size_t>(p + u) * TK + r];
+            for (int u = 0; u < 16; ++u) v[u] = dS_part[static_cast<size_t>(p + u) * TK + r];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) acc += v[u];
+            for (int u = 0; u < 16; ++u) acc += v[u];
         }
         for (; p < nparts; ++p) acc += dS_part[static_cast<size_t>(p) * TK + r];
     }
