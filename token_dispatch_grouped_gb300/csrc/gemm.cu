@@ -77,7 +77,7 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;                      // rows per CTA
-constexpr int BK = 64;                       // reduction depth per stage
+constexpr int BK0 = 64;                      // K elements in one 128-byte swizzled row
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait, then give up
 constexpr int kMaxE = 256;
 
@@ -97,11 +97,36 @@ template <> struct Tr<G2_SLOT> : Tr<G1_UP> {};  // gathered K-major A, K-major B
 template <> struct Tr<G3_DH_ACT> : Tr<G3_DH> {};
 template <> struct Tr<G7_DWG> : Tr<G4_DW2> {};  // gathered x (MN-major A), B rows MN-major
 
-template <int BN, int CTAS, int EPI_BOXES = 2>
+// Reduction depth per pipeline stage. A stage's handshake (barrier waits,
+// expect-tx, the gather warps' arrivals, the relay) costs about the same
+// whatever the stage holds, so deeper stages feed the MMA faster: measured on
+// GB300 with a probe of this kernel's feed (cp.async of 128 gathered rows plus
+// a TMA box per stage, one CTA per SM), 80 GB/s per SM with 32 KB stages
+// against 143 GB/s with 64 KB stages. CTA pairs of the up projection, the
+// weight gradients and dX take 128 (three 64 KB stages); the dH GEMM keeps 64,
+// since its epilogue's H ring would leave room for two 128-deep stages only
+// (measured 15-29% slower that way), and the down projections keep 64 (no
+// gain measured). A stage holds BK / BK0 sub-blocks of 64 K elements: K-major
+// operands as [rows x 64] tiles one after the other, MN-major operands as
+// 64-column chunks of BK rows.
+template <GemmKind KIND, int CTAS>
+__host__ __device__ constexpr int bk_of() {
+    return CTAS == 2 && (KIND == G1_UP || KIND == G1_UP_ACT || KIND == G4_DW2 ||
+                         KIND == G5_DW13 || KIND == G6_DX || KIND == G7_DWG)
+               ? 128
+               : 64;
+}
+
+template <int BN, int CTAS, int EPI_BOXES, int BK_>
 struct Cfg {
+    static constexpr int BK = BK_;
+    static constexpr int KSUB = BK / BK0;           // 64-deep sub-blocks per stage
     static constexpr int BNL = BN / CTAS;           // B rows (N) staged by this CTA
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BNL * BK * 2;
+    static constexpr int SUB_A = BM * BK0 * 2;      // K-major A: bytes per sub-block
+    static constexpr int SUB_B = BNL * BK0 * 2;     // K-major B: bytes per sub-block
+    static constexpr int CHUNK = BK * 128;          // MN-major: bytes per 64-column chunk
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int SMEM_MISC = 7168;        // barriers, TMEM slot, segments, tile prefix
     static constexpr int SMEM_EPI = 4 * EPI_BOXES * 2048;  // per epilogue warp: 32x32 bf16 boxes
@@ -391,12 +416,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB1,
                     const __grid_constant__ CUtensorMap mapO, const Params p) {
     using TR = Tr<KIND>;
-    using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND>(), bk_of<KIND, CTAS>()>;
     constexpr bool VK = TR::VK;
     constexpr bool PAIR = CTAS == 2;
     constexpr int BMC = BM * CTAS;  // rows per tile
     constexpr int NMMA = BN;        // MMA N (for G1: 128 gate + 128 up columns)
     constexpr int BNL = C::BNL;     // N columns whose B rows this CTA stages
+    constexpr int BK = C::BK;
+    constexpr int KSUB = C::KSUB;
     constexpr uint32_t IDESC = idesc_bf16(BMC, NMMA, TR::A_MN, TR::B_MN);
     // Half-height pair tiles (see half_ok): M = 128 over the pair, 64 rows per CTA.
     constexpr bool HALF = PAIR && !VK && half_ok<KIND>();
@@ -526,7 +553,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         bytes = 0;
                         for (int r = 0; r < CTAS; ++r)
                             for (int l = 0; l < BNL / 64; ++l)
-                                if (nin + r * BNL + l * 64 < p.h) bytes += 8192;
+                                if (nin + r * BNL + l * 64 < p.h) bytes += C::CHUNK;
                     }
                     // In a gathering pair, the relay's 16-byte signal copy.
                     if constexpr (TR::A_G && PAIR) bytes += 16;
@@ -543,53 +570,68 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 };
                 if constexpr (KIND == G2_DOWN || KIND == G6_DX) {
                     // Half tiles read 64 rows (a 64-row box map in the output slot).
-                    if (lane == 0) load(a_dst, (HALF && half) ? &mapO : &mapA, k0, row0);
+                    if (lane == 0)
+                        for (int u = 0; u < KSUB; ++u)
+                            load(a_dst + u * C::SUB_A, (HALF && half) ? &mapO : &mapA, k0 + u * BK0,
+                                 row0);
                 }
                 if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
                     // SwiGLU: B = 128 gate rows (W1) then 128 up rows (W3); in a
                     // pair the first CTA stages W1's rows and the second W3's.
                     // Non-gated: B = 256 consecutive rows of W1.
                     if (lane == 0) {
-                        if constexpr (KIND == G1_UP) {
-                            const int brow = t.e * p.h + t.n_blk * 128;
-                            if (PAIR && half) {
-                                // 64 gate rows then the same 64 up rows (64-row boxes
-                                // of W1 and W3 in the A and output map slots).
-                                const int hrow = brow + static_cast<int>(rank) * 64;
-                                load(b_dst, &mapA, k0, hrow);
-                                load(b_dst + 8192, &mapO, k0, hrow);
-                            } else if constexpr (PAIR) {
-                                load(b_dst, leader ? &mapB0 : &mapB1, k0, brow);
+                        for (int u = 0; u < KSUB; ++u) {
+                            const uint32_t bd = b_dst + u * C::SUB_B;
+                            const int kc = k0 + u * BK0;
+                            if constexpr (KIND == G1_UP) {
+                                const int brow = t.e * p.h + t.n_blk * 128;
+                                if (PAIR && half) {
+                                    // 64 gate rows then the same 64 up rows (64-row
+                                    // boxes of W1 and W3 in the A and output map slots).
+                                    const int hrow = brow + static_cast<int>(rank) * 64;
+                                    load(bd, &mapA, kc, hrow);
+                                    load(bd + 8192, &mapO, kc, hrow);
+                                } else if constexpr (PAIR) {
+                                    load(bd, leader ? &mapB0 : &mapB1, kc, brow);
+                                } else {
+                                    load(bd, &mapB0, kc, brow);
+                                    load(bd + 16384, &mapB1, kc, brow);
+                                }
                             } else {
-                                load(b_dst, &mapB0, k0, brow);
-                                load(b_dst + 16384, &mapB1, k0, brow);
-                            }
-                        } else {
-                            const int brow = t.e * p.h + t.n_blk * 256;
-                            if constexpr (PAIR) {
-                                load(b_dst, &mapB0, k0, brow + static_cast<int>(rank) * 128);
-                            } else {
-                                load(b_dst, &mapB0, k0, brow);
-                                load(b_dst + 16384, &mapB0, k0, brow + 128);
+                                const int brow = t.e * p.h + t.n_blk * 256;
+                                if constexpr (PAIR) {
+                                    load(bd, &mapB0, kc, brow + static_cast<int>(rank) * 128);
+                                } else {
+                                    load(bd, &mapB0, kc, brow);
+                                    load(bd + 16384, &mapB0, kc, brow + 128);
+                                }
                             }
                         }
                     }
                 } else if constexpr (KIND == G2_DOWN || KIND == G2_SLOT) {
-                    if (lane == 0) load(b_dst, &mapB0, k0, t.e * p.d + p.n_off + ncol);
+                    if (lane == 0)
+                        for (int u = 0; u < KSUB; ++u)
+                            load(b_dst + u * C::SUB_B, &mapB0, k0 + u * BK0, t.e * p.d + p.n_off + ncol);
                 } else if constexpr (KIND == G3_DH || KIND == G3_DH_ACT) {
                     if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
-                        load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.e * p.d + k0);
+                        for (int u = 0; u < KSUB; ++u)
+                            load(b_dst + lane * C::CHUNK + u * 8192, &mapB0, ncol + lane * 64,
+                                 t.e * p.d + k0 + u * BK0);
                 } else if constexpr (KIND == G4_DW2 || KIND == G5_DW13 || KIND == G7_DWG) {
                     // B rows of this expert (A' for dW2, dH for dW1/dW3; the chunk's
                     // rows of [dz_hi | dz_lo] for the router gradient), MN-major.
                     if (lane < BNL / 64 && nin + static_cast<int>(rank) * BNL + lane * 64 < p.h)
-                        load(b_dst + lane * 8192, &mapB0, ncol + lane * 64, t.lo + k0);
+                        for (int u = 0; u < KSUB; ++u)
+                            load(b_dst + lane * C::CHUNK + u * 8192, &mapB0, ncol + lane * 64,
+                                 t.lo + k0 + u * BK0);
                 } else {  // G6: K = 2h, first h from W1, then W3 (non-gated: K = h, W1).
+                    // h % 128 == 0, so a stage never straddles the W1 | W3 boundary.
                     if (lane < BNL / 64) {
                         const bool up = p.act == 0 && k0 >= p.h;
                         const int brow = t.e * p.h + (up ? k0 - p.h : k0);
-                        load(b_dst + lane * 8192, up ? &mapB1 : &mapB0, p.n_off + ncol + lane * 64,
-                             brow);
+                        for (int u = 0; u < KSUB; ++u)
+                            load(b_dst + lane * C::CHUNK + u * 8192, up ? &mapB1 : &mapB0,
+                                 p.n_off + ncol + lane * 64, brow + u * BK0);
                     }
                 }
                 if (++stage == C::STAGES) {
@@ -630,10 +672,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         const uint32_t b_s = sB + stage * C::B_BYTES;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t ad = TR::A_MN ? sdesc_sw128(a_s + k * 2048, 8192, 1024)
-                                                         : sdesc_sw128(a_s + k * 32, 16, 1024);
-                            const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, 8192, 1024)
-                                                         : sdesc_sw128(b_s + k * 32, 16, 1024);
+                            // K-major: sub-block k / 4, 32 bytes per 16 K; MN-major: 16
+                            // rows of 128 bytes per 16 K, chunks of 64 columns CHUNK apart.
+                            const uint32_t ka = (k >> 2) * C::SUB_A + (k & 3) * 32;
+                            const uint32_t kb2 = (k >> 2) * C::SUB_B + (k & 3) * 32;
+                            const uint64_t ad = TR::A_MN ? sdesc_sw128(a_s + k * 2048, C::CHUNK, 1024)
+                                                         : sdesc_sw128(a_s + ka, 16, 1024);
+                            const uint64_t bd = TR::B_MN ? sdesc_sw128(b_s + k * 2048, C::CHUNK, 1024)
+                                                         : sdesc_sw128(b_s + kb2, 16, 1024);
                             if constexpr (PAIR) mma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
                             else mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         }
@@ -1072,10 +1118,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         const uint32_t a_dst = sA + stage * C::A_BYTES + soff;
                         const size_t coff = static_cast<size_t>(kb * BK) * 2 + col16 * 16;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const char* src = src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff : 0);
-                            cp_async16(a_dst + j * 16 * 128, src, idx[j] >= 0 ? 16u : 0u);
-                        }
+                        for (int u = 0; u < KSUB; ++u)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const char* src =
+                                    src0 + (idx[j] >= 0 ? idx[j] * rowbytes + coff + u * 128 : 0);
+                                cp_async16(a_dst + u * C::SUB_A + j * 16 * 128, src,
+                                           idx[j] >= 0 ? 16u : 0u);
+                            }
                         cp_async_arrive_noinc(done_bar(stage));
                         if (++stage == C::STAGES) {
                             stage = 0;
@@ -1086,18 +1136,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     for (int j = 0; j < 8; ++j) idx[j] = nidx[j];
                 }
             } else {
-                // MN-major A: 64 k-rows (tokens) x 128 m-columns in two 64-column
-                // chunks of 8 KB; this thread copies 16-byte chunk col16 of column
-                // chunk ch for token rows rb + 8 j, j = 0..7. Work items (tile,
-                // k-block) change their row indices every k-block, so the indices
-                // are loaded kLook items ahead (a ring of register slots, about a
-                // microsecond of lead); tiles of experts without rows have no
-                // k-blocks and are skipped.
-                constexpr int kLook = 4;
+                // MN-major A: BK k-rows (tokens) x 128 m-columns in two 64-column
+                // chunks of BK x 128 bytes; this thread copies 16-byte chunk col16 of
+                // column chunk ch for token rows rb + 8 j, j < BK / 8. Work items
+                // (tile, k-block) change their row indices every k-block, so the
+                // indices are loaded kLook items ahead (a ring of register slots,
+                // about a microsecond of lead); tiles of experts without rows have
+                // no k-blocks and are skipped.
+                constexpr int NR = BK / 8;             // token rows per thread and item
+                constexpr int kLook = 4 * BK0 / BK;    // items of lookahead (same lead)
                 const int ch = (g >> 3) & 1;
                 const int rb = g >> 4;
                 const uint32_t soff =
-                    static_cast<uint32_t>(ch * 8192 + rb * 128 + ((col16 ^ (rb & 7)) << 4));
+                    static_cast<uint32_t>(ch * C::CHUNK + rb * 128 + ((col16 ^ (rb & 7)) << 4));
                 struct Pos {
                     int tile, kb, nkb;
                     Tile t;
@@ -1123,15 +1174,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     }
                     return first_from(ps.tile + tstep, ps);
                 };
-                auto load_idx = [&](const Pos& ps, int (&dst)[8]) {
+                auto load_idx = [&](const Pos& ps, int (&dst)[NR]) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < NR; ++j) {
                         const int r = ps.t.lo + ps.kb * BK + rb + 8 * j;
                         dst[j] = r < ps.t.hi ? p.eti[r] : -1;
                     }
                 };
                 Pos slot[kLook];
-                int idx[kLook][8];
+                int idx[kLook][NR];
                 bool have[kLook];
                 Pos tail{};
                 bool more = first_from(tile0, tail);  // tail: the next item to prefetch
@@ -1161,7 +1212,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                             static_cast<size_t>(slot[u].t.m_blk * BMC + rank * BM + ch * 64) * 2 +
                             col16 * 16;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
+                        for (int j = 0; j < NR; ++j) {
                             const int ix = idx[u][j];
                             const char* src = src0 + (ix >= 0 ? ix * rowbytes + coff : 0);
                             cp_async16(a_dst + j * 8 * 128, src, ix >= 0 ? 16u : 0u);
@@ -1244,7 +1295,7 @@ template <GemmKind KIND, int BN, int CTAS>
 cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                         const char* name) {
     const bool pdl = pdl_enabled(true);
-    using C = Cfg<BN, CTAS, epi_boxes<KIND>()>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND>(), bk_of<KIND, CTAS>()>;
     auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
