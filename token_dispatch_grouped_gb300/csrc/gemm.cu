@@ -190,7 +190,9 @@ struct Tile {
 
 // Tile order inside one expert: M fastest, so tiles that run at the same time
 // share their B panel (a weight panel for the VM kinds, the A' or dH panel
-// for the weight gradients). bmc = rows per tile (128 or 256).
+// for the weight gradients). bmc = rows per tile (128 or 256). The weight-
+// gradient kinds (vk) walk the segments sorted by row count, each carrying
+// its expert in `pad`.
 __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const Seg* segs, int E,
                                             bool vk, int m_tiles_vk, int bmc) {
     int lo = 0, hi = E;  // largest e with prefix[e] <= tile
@@ -200,8 +202,8 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* prefix, const S
         else hi = mid;
     }
     Tile t;
-    t.e = lo;
     const Seg s = segs[lo];
+    t.e = vk ? s.pad : lo;
     t.lo = s.lo;
     t.hi = s.hi;
     t.out = s.out;
@@ -462,6 +464,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     const bool leader = rank == 0;
     const int tile0 = blockIdx.x / CTAS;   // first tile of this CTA (pair)
     const int tstep = gridDim.x / CTAS;    // tiles advance by the number of pairs
+    // Tiles are dealt in waves of one per pair. The weight-gradient kinds deal
+    // them in snake order (even waves pairs 0..n-1, odd waves n-1..0) over the
+    // experts sorted by row count, largest first: a tile's cost grows with its
+    // expert's rows, and on Zipf-skewed routing this keeps the longest pair's
+    // share within about 4% of the mean (11-14% in expert order). Row-tiled
+    // kinds (tiles of one cost) keep a plain round-robin in expert order.
+    auto next_tile = [&](int tl) -> int {
+        if constexpr (VK) {
+            const int w = tl / tstep + 1;
+            return w * tstep + ((w & 1) ? tstep - 1 - tile0 : tile0);
+        } else {
+            return tl + tstep;
+        }
+    };
 
     // Programmatic dependent launch (see pdl_wait in common.cuh): wait for the
     // previous kernel, then let the next one be scheduled.
@@ -474,6 +490,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     // ---- setup: segments, tile prefix, barriers, TMEM
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_segs[e] = p.segs[e];
     __syncthreads();
+    if constexpr (VK) {
+        // Segments sorted by row count, largest first, ties by index (every CTA
+        // computes the same order); thread e places expert e at its rank.
+        static_assert(threads_of<KIND, CTAS>() >= kMaxE, "one thread per expert");
+        Seg mine{0, 0, 0, 0};
+        int rk = 0;
+        const int e = threadIdx.x;
+        if (e < E) {
+            mine = s_segs[e];
+            const int rows = mine.hi - mine.lo;
+            for (int f = 0; f < E; ++f) {
+                const int rf = s_segs[f].hi - s_segs[f].lo;
+                rk += (rf > rows || (rf == rows && f < e)) ? 1 : 0;
+            }
+            mine.pad = e;
+        }
+        __syncthreads();
+        if (e < E) s_segs[rk] = mine;
+        __syncthreads();
+    }
     if (threadIdx.x == 0) {
         int run = 0;
         for (int e = 0; e < E; ++e) {
@@ -527,7 +563,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         int stage = 0;
         uint32_t phase = 0;
         bool stop = false;
-        for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
+        for (int tile = tile0; tile < num_tiles && !stop; tile = next_tile(tile)) {
             const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
             const bool half = HALF && p.half && half_tile(t, BMC);
@@ -646,7 +682,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
-            for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
+            for (int tile = tile0; tile < num_tiles; tile = next_tile(tile), ++it) {
                 const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
                 const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
                 const int acc = it & 1;
@@ -722,7 +758,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
             if constexpr (KIND == G3_DH) tma_load_2d(dst + 2048, &mapA, h_bar(c), p.h + col, row);
         };
         int it = 0;
-        for (int tile = tile0; tile < num_tiles; tile += tstep, ++it) {
+        for (int tile = tile0; tile < num_tiles; tile = next_tile(tile), ++it) {
             const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
@@ -1104,8 +1140,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 int tile = tile0;
                 if (tile < num_tiles)
                     load_idx(decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC), idx);
-                for (; tile < num_tiles && !stop; tile += tstep) {
-                    const int ntile = tile + tstep;
+                for (; tile < num_tiles && !stop; tile = next_tile(tile)) {
+                    const int ntile = next_tile(tile);
                     if (ntile < num_tiles)
                         load_idx(decode_tile(ntile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC),
                                  nidx);
@@ -1154,7 +1190,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     Tile t;
                 };
                 auto first_from = [&](int tile, Pos& ps) -> bool {
-                    for (; tile < num_tiles; tile += tstep) {
+                    for (; tile < num_tiles; tile = next_tile(tile)) {
                         const Tile tt = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
                         const int nk = (tt.hi - tt.lo + BK - 1) / BK;
                         if (nk > 0) {
@@ -1172,7 +1208,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                         ++ps.kb;
                         return true;
                     }
-                    return first_from(ps.tile + tstep, ps);
+                    return first_from(next_tile(ps.tile), ps);
                 };
                 auto load_idx = [&](const Pos& ps, int (&dst)[NR]) {
 #pragma unroll
@@ -1246,7 +1282,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                 uint32_t phase = 0;
                 bool stop = false;
                 const uint32_t dst = mapa_shared(relay_slot, 0);
-                for (int tile = tile0; tile < num_tiles && !stop; tile += tstep) {
+                for (int tile = tile0; tile < num_tiles && !stop; tile = next_tile(tile)) {
                     const Tile t = decode_tile(tile, s_prefix, s_segs, E, VK, m_tiles_vk, BMC);
                     const int num_kb = VK ? (t.hi - t.lo + BK - 1) / BK : p.Kdim / BK;
                     for (int kb = 0; kb < num_kb; ++kb) {
@@ -1376,10 +1412,11 @@ int gemm_bn(GemmKind kind, const moe_shape& s) {
 
 // Router-gradient split: B has nw = 2 * e_pad columns; the token range is cut
 // into chunks (multiples of 64 tokens, at least 256 unless T is smaller, at
-// most about 8192) so that the tile count is at least about 152 (two waves of
-// CTA pairs on a 152-SM GB300) and no tile's reduction runs much past 128
-// k-blocks. The split depends on the shape alone, so workspace sizes need no
-// device.
+// most about 8192 while that needs no more than 256 chunks) so that the tile
+// count is at least about 152 (two waves of CTA pairs on a 152-SM GB300) and
+// no tile's reduction runs much past 64 k-blocks. The GEMM holds at most 256
+// segments (kMaxE), so layers of more than 2^21 tokens take longer chunks.
+// The split depends on the shape alone, so workspace sizes need no device.
 DwgPlan dwg_plan(const moe_shape& s) {
     DwgPlan p{};
     p.e_pad = (s.E + 63) / 64 * 64;
@@ -1388,7 +1425,7 @@ DwgPlan dwg_plan(const moe_shape& s) {
     const int bmc = (s.d % 256 == 0) ? 256 : 128;  // CTA pairs when d % 256 == 0
     const int tiles_per_chunk = (s.d / bmc) * ((p.nw + bn - 1) / bn);
     int n = std::max((152 + tiles_per_chunk - 1) / tiles_per_chunk, (s.T + 8191) / 8192);
-    n = std::max(1, std::min(n, s.T / 256));
+    n = std::max(1, std::min(std::min(n, s.T / 256), kMaxE));
     p.chunk = ((s.T + n - 1) / n + 63) / 64 * 64;
     p.nchunks = (s.T + p.chunk - 1) / p.chunk;
     return p;
@@ -1534,6 +1571,7 @@ cudaError_t launch_gemm_ctas(const GemmProblem& g, int ctas, cudaStream_t st) {
             break;
     }
     if (!ok) return cudaErrorInvalidValue;
+    if (prm.E < 1 || prm.E > kMaxE) return cudaErrorInvalidValue;  // segments held in shared memory
     switch (g.kind) {
         case G1_UP:
             return gated ? launch_ctas<G1_UP>(ctas, BN, mp, prm, max_tiles, st, "g1_up_swiglu")
