@@ -23,9 +23,10 @@
 //               only signal a barrier of its own CTA) as the byte count of a
 //               16-byte bulk copy into the first CTA.
 // The accumulator is double-buffered in TMEM, so the epilogue of one tile
-// overlaps the main loop of the next. Tiles are walked in a static
-// round-robin over a device-side tile list derived from the per-expert row
-// ranges (counts never go to the host).
+// overlaps the main loop of the next. Tiles are dealt statically over a
+// device-side tile list derived from the per-expert row ranges (counts never
+// go to the host): round-robin for the row-tiled kinds, snake order over the
+// experts sorted by rows for the weight gradients (see next_tile).
 //
 // The six GEMMs (T_e = rows of expert e, all bf16 with fp32 accumulation):
 //   G1  [T_e, d] x [d, h|h]  gather x; B = W1_e, W3_e (K-major);
