@@ -157,15 +157,15 @@ def test_workspace_follows_the_pass_and_router_gradient_rules(monkeypatch):
     monkeypatch.delenv("MOE_COLUMN_PASSES")
     assert A + TK * 2048 * 2 <= two < A + TK * 2048 * 2 + 2**20    # half-width chunk
     assert A + TK * 1024 * 2 <= four < A + TK * 1024 * 2 + 2**20   # quarter-width chunk
-    # router gradient: gathered path (32 row parts per expert) below 64 MiB of x ...
+    # router gradient: gathered path (P row parts per expert, P from the shape) below 64 MiB of x ...
     gather = B.moe_workspace_size(s, B.MOE_WS_BACKWARD)
     monkeypatch.setenv("MOE_ROUTER_DWG", "mma")
     mma = B.moe_workspace_size(s, B.MOE_WS_BACKWARD)
     monkeypatch.delenv("MOE_ROUTER_DWG")
     # ... the tensor-core path adds B = [dz_hi | dz_lo] [T, 128] bf16, the identity list
-    # and fp32 chunk partials [chunks, d, 128] in place of [32, E, d] fp32 parts
+    # and fp32 chunk partials [chunks, d, 128] in place of [P, E, d] fp32 parts (P = 76 here)
     diff = mma - gather
-    assert diff >= 4096 * 128 * 2 + 4096 * 4 + 4096 * 128 * 4 - 32 * 8 * 4096 * 4
+    assert diff >= 4096 * 128 * 2 + 4096 * 4 + 4096 * 128 * 4 - 76 * 8 * 4096 * 4
     # skew-shaped (x = 128 MiB): the tensor-core path is the default
     k = B.shape(32768, 2048, 128, 8, 768)
     default = B.moe_workspace_size(k, B.MOE_WS_BACKWARD)

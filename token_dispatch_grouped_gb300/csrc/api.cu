@@ -238,7 +238,7 @@ size_t layout_bwd(const moe_shape& s, size_t rows, bool row_mode, void* ws, BwdW
         w.dwg_B = nullptr;
         w.dwg_iota = nullptr;
         w.dwg_segs = nullptr;
-        w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts()) * s.E * s.d);
+        w.dwg_part = c.take<float>(static_cast<size_t>(dwg_parts(s)) * s.E * s.d);
     }
     if (o) *o = w;
     return align_up(c.off, 256);

@@ -187,7 +187,7 @@ cudaError_t launch_router_dz(const moe_shape& s, int nparts, const float* dS_par
 // Router weight gradient dW_g = dz^T x (R2b), gathered per expert (x rows
 // read through eti, fp32 sums over 32 row parts of each expert, then a
 // fixed-order sum): used while x fits in L2.
-int dwg_parts();
+int dwg_parts(const moe_shape& s);
 cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
                               const int32_t* offsets, const float* dz_row, float* part,
                               float* dWg, int* err, cudaStream_t st);

@@ -366,67 +366,112 @@ __global__ void router_dz_rows_kernel(int T, int rows_cap, int nparts,
     }
 }
 
-constexpr int kDwgParts = 32;      // row parts per expert
 constexpr int kDwgCols = 2048;     // columns per CTA (256 threads x 8)
 
 // dW_g[e] = sum over expert e's rows r of dz_row[r] * x[eti[r]] (the router
 // gradient dz^T x, with dz non-zero only at the chosen experts). grid =
-// (E, ceil(d / 2048), 32): CTA (e, cb, z) sums the z-th of 32 equal parts of
-// e's rows for 2048 columns, 8 per thread, rows in ascending order.
+// (E, ceil(d / 2048), P): CTA (e, cb, z) sums the z-th of P equal parts of
+// e's rows for up to 2048 columns, 8 per thread. When d < 2048 the CTA's
+// threads form G = 256 / (d / 8) groups, group g taking rows r0 + g,
+// r0 + g + G, ... in ascending order; the groups' sums are then added in group
+// order, so every partial has one fixed summation order. GROUPED: d < 2048.
+template <bool GROUPED>
 __global__ void __launch_bounds__(256)
-router_dwg_part_kernel(int d, int E, const __nv_bfloat16* __restrict__ x,
+router_dwg_part_kernel(int d, int E, int P, const __nv_bfloat16* __restrict__ x,
                        const int32_t* __restrict__ eti, const int32_t* __restrict__ offsets,
                        const float* __restrict__ dz_row, float* __restrict__ part, int* err) {
     pdl_wait();
     pdl_trigger();
-    if (has_error(err)) return;
+    if (has_error(err)) return;  // uniform over the CTA
     const int e = blockIdx.x;
-    const int c = blockIdx.y * kDwgCols + threadIdx.x * 8;
     const int z = blockIdx.z;
+    const int gt = GROUPED ? d / 8 : 256;  // threads per row group
+    const int G = GROUPED ? 256 / gt : 1;  // row groups
+    const int g = threadIdx.x / gt;
+    const int c = blockIdx.y * kDwgCols + (threadIdx.x % gt) * 8;
+    const bool active = g < G && c < d;
     const int lo = offsets[e], len = offsets[e + 1] - lo;
-    const int r0 = lo + static_cast<int>(static_cast<long long>(len) * z / kDwgParts);
-    const int r1 = lo + static_cast<int>(static_cast<long long>(len) * (z + 1) / kDwgParts);
-    if (c >= d) return;
+    const int r0 = lo + static_cast<int>(static_cast<long long>(len) * z / P);
+    const int r1 = lo + static_cast<int>(static_cast<long long>(len) * (z + 1) / P);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int r = r0;
-    for (; r + 4 <= r1; r += 4) {
-        uint4 v[4];
-        float zz[4];
+    if (active) {
+        int r = r0 + g;
+        for (; r + 3 * G < r1; r += 4 * G) {
+            uint4 v[4];
+            float zz[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            v[q] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r + q]) * d + c);
-            zz[q] = dz_row[r + q];
+            for (int q = 0; q < 4; ++q) {
+                v[q] = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r + q * G]) * d + c);
+                zz[q] = dz_row[r + q * G];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+                bf16x8_to_f32(v[q], f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(zz[q], f[j], acc[j]);
+            }
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (; r < r1; r += G) {
             float f[8];
-            bf16x8_to_f32(v[q], f);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r]) * d + c), f);
+            const float zq = dz_row[r];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = fmaf(zz[q], f[j], acc[j]);
+            for (int j = 0; j < 8; ++j) acc[j] = fmaf(zq, f[j], acc[j]);
         }
     }
-    for (; r < r1; ++r) {
-        float f[8];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + static_cast<size_t>(eti[r]) * d + c), f);
-        const float zq = dz_row[r];
+    if constexpr (GROUPED) {
+        __shared__ float red[256 * 8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(zq, f[j], acc[j]);
+        for (int j = 0; j < 8; ++j) red[threadIdx.x * 8 + j] = acc[j];
+        __syncthreads();
+        if (g == 0) {
+            for (int q = 1; q < G; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] += red[(q * gt + threadIdx.x) * 8 + j];
+        }
     }
-    float* out = part + (static_cast<size_t>(z) * E + e) * d + c;
-    *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(out + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (g == 0 && c < d) {
+        float* out = part + (static_cast<size_t>(z) * E + e) * d + c;
+        *reinterpret_cast<float4*>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(out + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
 }
 
-__global__ void router_dwg_reduce_kernel(int n, const float* __restrict__ part,
-                                         float* __restrict__ dWg, int* err) {
+// dWg[i] = sum of the P partials part[q * n + i] in a fixed order. SPLIT
+// (fewer than 65536 outputs, too few threads for one per output): 32 outputs
+// per CTA (one per lane), warp w sums the parts q = w, w + 8, ... in ascending
+// order, and the eight warp sums are added in warp order. Otherwise one thread
+// per output sums q = 0, 1, ... in order.
+template <bool SPLIT>
+__global__ void __launch_bounds__(256)
+router_dwg_reduce_kernel(int n, int P, const float* __restrict__ part, float* __restrict__ dWg,
+                         int* err) {
     pdl_wait();
     pdl_trigger();
-    if (has_error(err)) return;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
+    if (has_error(err)) return;  // uniform over the CTA
+    if constexpr (!SPLIT) {
+        const int i = blockIdx.x * blockDim.x + threadIdx.x;
+        if (i >= n) return;
+        float s = 0.f;
+        for (int q = 0; q < P; ++q) s += part[static_cast<size_t>(q) * n + i];
+        dWg[i] = s;
+        return;
+    }
+    __shared__ float ws[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int i = blockIdx.x * 32 + lane;
     float s = 0.f;
-    for (int q = 0; q < kDwgParts; ++q) s += part[static_cast<size_t>(q) * n + i];
-    dWg[i] = s;
+    if (i < n)
+        for (int q = w; q < P; q += 8) s += part[static_cast<size_t>(q) * n + i];
+    ws[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && i < n) {
+        float t = ws[0][lane];
+#pragma unroll
+        for (int q = 1; q < 8; ++q) t += ws[q][lane];
+        dWg[i] = t;
+    }
 }
 
 // Router-gradient operand: zero B [T, nw] (16-byte pieces), the identity
@@ -612,20 +657,39 @@ cudaError_t launch_router_dz_rows(const moe_shape& s, int rows_cap, int nparts,
     return cudaGetLastError();
 }
 
-int dwg_parts() { return kDwgParts; }
+// Row parts per expert of the gathered router gradient: enough CTAs for
+// about eight 256-thread CTAs per SM of a 152-SM GB300 (1216), at least 32 and
+// at most 256. Depends on the shape alone (workspace sizes need no device).
+int dwg_parts(const moe_shape& s) {
+    const int cb = (s.d + kDwgCols - 1) / kDwgCols;
+    const int want = (1216 + s.E * cb - 1) / (s.E * cb);
+    return std::max(32, std::min(256, want));
+}
 
 cudaError_t launch_router_dwg(const moe_shape& s, const __nv_bfloat16* x, const int32_t* eti,
                               const int32_t* offsets, const float* dz_row, float* part,
                               float* dWg, int* err, cudaStream_t st) {
+    const int P = dwg_parts(s);
     {
         LaunchScope ls("router_dwg", st);
-        launch_k(router_dwg_part_kernel, dim3(dim3(s.E, (s.d + kDwgCols - 1) / kDwgCols, kDwgParts)), dim3(256), 0, st, s.d, s.E, x, eti, offsets, dz_row, part, err);
+        const dim3 grid(s.E, (s.d + kDwgCols - 1) / kDwgCols, P);
+        if (s.d < kDwgCols)
+            launch_k(router_dwg_part_kernel<true>, grid, dim3(256), 0, st, s.d, s.E, P, x, eti,
+                     offsets, dz_row, part, err);
+        else
+            launch_k(router_dwg_part_kernel<false>, grid, dim3(256), 0, st, s.d, s.E, P, x, eti,
+                     offsets, dz_row, part, err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int n = s.E * s.d;
     LaunchScope ls("router_dwg_reduce", st);
-    launch_k(router_dwg_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, st, n, part, dWg, err);
+    if (n < 65536)
+        launch_k(router_dwg_reduce_kernel<true>, dim3((n + 31) / 32), dim3(256), 0, st, n, P, part,
+                 dWg, err);
+    else
+        launch_k(router_dwg_reduce_kernel<false>, dim3((n + 255) / 256), dim3(256), 0, st, n, P,
+                 part, dWg, err);
     return cudaGetLastError();
 }
 
