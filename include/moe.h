@@ -107,11 +107,12 @@ size_t moe_workspace_size(moe_shape s, int which);
 /* Transient-buffer bound: moe_forward runs the down projection and the
  * weighted combine (and moe_backward the dX of the up projection and the
  * token-gradient sum) in passes once T >= 1024, so the expert-output buffer
- * holds at most about a quarter of T*K*d elements (never the whole routed
- * T*K*d buffer). A pass covers either a chunk of tokens (four chunks) or,
- * when d is a multiple of 512, a slice of the output columns: a quarter of
- * them, or half of them when that half-width buffer is at most 64 MiB (small
- * layers; the environment variable MOE_COLUMN_PASSES=2|4 forces a count).
+ * holds at most about a quarter of T*K*d elements, or half of them when that
+ * half buffer is at most 64 MiB (small layers); never the whole routed T*K*d
+ * buffer. A pass covers either a chunk of tokens (two or four chunks by that
+ * rule) or, when d is a multiple of 512, a slice of the output columns (half
+ * or a quarter of them by the same rule; the environment variable
+ * MOE_COLUMN_PASSES=2|4 forces the column-pass count).
  * The library takes the split that re-reads fewer bytes (token chunks
  * re-read the expert weights once per pass, column chunks re-read the
  * activation operand). This function returns the tokens per token chunk.

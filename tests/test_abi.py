@@ -36,7 +36,10 @@ def test_every_declared_symbol_is_exported(lib):
 def test_host_functions():
     from token_dispatch_grouped_gb300 import binding as B
     s = B.shape(4096, 4096, 8, 2, 14336)
-    assert B.moe_chunk_tokens(s) == 1024
+    assert B.moe_chunk_tokens(s) == 2048       # T*K*d = 32 MiB: two token chunks
+    assert B.moe_chunk_tokens(B.shape(32768, 2048, 128, 8, 768)) == 8192  # 512 MiB: four
+    assert B.moe_chunk_tokens(B.shape(8192, 2048, 8, 4, 8192)) == 4096    # exactly 64 MiB: two
+    assert B.moe_chunk_tokens(B.shape(512, 256, 8, 2, 256)) == 512        # T < 1024: one
     fwd = B.moe_workspace_size(s, B.MOE_WS_FORWARD)
     # the forward workspace holds the SwiGLU output [TK, h] and one Y chunk:
     # two column passes here (the half-width chunk is 32 MiB), so half of the

@@ -108,8 +108,8 @@ int nchunks_of(const moe_shape& s, int tc) { return (s.T + tc - 1) / tc; }
 
 // How a down projection (forward) or dX pass (backward) is split so that its
 // transient [rows, columns] output buffer holds at most a quarter of T*K*d
-// once T >= 1024 (half of it for column passes of small layers, see
-// column_passes). Splitting by token chunks streams the expert weights once
+// once T >= 1024 (half of it on small layers, see column_passes and
+// moe_chunk_tokens). Splitting by token chunks streams the expert weights once
 // per chunk; splitting by output-column chunks streams the activation
 // operand once per chunk instead. The split that re-reads fewer bytes wins.
 struct Plan {
@@ -631,7 +631,11 @@ extern "C" {
 
 int moe_chunk_tokens(moe_shape s) {
     if (s.T < 1024) return std::max(1, s.T);
-    return (s.T + 3) / 4;
+    // Two chunks when their buffer (T/2 tokens x K rows x d, bf16) is at most
+    // 64 MiB, as for column passes; four otherwise.
+    const long long half_bytes = static_cast<long long>(s.T) * s.K * s.d;
+    const int n = half_bytes <= (64ll << 20) ? 2 : 4;
+    return (s.T + n - 1) / n;
 }
 
 size_t moe_workspace_size(moe_shape s, int which) {
