@@ -53,15 +53,16 @@ SMALL = [
     I.WORKLOADS["tiny"],
     I.Shape(300, 256, 6, 3, 384),     # ragged tiles, h % 256 != 0 (128-wide N tiles)
     I.Shape(1, 128, 4, 4, 128),       # one token, K = E
-    I.Shape(1500, 128, 16, 1, 256),   # K = 1 (router gradient is zero), 4 token chunks
+    I.Shape(1500, 128, 16, 1, 256),   # K = 1 (router gradient is zero), 2 token chunks
     I.Shape(129, 384, 8, 8, 128),     # K = E = 8
     I.Shape(1100, 512, 8, 2, 256),    # passes split by output columns (d % 512 == 0)
     I.Shape(2100, 512, 4, 2, 512),    # ~1000 rows per expert: CTA-pair (M = 256) tiles
     # non-gated two-layer experts (SiLU / ReLU), no W3
     I.Shape(300, 256, 6, 3, 512, "silu"),    # ragged tiles, two 256-wide up tiles
-    I.Shape(1500, 128, 16, 1, 256, "relu"),  # K = 1, 4 token chunks
+    I.Shape(1500, 128, 16, 1, 256, "relu"),  # K = 1, 2 token chunks
     I.Shape(1100, 512, 8, 2, 768, "relu"),   # column-split passes, three up tiles
     I.Shape(2100, 512, 4, 2, 256, "silu"),   # CTA-pair down / dX GEMMs
+    I.Shape(1200, 2048, 4, 2, 512, "silu"),  # CTA pairs at d = 2048: 128-deep dH stages
 ]
 
 

@@ -104,16 +104,19 @@ template <> struct Tr<G7_DWG> : Tr<G4_DW2> {};  // gathered x (MN-major A), B ro
 // GB300 with a probe of this kernel's feed (cp.async of 128 gathered rows plus
 // a TMA box per stage, one CTA per SM), 80 GB/s per SM with 32 KB stages
 // against 143 GB/s with 64 KB stages. CTA pairs of the up projection, the
-// weight gradients and dX take 128 (three 64 KB stages); the dH GEMM keeps 64,
-// since its epilogue's H ring would leave room for two 128-deep stages only
-// (measured 15-29% slower that way), and the down projections keep 64 (no
-// gain measured). A stage holds BK / BK0 sub-blocks of 64 K elements: K-major
+// weight gradients and dX take 128 (three 64 KB stages). The non-gated dH
+// GEMM takes 128 (DEEP, with a two-slot H ring) when d >= 2048: measured 9-11%
+// faster at d = 2048, but 5-10% slower at d = 512 and 1024, where its few
+// k-blocks per tile leave the epilogue's shorter H prefetch exposed. The
+// SwiGLU dH GEMM keeps 64, since its epilogue's H ring (a and b boxes) would
+// leave room for two 128-deep stages only (measured 15-29% slower that way),
+// and the down projections keep 64 (no gain measured). A stage holds BK / BK0 sub-blocks of 64 K elements: K-major
 // operands as [rows x 64] tiles one after the other, MN-major operands as
 // 64-column chunks of BK rows.
-template <GemmKind KIND, int CTAS>
+template <GemmKind KIND, int CTAS, bool DEEP = false>
 __host__ __device__ constexpr int bk_of() {
-    return CTAS == 2 && (KIND == G1_UP || KIND == G1_UP_ACT || KIND == G4_DW2 ||
-                         KIND == G5_DW13 || KIND == G6_DX || KIND == G7_DWG)
+    return (CTAS == 2 && (DEEP || KIND == G1_UP || KIND == G1_UP_ACT || KIND == G4_DW2 ||
+                          KIND == G5_DW13 || KIND == G6_DX || KIND == G7_DWG))
                ? 128
                : 64;
 }
@@ -147,14 +150,20 @@ struct Cfg {
 
 constexpr int kGatherThreads = 128;
 // G3 epilogue: chunks of H (32 rows x 32 columns of a, and of b when gated) are
-// loaded by TMA into a ring of kHR shared slots per warp, kHR - 1 chunks ahead.
-constexpr int kHR = 3;
-static_assert(768 + 8 * 4 * kHR <= 1024, "H-ring barriers");
+// loaded by TMA into a ring of hr_of slots per warp, one slot fewer chunks
+// ahead: three slots for SwiGLU (a and b boxes), two for non-gated experts (a
+// alone), which leaves the shared memory for three 128-deep stages.
+template <GemmKind KIND, bool DEEP = false>
+__host__ __device__ constexpr int hr_of() {
+    return KIND == G3_DH_ACT && DEEP ? 2 : 3;
+}
+constexpr int kHRMax = 3;
+static_assert(768 + 8 * 4 * kHRMax <= 1024, "H-ring barriers");
 // Shared 2 KB staging boxes per epilogue warp: two for the stored outputs; for
 // G3 the H ring (whose boxes are rewritten in place as dH) plus one box for A'.
-template <GemmKind KIND>
+template <GemmKind KIND, bool DEEP = false>
 __host__ __device__ constexpr int epi_boxes() {
-    return KIND == G3_DH ? 2 * kHR + 1 : KIND == G3_DH_ACT ? kHR + 1 : 2;
+    return KIND == G3_DH ? 2 * hr_of<KIND>() + 1 : KIND == G3_DH_ACT ? hr_of<KIND, DEEP>() + 1 : 2;
 }
 template <GemmKind KIND, int CTAS>
 constexpr int threads_of() {
@@ -424,14 +433,14 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > kWaitNs) break;
 }
 
-template <GemmKind KIND, int BN, int CTAS>
+template <GemmKind KIND, int BN, int CTAS, bool DEEP>
 __global__ void __launch_bounds__(threads_of<KIND, CTAS>(), 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB0,
                     const __grid_constant__ CUtensorMap mapB1,
                     const __grid_constant__ CUtensorMap mapO, const Params p) {
     using TR = Tr<KIND>;
-    using C = Cfg<BN, CTAS, epi_boxes<KIND>(), bk_of<KIND, CTAS>()>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND, DEEP>(), bk_of<KIND, CTAS, DEEP>()>;
     constexpr bool VK = TR::VK;
     constexpr bool PAIR = CTAS == 2;
     constexpr int BMC = BM * CTAS;  // rows per tile
@@ -439,6 +448,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
     constexpr int BNL = C::BNL;     // N columns whose B rows this CTA stages
     constexpr int BK = C::BK;
     constexpr int KSUB = C::KSUB;
+    constexpr int kHR = hr_of<KIND, DEEP>();  // G3: slots of this warp's H ring
     constexpr uint32_t IDESC = idesc_bf16(BMC, NMMA, TR::A_MN, TR::B_MN);
     // Half-height pair tiles (see half_ok): M = 128 over the pair, 64 rows per CTA.
     constexpr bool HALF = PAIR && !VK && half_ok<KIND>();
@@ -754,7 +764,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap mapA,
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* stg = epi + (warp - 2) * epi_boxes<KIND>() * 2048;  // this warp's boxes
+        uint8_t* stg = epi + (warp - 2) * epi_boxes<KIND, DEEP>() * 2048;  // this warp's boxes
         int nstore = 0;                           // TMA stores issued by this warp
         // G3: this warp's H ring. Slot s holds box a (and box b when gated) of one
         // chunk; the A' box follows the ring; hc counts the chunks consumed.
@@ -1340,12 +1350,12 @@ struct Maps {
     CUtensorMap a, b0, b1, o;
 };
 
-template <GemmKind KIND, int BN, int CTAS>
+template <GemmKind KIND, int BN, int CTAS, bool DEEP = false>
 cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
                         const char* name) {
     const bool pdl = pdl_enabled(true);
-    using C = Cfg<BN, CTAS, epi_boxes<KIND>(), bk_of<KIND, CTAS>()>;
-    auto kfn = grouped_gemm_kernel<KIND, BN, CTAS>;
+    using C = Cfg<BN, CTAS, epi_boxes<KIND, DEEP>(), bk_of<KIND, CTAS, DEEP>()>;
+    auto kfn = grouped_gemm_kernel<KIND, BN, CTAS, DEEP>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
@@ -1370,7 +1380,12 @@ cudaError_t launch_kind(const Maps& mp, const Params& prm, int max_tiles, cudaSt
 
 template <GemmKind KIND, int CTAS>
 cudaError_t launch_bn(int BN, const Maps& mp, const Params& prm, int max_tiles, cudaStream_t st,
-                      const char* name) {
+                      const char* name, bool deep) {
+    if constexpr (KIND == G3_DH_ACT && CTAS == 2) {
+        if (deep)
+            return BN == 256 ? launch_kind<KIND, 256, CTAS, true>(mp, prm, max_tiles, st, name)
+                             : launch_kind<KIND, 128, CTAS, true>(mp, prm, max_tiles, st, name);
+    }
     if constexpr (KIND == G1_UP || KIND == G1_UP_ACT) {
         return launch_kind<KIND, 256, CTAS>(mp, prm, max_tiles, st, name);
     } else {
@@ -1381,9 +1396,9 @@ cudaError_t launch_bn(int BN, const Maps& mp, const Params& prm, int max_tiles, 
 
 template <GemmKind KIND>
 cudaError_t launch_ctas(int ctas, int BN, const Maps& mp, const Params& prm, int max_tiles,
-                        cudaStream_t st, const char* name) {
-    return ctas == 2 ? launch_bn<KIND, 2>(BN, mp, prm, max_tiles, st, name)
-                     : launch_bn<KIND, 1>(BN, mp, prm, max_tiles, st, name);
+                        cudaStream_t st, const char* name, bool deep = false) {
+    return ctas == 2 ? launch_bn<KIND, 2>(BN, mp, prm, max_tiles, st, name, deep)
+                     : launch_bn<KIND, 1>(BN, mp, prm, max_tiles, st, name, deep);
 }
 
 // CTA pairs halve each SM's share of the B tile (more stages in flight, half
@@ -1610,7 +1625,8 @@ cudaError_t launch_gemm_ctas(const GemmProblem& g, int ctas, cudaStream_t st) {
         case G2_SLOT: return launch_ctas<G2_SLOT>(ctas, BN, mp, prm, max_tiles, st, "g2_slot");
         case G3_DH:
             return gated ? launch_ctas<G3_DH>(ctas, BN, mp, prm, max_tiles, st, "g3_dh")
-                         : launch_ctas<G3_DH_ACT>(ctas, BN, mp, prm, max_tiles, st, "g3_dh_act");
+                         : launch_ctas<G3_DH_ACT>(ctas, BN, mp, prm, max_tiles, st, "g3_dh_act",
+                                                  s.d >= 2048);
         case G4_DW2: return launch_ctas<G4_DW2>(ctas, BN, mp, prm, max_tiles, st, "g4_dw2");
         case G5_DW13: return launch_ctas<G5_DW13>(ctas, BN, mp, prm, max_tiles, st, "g5_dw13");
         case G6_DX: return launch_ctas<G6_DX>(ctas, BN, mp, prm, max_tiles, st, "g6_dx");
