@@ -585,3 +585,25 @@ def test_programmatic_launch_modes_are_bit_identical(s, monkeypatch):
     for mode in ("1", "0", "small"):
         for a, b in zip(outs[None], outs[mode]):
             assert torch.equal(a, b), mode
+
+
+# Tile order of the row-tiled GEMMs: every output element is computed by one tile
+# with a fixed reduction order, so grouping an expert's M tiles (MOE_GEMM_GROUP_MB)
+# moves work between CTAs but must leave every bit of every output in place.
+# 2100 tokens x K = 2 over 4 experts: 4-5 M tiles of 256 rows per expert; a 1 MiB
+# budget groups them by 4 (d = 512: 256 KB of A per tile), 0 walks M fastest.
+@pytest.mark.parametrize("s", [I.Shape(2100, 512, 4, 2, 512), I.Shape(2100, 512, 4, 2, 256, "silu")],
+                         ids=_sid)
+def test_row_tile_order_is_bit_identical(s, monkeypatch):
+    inp = to_dev(I.make_layer_inputs(s, seed=13))
+    L = _layer(s)
+    outs = {}
+    for mb in ("0", "1", "32"):
+        monkeypatch.setenv("MOE_GEMM_GROUP_MB", mb)
+        r, dp, y, H, g = L.step(inp["x"], inp["Wg"], inp["W1"], inp["W3"], inp["W2"], inp["dO"])
+        L.check_error()
+        outs[mb] = [t.clone() for t in (y, H, *g.values()) if t is not None]
+    monkeypatch.delenv("MOE_GEMM_GROUP_MB")
+    for mb in ("1", "32"):
+        for a, b in zip(outs["0"], outs[mb]):
+            assert torch.equal(a, b), mb
