@@ -96,7 +96,7 @@ PEAK_RULE = ("the burst bf16 peak applies when the timed region is shorter than 
 
 
 def choose_bf16_peak(peaks: dict, timed_ms: float, clk: dict) -> tuple[float, str]:
-    """The measured bf16 peak that a timed region is judged against: the burst
+    """The measured bf16 peak that a timed region is compared against: the burst
     figure for a short region or one that ran at full clock, the sustained
     figure (a seconds-long loop under the power cap) otherwise."""
     sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
