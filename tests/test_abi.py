@@ -196,3 +196,21 @@ def test_dispatch_entry_points_share_host_checks():
     ok = B.shape(16, 128, 8, 2, 128)
     assert B.LIB.moe_build_dispatch_noalloc(ok, None, None, None, None, None) == \
         B.MOE_ERR_INVALID_ARG
+
+
+def test_forward_buffer_never_holds_the_routed_buffer():
+    """For every workload, the forward workspace beyond the [T*K, h] activation
+    output (the down-projection chunk buffer and the segment tables) stays within
+    half of the T*K*d bf16 routed buffer once T >= 1024 -- a quarter when that
+    half exceeds 64 MiB -- so the routed buffer itself is never allocated."""
+    from token_dispatch_grouped_gb300 import binding as B
+    from token_dispatch_grouped_gb300 import inputs as I
+    for name, s in I.WORKLOADS.items():
+        if s.T < 1024:
+            continue
+        sh = B.shape(s.T, s.d, s.E, s.K, s.h, s.expert)
+        TK = s.T * s.K
+        routed = TK * s.d * 2
+        extra = B.moe_workspace_size(sh, B.MOE_WS_FORWARD) - TK * s.h * 2
+        bound = routed // 2 if routed // 2 <= 64 * 2**20 else routed // 4
+        assert 0 < extra <= bound + 2**20, (name, extra, bound)
